@@ -1,0 +1,169 @@
+"""Reference model of the host block manager (free list, refcounts, fork, CoW).
+
+Sources:
+* "PagedAttention vs Traditional KV Cache", Section 4 "PagedAttention: How It
+  Works": a free list of block ids (allocation pops from it and fails when it
+  is empty - the caller then preempts), a per-sequence block table, and
+  appending a token allocates a new block only when the last one is full.
+* "Inference serving: the KV-cache machine", section "Paged KV: virtual memory
+  for tokens" and Lab B's BlockPool: blocks carry a reference count; a block
+  returns to the pool only when its count reaches zero; fork makes the child
+  table alias the parent's blocks (incref each), and the first divergent token
+  gets a private block.
+* "Modern AI Infrastructure and Agentic System Design", 9.1, copy-on-write
+  figure: three tables share b0..b2 (refcount 3); a write to a shared block
+  first copies it into a fresh block.
+
+Readings taken where the pages are silent or disagree:
+* The first page's free_sequence returns every block to the free list, which
+  would free blocks still shared by a sibling; the refcounted release of the
+  other two pages is followed instead.
+* refcount = number of block tables that reference the block.
+* Appending into a partially filled last block whose refcount > 1 copies it
+  first (copy pair emitted, src decref'd, table repointed). If the shared last
+  block is full, the new token simply starts a new private block.
+* ``make_private`` forces the copy of any shared block of a sequence (used to
+  model a divergent overwrite of an already full block).
+* An append of n tokens is all-or-nothing: if the free list cannot supply
+  every block it needs, nothing changes and OutOfBlocks is raised.
+* Allocation order (LIFO pop) is not part of any result the tests compare.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Tuple
+
+
+class OutOfBlocks(Exception):
+    pass
+
+
+class BlockManagerError(Exception):
+    pass
+
+
+class BlockManagerModel:
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        if num_blocks < 0 or block_size <= 0:
+            raise BlockManagerError("bad sizes")
+        self.block_size = block_size
+        self.free: List[int] = list(range(num_blocks))
+        self.ref: List[int] = [0] * num_blocks
+        self.tables: Dict[int, List[int]] = {}
+        self.lens: Dict[int, int] = {}
+
+    # -- allocation primitives ---------------------------------------------
+    def _alloc(self) -> int:
+        if not self.free:
+            raise OutOfBlocks()
+        b = self.free.pop()
+        assert self.ref[b] == 0
+        self.ref[b] = 1
+        return b
+
+    def _put(self, b: int) -> None:
+        if self.ref[b] <= 0:
+            raise BlockManagerError("refcount underflow")
+        self.ref[b] -= 1
+        if self.ref[b] == 0:
+            self.free.append(b)
+
+    # -- sequence operations -----------------------------------------------
+    def add_seq(self, seq_id: int) -> None:
+        if seq_id in self.tables:
+            raise BlockManagerError("sequence exists")
+        self.tables[seq_id] = []
+        self.lens[seq_id] = 0
+
+    def _blocks_needed(self, seq_id: int, n: int) -> int:
+        bs = self.block_size
+        L = self.lens[seq_id]
+        tab = self.tables[seq_id]
+        need = 0
+        if n > 0 and L % bs != 0 and self.ref[tab[-1]] > 1:
+            need += 1                                   # copy-on-write of the tail
+        have_slots = len(tab) * bs - L
+        extra = n - have_slots
+        if extra > 0:
+            need += (extra + bs - 1) // bs
+        return need
+
+    def append_tokens(self, seq_id: int, n: int) -> Tuple[List[int], List[Tuple[int, int]]]:
+        """Append n tokens; returns (slots, cow_pairs)."""
+        if seq_id not in self.tables:
+            raise BlockManagerError("unknown sequence")
+        if n < 0:
+            raise BlockManagerError("negative count")
+        if self._blocks_needed(seq_id, n) > len(self.free):
+            raise OutOfBlocks()
+        bs = self.block_size
+        tab = self.tables[seq_id]
+        slots: List[int] = []
+        cow: List[Tuple[int, int]] = []
+        for _ in range(n):
+            L = self.lens[seq_id]
+            if L % bs == 0 and L // bs == len(tab):
+                tab.append(self._alloc())
+            else:
+                last = tab[L // bs]
+                if self.ref[last] > 1:
+                    fresh = self._alloc()
+                    cow.append((last, fresh))
+                    self._put(last)
+                    tab[L // bs] = fresh
+            slots.append(tab[L // bs] * bs + L % bs)
+            self.lens[seq_id] = L + 1
+        return slots, cow
+
+    def make_private(self, seq_id: int, logical_block: int) -> List[Tuple[int, int]]:
+        tab = self.tables[seq_id]
+        b = tab[logical_block]
+        if self.ref[b] <= 1:
+            return []
+        fresh = self._alloc()
+        self._put(b)
+        tab[logical_block] = fresh
+        return [(b, fresh)]
+
+    def fork(self, parent: int, child: int) -> None:
+        if parent not in self.tables:
+            raise BlockManagerError("unknown parent")
+        if child in self.tables:
+            raise BlockManagerError("child exists")
+        self.tables[child] = list(self.tables[parent])
+        self.lens[child] = self.lens[parent]
+        for b in self.tables[child]:
+            self.ref[b] += 1
+
+    def free_seq(self, seq_id: int) -> None:
+        if seq_id not in self.tables:
+            raise BlockManagerError("unknown sequence")
+        for b in self.tables.pop(seq_id):
+            self._put(b)
+        del self.lens[seq_id]
+
+    # -- queries -----------------------------------------------------------
+    def block_table(self, seq_id: int) -> List[int]:
+        return list(self.tables[seq_id])
+
+    def seq_len(self, seq_id: int) -> int:
+        return self.lens[seq_id]
+
+    def num_free(self) -> int:
+        return len(self.free)
+
+    def refcount(self, block: int) -> int:
+        return self.ref[block]
+
+    def check_invariants(self) -> None:
+        """Sum of refcounts == sum of table lengths; a block is free iff its
+        refcount is 0; every table covers exactly ceil(len / bs) blocks."""
+        total_refs = sum(self.ref)
+        total_entries = sum(len(t) for t in self.tables.values())
+        assert total_refs == total_entries, (total_refs, total_entries)
+        free = set(self.free)
+        assert len(free) == len(self.free), "duplicate free entry"
+        for b, r in enumerate(self.ref):
+            assert (r == 0) == (b in free), (b, r)
+        bs = self.block_size
+        for s, t in self.tables.items():
+            assert len(t) == (self.lens[s] + bs - 1) // bs
