@@ -1,0 +1,259 @@
+/*
+ * pagedkv.h - C ABI of libpagedkv.so: PagedAttention decode over a paged
+ * bf16 KV cache on NVIDIA GB300 (sm_103a), the two kernels that keep the
+ * cache valid, a chunked causal prefill over the same cache, and a host-side
+ * block manager that builds the tables.
+ *
+ * Sources (page title, section):
+ *  [PA]  "PagedAttention vs Traditional KV Cache: How vLLM Reinvented GPU
+ *        Memory for LLM Inference", Section 4 "PagedAttention: How It Works".
+ *  [LD]  "LLM Inference Optimization: KV-Cache, PagedAttention, and GPU
+ *        Memory Efficiency", section "PagedAttention: OS Concepts Meet GPU
+ *        Memory" (block table, kernel outline, copy-on-write).
+ *  [KE]  "KV Cache Explained Like You're an LLM Engineer", sections
+ *        "Transformer Attention: A Quick Refresher", "What KV Cache Stores",
+ *        "Prefill Phase vs. Decode Phase".
+ *  [MA]  "Modern AI Infrastructure and Agentic System Design", 9.1 "The key
+ *        and value cache" (closed form, copy-on-write figure), "Two workloads
+ *        wearing one name" (chunked prefill).
+ *  [DR]  "Inference serving: the KV-cache machine", sections "Paged KV:
+ *        virtual memory for tokens" and "Continuous batching: the server as
+ *        an allocator".
+ *
+ * Common conventions
+ *  - Every pointer argument of pa_decode, pa_reshape_and_cache, pa_copy_blocks
+ *    and pa_prefill_paged is DEVICE memory owned by the caller, 16-byte
+ *    aligned; bf16 tensors are raw 16-bit patterns. The library allocates no
+ *    device memory in these calls; it owns only a 4-byte device error word
+ *    per device.
+ *  - KV pool layout: k_pool and v_pool are bf16
+ *        [num_blocks][n_kv_heads][block_size][head_dim]
+ *    so that one (block, kv-head) tile - block_size tokens of one head - is a
+ *    contiguous block_size*head_dim*2 bytes. block_size must be 16 (the
+ *    pages' block size), head_dim 64 or 128, n_heads a multiple of
+ *    n_kv_heads with group n_heads/n_kv_heads in {1, 2, 4, 8}; query head h
+ *    reads KV head h / (n_heads / n_kv_heads).
+ *  - A slot is physical_block * block_size + offset ([LD]: logical position p
+ *    lives at table[p / block_size], offset p % block_size).
+ *  - All kernels run asynchronously on `stream` (NULL = legacy default
+ *    stream). Argument errors are returned synchronously and nothing is
+ *    launched. A launch failure returns PA_ERR_CUDA. Faults the kernels can
+ *    detect only on the device (a block id or slot outside the pool, a wait
+ *    that timed out) skip the offending work and set a bit in the device
+ *    error word, read and cleared with pa_get_device_error().
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t; /* same type as cudaStream_t */
+
+enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1, /* null/misaligned pointer, negative size, ... */
+    PA_ERR_UNSUPPORTED = -2, /* valid but not built: head_dim, block_size, group */
+    PA_ERR_WORKSPACE = -3,   /* workspace missing or too small */
+    PA_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
+    PA_ERR_DEVICE = -5,      /* device error word was non-zero */
+    PA_ERR_OOM = -6,         /* block manager: free list cannot supply the blocks */
+    PA_ERR_REFCOUNT = -7,    /* block manager: unknown sequence / refcount misuse */
+    PA_ERR_CAPACITY = -8     /* an output buffer given by the caller is too small */
+};
+
+/* Bits of the device error word. */
+enum pa_device_error {
+    PA_DEVERR_BLOCK_ID = 1, /* a block-table entry outside [0, num_blocks) */
+    PA_DEVERR_SLOT = 2,     /* a slot >= num_blocks * block_size */
+    PA_DEVERR_TIMEOUT = 4,  /* an mbarrier / async-copy wait ran out */
+    PA_DEVERR_PAIR = 8,     /* a copy_blocks pair outside the pool */
+    PA_DEVERR_CONTEXT = 16  /* a context length beyond 16*max_blocks_per_seq or
+                               max_context_len (the excess is not attended) */
+};
+
+/* ------------------------------------------------------------------ decode */
+
+/*
+ * Workspace bytes pa_decode needs for this batch shape (0 when every context
+ * fits in one partition, in which case workspace may be NULL). The workspace
+ * holds fp32 split-K partials: running max m and sum l per (seq, q-head,
+ * partition) and the unnormalised output per (seq, q-head, partition, dim).
+ * partition_tokens: tokens per context partition, a multiple of 64 in
+ * [64, 2048]; 0 selects the library default.
+ */
+size_t pa_decode_workspace_bytes(int n_seqs, int n_heads, int head_dim,
+                                 int max_context_len, int partition_tokens);
+
+/*
+ * PagedAttention decode ([LD] kernel outline; [KE] attention formula):
+ * for every sequence b and query head h,
+ *     out[b][h][:] = softmax_t( scale * q[b][h] . K_b[t] ) . V_b[t],
+ *                    t = 0 .. context_lens[b]-1,
+ * where K_b[t] / V_b[t] is token t of sequence b, stored in physical block
+ * block_tables[b][t / 16] at offset t % 16, for KV head h / group.
+ *
+ *  out            bf16 [n_seqs][n_heads][head_dim]   (written; must not alias q)
+ *  q              bf16 [n_seqs][n_heads][head_dim]
+ *  k_pool, v_pool bf16 pool layout above (read only)
+ *  block_tables   int32 [n_seqs][max_blocks_per_seq]; entries past
+ *                 ceil(context_lens[b]/16) are never read
+ *  context_lens   int32 [n_seqs]: valid tokens of each sequence, including
+ *                 any token written this step; <= 0 gives a zero output row;
+ *                 must be <= max_context_len and <= 16*max_blocks_per_seq
+ *  scale          softmax scale (typically 1/sqrt(head_dim))
+ *  max_context_len upper bound of context_lens (sizes the partition grid)
+ *  num_blocks     pool size in blocks (bounds check of table entries)
+ *  workspace      device scratch of >= pa_decode_workspace_bytes(...) bytes,
+ *                 caller-owned; contents need no initialisation
+ * Arithmetic: bf16 inputs, fp32 dot products, fp32 online softmax (base-2
+ * exponent with scale*log2(e) folded into q), fp32 split-K merge, bf16 output
+ * rounded to nearest even.
+ */
+int pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+              const int32_t* block_tables, const int32_t* context_lens, float scale,
+              int n_heads, int n_kv_heads, int head_dim, int block_size,
+              int n_seqs, int max_blocks_per_seq, int max_context_len, int num_blocks,
+              void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* pa_decode with an explicit partition size (see pa_decode_workspace_bytes). */
+int pa_decode_ex(void* out, const void* q, const void* k_pool, const void* v_pool,
+                 const int32_t* block_tables, const int32_t* context_lens, float scale,
+                 int n_heads, int n_kv_heads, int head_dim, int block_size,
+                 int n_seqs, int max_blocks_per_seq, int max_context_len, int num_blocks,
+                 int partition_tokens, void* workspace, size_t workspace_bytes,
+                 pa_stream_t stream);
+
+/* --------------------------------------------------------- cache upkeep */
+
+/*
+ * reshape_and_cache ([KE] "What KV Cache Stores": append the new token's K/V;
+ * [DR] slot = table[p / 16], offset p % 16): for t < n_tokens with
+ * slot_mapping[t] >= 0, copy k[t][h][:] to k_pool[slot/16][h][slot%16][:] and
+ * v[t][h][:] to v_pool likewise, for every KV head h. Bit copy.
+ *  k, v          bf16 [n_tokens][n_kv_heads][head_dim]
+ *  slot_mapping  int64 [n_tokens]; negative = skip (padding);
+ *                >= num_blocks*16 sets PA_DEVERR_SLOT and is skipped
+ * Two tokens naming the same slot race (one of them wins).
+ */
+int pa_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+                         const int64_t* slot_mapping, int n_tokens, int n_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_stream_t stream);
+
+/*
+ * copy_blocks ([MA] copy-on-write figure; [LD] only the diverging block is
+ * copied): for each pair i, the whole block block_mapping[2i] (all KV heads,
+ * all 16 slots) is copied to block block_mapping[2i+1], in k_pool and v_pool.
+ * Bit copy. Destinations must be distinct and must not be sources of other
+ * pairs. A pair outside [0, num_blocks) sets PA_DEVERR_PAIR and is skipped.
+ *  block_mapping int64 [n_pairs][2] (src, dst), device memory
+ */
+int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs,
+                   int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                   pa_stream_t stream);
+
+/* ------------------------------------------------------- chunked prefill */
+
+/*
+ * Causal attention of prompt chunks over the paged cache ([MA] "Two workloads
+ * wearing one name": chunked prefill; [KE] "Prefill Phase vs. Decode Phase").
+ * Sequence s owns query rows q_start_loc[s] .. q_start_loc[s+1]-1 (L_s rows);
+ * its chunk occupies the last L_s of its context_lens[s] tokens, which must
+ * already be in the cache (write them with pa_reshape_and_cache first). Row
+ * i of the chunk sits at position p = context_lens[s] - L_s + i and attends to
+ * positions 0..p:
+ *     out[r][h][:] = softmax_{t<=p}( scale * q[r][h] . K_s[t] ) . V_s[t].
+ *  out, q        bf16 [q_start_loc[n_seqs]][n_heads][head_dim]
+ *  q_start_loc   int32 [n_seqs+1], non-decreasing, q_start_loc[0] = 0
+ *  context_lens  int32 [n_seqs], >= L_s
+ *  max_chunk_len upper bound of L_s
+ * head_dim must be 128 and the group n_heads/n_kv_heads 1, 2, 4 or 8.
+ * QK^T and PV run on the tcgen05 tensor cores (bf16 in, fp32 accumulate in
+ * tensor memory); softmax in fp32.
+ */
+int pa_prefill_paged(void* out, const void* q, const void* k_pool, const void* v_pool,
+                     const int32_t* block_tables, const int32_t* context_lens,
+                     const int32_t* q_start_loc, float scale, int n_heads, int n_kv_heads,
+                     int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
+                     int max_chunk_len, int num_blocks, pa_stream_t stream);
+
+/* ----------------------------------------------------------- diagnostics */
+
+/* Reads the current device's error word into *flags_out (a PA_DEVERR_* mask)
+ * and clears it. Synchronises with the device. */
+int pa_get_device_error(int* flags_out);
+
+/* Static string for a status code. */
+const char* pa_status_string(int status);
+
+/* ------------------------------------------------------ host block manager */
+/*
+ * Builds block tables, slot mappings and copy-on-write pairs on the host
+ * ([PA] free list and append-allocates-on-full; [DR] refcounts, fork aliasing,
+ * copy-on-write; [MA] copy-on-write figure). Not thread-safe; one manager per
+ * pool. refcount(b) = number of block tables that reference block b; a block
+ * returns to the free list when its refcount reaches 0. Allocation pops the
+ * most recently freed block (LIFO). Every call that can fail is all-or-nothing.
+ */
+typedef struct pa_bm pa_bm;
+
+/* NULL on bad sizes or allocation failure. */
+pa_bm* pa_bm_create(int num_blocks, int block_size);
+void pa_bm_destroy(pa_bm* bm);
+
+/* New empty sequence. PA_ERR_REFCOUNT if seq_id exists. */
+int pa_bm_add_seq(pa_bm* bm, int64_t seq_id);
+
+/*
+ * Appends n tokens to seq_id. slots_out[0..n) receives each token's slot.
+ * If the sequence's last block is partially filled and shared (refcount > 1),
+ * it is first copied: a fresh block replaces it in this table, the old one is
+ * decref'd, and the pair (old, fresh) is written to cow_pairs_out (int64
+ * [cap][2]); *n_cow_out receives the number of pairs (0 or 1). New blocks are
+ * taken from the free list when the last block is full. PA_ERR_OOM (no state
+ * change) if the free list cannot supply every block needed; PA_ERR_CAPACITY
+ * if cow_cap < 1 and a copy would be needed.
+ */
+int pa_bm_append_tokens(pa_bm* bm, int64_t seq_id, int n, int64_t* slots_out,
+                        int64_t* cow_pairs_out, int cow_cap, int* n_cow_out);
+
+/* Forces logical block `logical_block` of seq_id to be private: if shared it is
+ * copied to a fresh block (pair written to pair_out[2], *n_out = 1), else
+ * *n_out = 0. */
+int pa_bm_make_private(pa_bm* bm, int64_t seq_id, int logical_block, int64_t* pair_out,
+                       int* n_out);
+
+/* child's table aliases parent's blocks; each block's refcount += 1. */
+int pa_bm_fork(pa_bm* bm, int64_t parent, int64_t child);
+
+/* Drops seq_id; each of its blocks is decref'd and freed at refcount 0. */
+int pa_bm_free_seq(pa_bm* bm, int64_t seq_id);
+
+/* Copies seq_id's table into out[0..cap); *n_out = its length. PA_ERR_CAPACITY
+ * (with *n_out set) if cap is too small. */
+int pa_bm_block_table(const pa_bm* bm, int64_t seq_id, int32_t* out, int cap, int* n_out);
+
+/* Number of tokens held by seq_id, or a negative status. */
+int64_t pa_bm_seq_len(const pa_bm* bm, int64_t seq_id);
+
+int pa_bm_num_free(const pa_bm* bm);
+/* Refcount of block_id, or a negative status if out of range. */
+int pa_bm_refcount(const pa_bm* bm, int block_id);
+
+/*
+ * Fills a padded int32 [n][max_blocks] table array (row i = seq_ids[i]'s
+ * table, -1 padded) and int32 context_lens[n] for a batch, ready for a
+ * host->device copy. PA_ERR_CAPACITY if a table is longer than max_blocks.
+ */
+int pa_bm_build_batch(const pa_bm* bm, const int64_t* seq_ids, int n, int max_blocks,
+                      int32_t* tables_out, int32_t* context_lens_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

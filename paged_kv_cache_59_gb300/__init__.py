@@ -1,0 +1,222 @@
+"""Python binding of libpagedkv.so: PagedAttention decode over a paged bf16 KV
+cache on GB300, the cache-write and block-copy kernels, chunked prefill, and
+the host block manager.
+
+Argument marshalling only: each function reads sizes from tensor shapes,
+checks device, dtype and contiguity, and calls the C entry point of the same
+name on the current CUDA stream. Every computation runs in the library's
+CUDA kernels; a missing library or a CPU tensor is an error.
+
+Tensors: bf16 tensors may be torch.bfloat16 or int16/uint16 carrying bf16
+bits. Pools are [num_blocks][n_kv_heads][16][head_dim]; block tables int32
+[n_seqs][max_blocks]; context lengths int32 [n_seqs]; slots int64.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import List, Optional, Sequence, Tuple
+
+from . import _capi
+from ._capi import PagedKVError, check, load  # noqa: F401
+
+__all__ = [
+    "pa_decode", "pa_decode_workspace_bytes", "pa_reshape_and_cache", "pa_copy_blocks",
+    "pa_prefill_paged", "pa_get_device_error", "BlockManager", "load", "PagedKVError",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+_BF16_LIKE = None
+
+
+def _ptr(t, what: str, bf16: bool = False, dtype=None):
+    torch = _torch()
+    global _BF16_LIKE
+    if _BF16_LIKE is None:
+        _BF16_LIKE = {torch.bfloat16, torch.int16, getattr(torch, "uint16", torch.int16)}
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{what} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if bf16 and t.dtype not in _BF16_LIKE:
+        raise TypeError(f"{what} must hold bf16 (bfloat16 or 16-bit integer bits), got {t.dtype}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def pa_decode_workspace_bytes(n_seqs: int, n_heads: int, head_dim: int, max_context_len: int,
+                              partition_tokens: int = 0) -> int:
+    return int(load().pa_decode_workspace_bytes(n_seqs, n_heads, head_dim, max_context_len,
+                                                partition_tokens))
+
+
+def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,
+              max_context_len: int, workspace=None, partition_tokens: int = 0, stream=None) -> None:
+    """out[b][h] = softmax(scale * q[b][h] . K_b^T) V_b over each sequence's
+    paged K/V. q, out: [n_seqs][n_heads][head_dim]."""
+    torch = _torch()
+    n_seqs, n_heads, head_dim = q.shape
+    num_blocks, n_kv_heads, block_size, hd2 = k_pool.shape
+    if hd2 != head_dim or tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if block_tables.dim() != 2 or block_tables.shape[0] != n_seqs or context_lens.numel() != n_seqs:
+        raise ValueError("block_tables must be [n_seqs][max_blocks], context_lens [n_seqs]")
+    ws_ptr, ws_bytes = C.c_void_p(None), 0
+    if workspace is not None:
+        ws_ptr = _ptr(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().pa_decode_ex(
+        _ptr(out, "out", bf16=True), _ptr(q, "q", bf16=True), _ptr(k_pool, "k_pool", bf16=True),
+        _ptr(v_pool, "v_pool", bf16=True), _ptr(block_tables, "block_tables", dtype=torch.int32),
+        _ptr(context_lens, "context_lens", dtype=torch.int32), float(scale), n_heads, n_kv_heads,
+        head_dim, block_size, n_seqs, block_tables.shape[1], int(max_context_len), num_blocks,
+        int(partition_tokens), ws_ptr, ws_bytes, _stream(stream))
+    check("pa_decode", st)
+
+
+def pa_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, stream=None) -> None:
+    """Writes k[t], v[t] ([n_tokens][n_kv_heads][head_dim]) to slot_mapping[t]."""
+    torch = _torch()
+    n_tokens, n_kv_heads, head_dim = k.shape
+    num_blocks, hk2, block_size, hd2 = k_pool.shape
+    if (hk2, hd2) != (n_kv_heads, head_dim) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between k/v and the pools")
+    if slot_mapping.numel() != n_tokens:
+        raise ValueError("slot_mapping must have n_tokens entries")
+    st = load().pa_reshape_and_cache(
+        _ptr(k, "k", bf16=True), _ptr(v, "v", bf16=True), _ptr(k_pool, "k_pool", bf16=True),
+        _ptr(v_pool, "v_pool", bf16=True), _ptr(slot_mapping, "slot_mapping", dtype=torch.int64),
+        n_tokens, n_kv_heads, head_dim, block_size, num_blocks, _stream(stream))
+    check("pa_reshape_and_cache", st)
+
+
+def pa_copy_blocks(k_pool, v_pool, block_mapping, stream=None) -> None:
+    """block_mapping int64 [n][2] (src, dst) on the device: dst block := src block."""
+    torch = _torch()
+    num_blocks, n_kv_heads, block_size, head_dim = k_pool.shape
+    n_pairs = block_mapping.shape[0] if block_mapping.numel() else 0
+    st = load().pa_copy_blocks(
+        _ptr(k_pool, "k_pool", bf16=True), _ptr(v_pool, "v_pool", bf16=True),
+        _ptr(block_mapping, "block_mapping", dtype=torch.int64) if n_pairs else C.c_void_p(None),
+        n_pairs, n_kv_heads, head_dim, block_size, num_blocks, _stream(stream))
+    check("pa_copy_blocks", st)
+
+
+def pa_prefill_paged(out, q, k_pool, v_pool, block_tables, context_lens, q_start_loc,
+                     scale: float, max_chunk_len: int, stream=None) -> None:
+    """Causal attention of each sequence's chunk rows over its paged cache."""
+    torch = _torch()
+    n_rows, n_heads, head_dim = q.shape
+    num_blocks, n_kv_heads, block_size, hd2 = k_pool.shape
+    n_seqs = context_lens.numel()
+    if hd2 != head_dim or tuple(out.shape) != tuple(q.shape) or q_start_loc.numel() != n_seqs + 1:
+        raise ValueError("shape mismatch in pa_prefill_paged arguments")
+    st = load().pa_prefill_paged(
+        _ptr(out, "out", bf16=True), _ptr(q, "q", bf16=True), _ptr(k_pool, "k_pool", bf16=True),
+        _ptr(v_pool, "v_pool", bf16=True), _ptr(block_tables, "block_tables", dtype=torch.int32),
+        _ptr(context_lens, "context_lens", dtype=torch.int32),
+        _ptr(q_start_loc, "q_start_loc", dtype=torch.int32), float(scale), n_heads, n_kv_heads,
+        head_dim, block_size, n_seqs, block_tables.shape[1], int(max_chunk_len), num_blocks,
+        _stream(stream))
+    check("pa_prefill_paged", st)
+
+
+def pa_get_device_error() -> int:
+    """Reads and clears the device error word (a PA_DEVERR_* mask)."""
+    v = C.c_int(0)
+    check("pa_get_device_error", load().pa_get_device_error(C.byref(v)))
+    return v.value
+
+
+class BlockManager:
+    """Host block manager (free list, refcounts, fork, copy-on-write) in the
+    library; builds block tables, slots and copy pairs."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        self._lib = load()
+        self._h = self._lib.pa_bm_create(num_blocks, block_size)
+        if not self._h:
+            raise ValueError("pa_bm_create failed")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.pa_bm_destroy(h)
+            self._h = None
+
+    def add_seq(self, seq_id: int) -> None:
+        check("pa_bm_add_seq", self._lib.pa_bm_add_seq(self._h, seq_id))
+
+    def append_tokens(self, seq_id: int, n: int) -> Tuple[List[int], List[Tuple[int, int]]]:
+        slots = (C.c_int64 * max(n, 1))()
+        pairs = (C.c_int64 * 2)()
+        ncow = C.c_int(0)
+        check("pa_bm_append_tokens", self._lib.pa_bm_append_tokens(
+            self._h, seq_id, n, slots, pairs, 1, C.byref(ncow)))
+        cow = [(pairs[0], pairs[1])] if ncow.value else []
+        return list(slots)[:n], cow
+
+    def make_private(self, seq_id: int, logical_block: int) -> List[Tuple[int, int]]:
+        pair = (C.c_int64 * 2)()
+        n = C.c_int(0)
+        check("pa_bm_make_private", self._lib.pa_bm_make_private(
+            self._h, seq_id, logical_block, pair, C.byref(n)))
+        return [(pair[0], pair[1])] if n.value else []
+
+    def fork(self, parent: int, child: int) -> None:
+        check("pa_bm_fork", self._lib.pa_bm_fork(self._h, parent, child))
+
+    def free_seq(self, seq_id: int) -> None:
+        check("pa_bm_free_seq", self._lib.pa_bm_free_seq(self._h, seq_id))
+
+    def block_table(self, seq_id: int) -> List[int]:
+        n = C.c_int(0)
+        st = self._lib.pa_bm_block_table(self._h, seq_id, None, 0, C.byref(n))
+        if st not in (_capi.PA_OK, _capi.PA_ERR_CAPACITY):
+            check("pa_bm_block_table", st)
+        buf = (C.c_int32 * max(n.value, 1))()
+        check("pa_bm_block_table", self._lib.pa_bm_block_table(self._h, seq_id, buf, n.value,
+                                                               C.byref(n)))
+        return list(buf)[:n.value]
+
+    def seq_len(self, seq_id: int) -> int:
+        v = self._lib.pa_bm_seq_len(self._h, seq_id)
+        if v < 0:
+            check("pa_bm_seq_len", int(v))
+        return int(v)
+
+    def num_free(self) -> int:
+        return int(self._lib.pa_bm_num_free(self._h))
+
+    def refcount(self, block_id: int) -> int:
+        v = self._lib.pa_bm_refcount(self._h, block_id)
+        if v < 0:
+            check("pa_bm_refcount", v)
+        return int(v)
+
+    def build_batch(self, seq_ids: Sequence[int], max_blocks: int):
+        """(tables int32 [n][max_blocks], context_lens int32 [n]) as numpy arrays."""
+        import numpy as np
+        n = len(seq_ids)
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        tabs = np.empty((n, max_blocks), dtype=np.int32)
+        lens = np.empty((n,), dtype=np.int32)
+        check("pa_bm_build_batch", self._lib.pa_bm_build_batch(
+            self._h, ids.ctypes.data_as(C.POINTER(C.c_int64)), n, max_blocks,
+            tabs.ctypes.data_as(C.POINTER(C.c_int32)), lens.ctypes.data_as(C.POINTER(C.c_int32))))
+        return tabs, lens

@@ -1,0 +1,119 @@
+// Cache upkeep kernels: new-token scatter (reshape_and_cache) and the
+// copy-on-write block copy (copy_blocks). Both are pure bit copies moved in
+// 16-byte vectors, bound by HBM bandwidth.
+//
+// reshape_and_cache: each decode step appends the new token's K and V to the
+// cache ("KV Cache Explained Like You're an LLM Engineer", section "What KV
+// Cache Stores"); in the paged cache the destination is the token's slot,
+// block table[p / 16] at offset p % 16 ("Inference serving: the KV-cache
+// machine", section "Paged KV: virtual memory for tokens").
+// copy_blocks: a write to a shared block first copies the whole block to a
+// fresh one ("Modern AI Infrastructure and Agentic System Design", 9.1, the
+// copy-on-write figure).
+#include "pa_common.cuh"
+
+namespace {
+
+constexpr int kBS = 16;
+
+// One thread moves one 16-byte chunk (8 dims) of one (token, KV head) row of
+// K and the same chunk of V. Threads of a warp cover consecutive chunks of
+// consecutive rows, so loads and stores are fully coalesced.
+__global__ void __launch_bounds__(256)
+reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                         uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                         const int64_t* __restrict__ slots, long long n_chunks, int n_kv_heads,
+                         int chunks_per_head, long long pool_slots, unsigned int* err) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n_chunks) return;
+    const int per_token = n_kv_heads * chunks_per_head;
+    const long long t = i / per_token;
+    const int rem = (int)(i - t * per_token);
+    const int h = rem / chunks_per_head;
+    const int c = rem - h * chunks_per_head;
+    const int64_t slot = slots[t];
+    if (slot < 0) return;
+    if (slot >= pool_slots) {
+        if (rem == 0) pa::set_error(err, PA_DEVERR_SLOT);
+        return;
+    }
+    const long long blk = slot / kBS, off = slot % kBS;
+    const long long dst = ((blk * n_kv_heads + h) * kBS + off) * chunks_per_head + c;
+    k_pool[dst] = k[i];
+    v_pool[dst] = v[i];
+}
+
+// grid.x = pair, grid.y = slice of the block; each CTA copies its slice of K
+// and of V for one pair. A block is n_kv_heads*16*head_dim*2 bytes.
+__global__ void __launch_bounds__(256)
+copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                   const int64_t* __restrict__ pairs, int chunks_per_block, int num_blocks,
+                   unsigned int* err) {
+    const int pr = blockIdx.x;
+    const int64_t src = pairs[2 * pr], dst = pairs[2 * pr + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) pa::set_error(err, PA_DEVERR_PAIR);
+        return;
+    }
+    const long long s0 = src * (long long)chunks_per_block, d0 = dst * (long long)chunks_per_block;
+    for (int c = blockIdx.y * blockDim.x + threadIdx.x; c < chunks_per_block;
+         c += gridDim.y * blockDim.x) {
+        const uint4 kk = k_pool[s0 + c];
+        const uint4 vv = v_pool[s0 + c];
+        k_pool[d0 + c] = kk;
+        v_pool[d0 + c] = vv;
+    }
+}
+
+}  // namespace
+
+extern "C" int pa_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+                                    const int64_t* slot_mapping, int n_tokens, int n_kv_heads,
+                                    int head_dim, int block_size, int num_blocks, pa_stream_t stream) {
+    if (n_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (block_size != kBS) return PA_ERR_UNSUPPORTED;
+    if (head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return PA_OK;
+    if (!k || !v || !k_pool || !v_pool || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!pa_aligned16(k) || !pa_aligned16(v) || !pa_aligned16(k_pool) || !pa_aligned16(v_pool) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    unsigned int* err = pa_device_error_ptr();
+    if (!err) return PA_ERR_CUDA;
+    const int cph = head_dim / 8;
+    const long long n_chunks = (long long)n_tokens * n_kv_heads * cph;
+    const int threads = 256;
+    const long long blocks = (n_chunks + threads - 1) / threads;
+    if (blocks > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_pool),
+        static_cast<uint4*>(v_pool), slot_mapping, n_chunks, n_kv_heads, cph,
+        (long long)num_blocks * kBS, err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs,
+                              int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                              pa_stream_t stream) {
+    if (n_pairs < 0 || n_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (block_size != kBS) return PA_ERR_UNSUPPORTED;
+    if (head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+    if (n_pairs == 0) return PA_OK;
+    if (n_pairs > 0x7fffffff / 2) return PA_ERR_UNSUPPORTED;
+    if (!k_pool || !v_pool || !block_mapping) return PA_ERR_INVALID_ARG;
+    if (!pa_aligned16(k_pool) || !pa_aligned16(v_pool) ||
+        (reinterpret_cast<uintptr_t>(block_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    unsigned int* err = pa_device_error_ptr();
+    if (!err) return PA_ERR_CUDA;
+    const long long chunks = (long long)n_kv_heads * kBS * head_dim / 8;
+    if (chunks > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    const int threads = 256;
+    int slices = (int)((chunks + threads - 1) / threads);
+    if (slices > 64) slices = 64;
+    dim3 grid(n_pairs, slices);
+    copy_blocks_kernel<<<grid, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), block_mapping, (int)chunks, num_blocks,
+        err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

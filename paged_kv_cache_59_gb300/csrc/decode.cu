@@ -1,0 +1,632 @@
+// PagedAttention decode for sm_103a.
+//
+// What is computed ("LLM Inference Optimization: KV-Cache, PagedAttention,
+// and GPU Memory Efficiency", section "PagedAttention: OS Concepts Meet GPU
+// Memory": for each query, walk the sequence's block table, load K and V of
+// each physical block, compute partial scores and accumulate with an online
+// softmax; "KV Cache Explained Like You're an LLM Engineer", section
+// "Transformer Attention: A Quick Refresher": softmax(q K^T / sqrt(d)) V):
+//
+//   out[b][h] = sum_t softmax_t(scale * q[b][h] . K_b[t]) V_b[t]
+//
+// Work decomposition (a GB300 design; the pages give none):
+//  * One CTA per (context partition, KV head, sequence). All G = n_heads /
+//    n_kv_heads query heads of the KV head's group are handled by the CTA, so
+//    every K/V byte read from HBM serves the whole group.
+//  * Each warp of the CTA streams its own share of the partition's blocks
+//    through a private ring of S shared-memory stages. A (block, KV head)
+//    tile of K and of V is block_size*head_dim*2 contiguous bytes in the pool
+//    layout [blocks][kv_heads][16][head_dim]; lane 0 moves each with one
+//    bulk asynchronous copy (cp.async.bulk, completion counted on an
+//    mbarrier), so several tiles per warp are in flight while the warp
+//    computes on an earlier one. Block ids come from the block table, read
+//    once per warp (one entry per lane) and broadcast with a shuffle.
+//  * Dot products: LPT lanes share one token row, each holding head_dim/LPT
+//    dims of q (pre-multiplied by scale*log2(e)) in registers; partial dots
+//    for all (head, token) pairs of the tile are combined with a
+//    transposing butterfly (each shuffle level halves the values a lane
+//    keeps), which costs far fewer shuffles than one reduction per dot.
+//  * Online softmax in fp32 (base-2): running max and sum per head; the
+//    probabilities of a tile are exchanged through a small per-warp shared
+//    buffer and the PV product accumulates fp32 outputs with packed
+//    fp32x2 FMAs.
+//  * Warps of a CTA are merged through shared memory. If the sequence fits in
+//    one partition the CTA writes the bf16 output directly; otherwise it
+//    writes (max, sum, unnormalised output) to the workspace and a second
+//    kernel merges the partitions (split-K).
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "pa_common.cuh"
+
+namespace {
+
+constexpr int kBS = 16;          // tokens per block
+constexpr unsigned kFull = 0xffffffffu;
+
+struct DecodeParams {
+    uint16_t* out;
+    const uint16_t* q;
+    const uint16_t* k_pool;
+    const uint16_t* v_pool;
+    const int32_t* tables;
+    const int32_t* ctx;
+    float* ws_ml;  // [B][H][P][2]
+    float* ws_o;   // [B][H][P][D]
+    float scale_log2;
+    int n_heads;
+    int n_kv_heads;
+    int max_blocks;
+    int num_blocks;
+    int part_blocks;
+    int max_parts;
+    unsigned int* err;
+};
+
+// Transposing butterfly: N values per lane are summed across the lanes that
+// differ in bits M, M/2, ..., 1; each level keeps half of the values.
+template <int N, int M>
+struct TransposeReduce {
+    static __device__ __forceinline__ void run(float* v, int lane) {
+        if constexpr (M >= 1) {
+            if constexpr (N > 1) {
+                constexpr int H2 = N / 2;
+                const bool up = (lane & M) != 0;
+#pragma unroll
+                for (int k = 0; k < H2; ++k) {
+                    float send = up ? v[k] : v[k + H2];
+                    float keep = up ? v[k + H2] : v[k];
+                    v[k] = keep + __shfl_xor_sync(kFull, send, M);
+                }
+                TransposeReduce<H2, M / 2>::run(v, lane);
+            } else {
+                v[0] += __shfl_xor_sync(kFull, v[0], M);
+                TransposeReduce<1, M / 2>::run(v, lane);
+            }
+        }
+    }
+};
+
+template <int D, int G, int LPT>
+struct Shape {
+    static constexpr int NCH = D / (8 * LPT);      // 16-byte chunks per lane per token row
+    static constexpr int TPP = 32 / LPT;           // tokens per warp pass
+    static constexpr int NPASS = kBS / TPP;        // passes per tile
+    static constexpr int NV = NPASS * G;           // partial dots per lane
+    static constexpr int NKEEP = NV / LPT > 0 ? NV / LPT : 1;
+    static constexpr int TILE_ELEMS = kBS * D;
+    static constexpr int TILE_BYTES = TILE_ELEMS * 2;
+    // lane-bit masks (within a warp) that do not select the head of the kept
+    // values, and the subset on which kept values are duplicated
+    static constexpr int HEAD_LO = LPT / G;        // masks >= HEAD_LO and < LPT select the head
+    static constexpr int nonhead_mask() {
+        int r = 0;
+        for (int m = 1; m < 32; m <<= 1)
+            if (m >= LPT || m < HEAD_LO) r |= m;
+        return r;
+    }
+    static constexpr int dup_mask() {              // levels run after a single value is left
+        int r = 0, n = NV;
+        for (int m = LPT / 2; m >= 1; m >>= 1) {
+            if (n > 1) n /= 2;
+            else r |= m;
+        }
+        return r;
+    }
+    static_assert(D % (8 * LPT) == 0, "head_dim must split into 16-byte chunks per lane");
+    static_assert(G <= LPT, "kept values of a lane must belong to one head");
+};
+
+template <int D, int G, int LPT, int NW, int S>
+struct Smem {
+    using SH = Shape<D, G, LPT>;
+    static constexpr size_t STAGES = (size_t)NW * S * 2 * SH::TILE_BYTES;
+    static constexpr size_t BARS = (size_t)NW * S * 8;
+    static constexpr size_t PBUF = (size_t)NW * G * kBS * 4;
+    static constexpr size_t ABUF = (size_t)NW * ((G + 3) / 4) * 16;
+    static constexpr size_t MERGE = (size_t)NW * (G * D + 2 * G) * 4;
+    static_assert(MERGE <= STAGES, "merge buffers reuse the stage ring");
+    static constexpr size_t TOTAL = STAGES + BARS + PBUF + ABUF;
+};
+
+template <int D, int G, int LPT, int NW, int S>
+__global__ void __launch_bounds__(NW * 32, 1)
+pa_decode_partition_kernel(const DecodeParams P) {
+    using SH = Shape<D, G, LPT>;
+    using SM = Smem<D, G, LPT, NW, S>;
+    constexpr int NCH = SH::NCH, TPP = SH::TPP, NPASS = SH::NPASS, NV = SH::NV;
+    constexpr int NKEEP = SH::NKEEP;
+    constexpr int NONHEAD = SH::nonhead_mask();
+    constexpr int LSUM = NONHEAD & ~SH::dup_mask();
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* stages = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::STAGES);
+    float* pbuf_all = reinterpret_cast<float*>(smem + SM::STAGES + SM::BARS);
+    float* abuf_all = reinterpret_cast<float*>(smem + SM::STAGES + SM::BARS + SM::PBUF);
+
+    const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = P.n_heads, Hk = P.n_kv_heads;
+    const int h0 = kvh * G;
+    const int ctx = P.ctx[b];
+
+    if (ctx <= 0) {  // empty sequence: zero output rows, written once
+        if (p == 0) {
+            for (int e = threadIdx.x; e < G * D / 2; e += NW * 32) {
+                int h = e / (D / 2), d2 = e % (D / 2);
+                reinterpret_cast<uint32_t*>(P.out + ((size_t)b * H + h0 + h) * D)[d2] = 0u;
+            }
+        }
+        return;
+    }
+    int nblk = (ctx + kBS - 1) / kBS;
+    int nparts = (nblk + P.part_blocks - 1) / P.part_blocks;
+    if (nblk > P.max_blocks || nparts > P.max_parts) {  // caller broke the bounds it passed
+        if (p == 0 && threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_CONTEXT);
+        nblk = min(nblk, P.max_blocks);
+        nparts = min((nblk + P.part_blocks - 1) / P.part_blocks, P.max_parts);
+        nblk = min(nblk, nparts * P.part_blocks);
+    }
+    if (p >= nparts) return;
+    const int blk_begin = p * P.part_blocks;
+    const int nb_local = min(blk_begin + P.part_blocks, nblk) - blk_begin;
+    const int my_n = nb_local > warp ? (nb_local - warp + NW - 1) / NW : 0;  // <= 32
+
+    const int c = lane % LPT;   // chunk lane within a token row
+    const int tg = lane / LPT;  // token group within a pass
+
+    unsigned char* my_stages = stages + (size_t)warp * S * 2 * SH::TILE_BYTES;
+    uint64_t* my_bars = bars + warp * S;
+    float* pbuf = pbuf_all + warp * G * kBS;
+    float* abuf = abuf_all + warp * ((G + 3) / 4) * 4;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) pa::mbar_init(&my_bars[s], 1);
+        pa::fence_mbar_init();
+    }
+    __syncwarp();
+
+    // one block-table entry per lane: local block warp + NW*lane
+    int my_bid = -1;
+    if (lane < my_n) my_bid = P.tables[(size_t)b * P.max_blocks + blk_begin + warp + NW * lane];
+
+    const uint64_t pol = pa::l2_evict_first_policy();
+    const size_t head_stride = (size_t)SH::TILE_ELEMS;
+    auto issue = [&](int i) {  // all lanes call (shuffle); lane 0 issues the copies
+        const int bid = __shfl_sync(kFull, my_bid, i);
+        if (lane == 0) {
+            const int st = i % S;
+            uint64_t* bar = &my_bars[st];
+            unsigned char* dk = my_stages + (size_t)st * 2 * SH::TILE_BYTES;
+            if (bid >= 0 && bid < P.num_blocks) {
+                const size_t off = ((size_t)bid * Hk + kvh) * head_stride;
+                pa::mbar_arrive_expect_tx(bar, 2 * SH::TILE_BYTES);
+                pa::bulk_g2s(dk, P.k_pool + off, SH::TILE_BYTES, bar, pol);
+                pa::bulk_g2s(dk + SH::TILE_BYTES, P.v_pool + off, SH::TILE_BYTES, bar, pol);
+            } else {
+                pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
+                pa::mbar_arrive(bar);  // completes the phase with no data
+            }
+        }
+    };
+
+    // q for the G heads, this lane's dims, pre-scaled into the base-2 domain
+    float2 qf[G][NCH][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const uint16_t* qrow = P.q + ((size_t)b * H + h0 + h) * D;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+            uint4 w = *reinterpret_cast<const uint4*>(qrow + (c + LPT * j) * 8);
+            uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float2 f = pa::bf16x2_to_float2(ws[k]);
+                qf[h][j][k] = make_float2(f.x * P.scale_log2, f.y * P.scale_log2);
+            }
+        }
+    }
+
+    // which (head, pass) values this lane keeps after the transposing butterfly
+    int base = 0;
+    {
+        int n = NV;
+#pragma unroll
+        for (int m = LPT / 2; m >= 1; m >>= 1) {
+            if (n > 1) {
+                n /= 2;
+                if (lane & m) base += n;
+            }
+        }
+    }
+    const int h_own = base / NPASS;
+    const int ip0 = base % NPASS;
+    const bool alpha_writer = (lane & NONHEAD) == 0;
+
+    float m_run = -INFINITY;  // running max of this lane's head (base-2 units)
+    float l_run = 0.f;        // partial sum of p over this lane's kept tokens
+    float2 o[G][NCH][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int j = 0; j < NCH; ++j)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[h][j][k] = make_float2(0.f, 0.f);
+
+    for (int s = 0; s < S && s < my_n; ++s) issue(s);
+
+    int consumed = 0;
+    bool aborted = false;
+    for (int i = 0; i < my_n; ++i) {
+        const int st = i % S;
+        const bool ok = pa::mbar_wait(&my_bars[st], (uint32_t)((i / S) & 1), P.err);
+        if (__any_sync(kFull, !ok)) {
+            aborted = true;
+            break;
+        }
+        consumed = i + 1;
+        const int bid = __shfl_sync(kFull, my_bid, i);
+        if (bid >= 0 && bid < P.num_blocks) {
+            const unsigned char* sK = my_stages + (size_t)st * 2 * SH::TILE_BYTES;
+            const unsigned char* sV = sK + SH::TILE_BYTES;
+            const int tok0 = (blk_begin + warp + NW * i) * kBS;
+
+            // ---- scores: partial dots over this lane's dims
+            float sc[NV];
+#pragma unroll
+            for (int ip = 0; ip < NPASS; ++ip) {
+                const int t = ip * TPP + tg;
+                float2 acc[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < NCH; ++j) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(sK + (t * D + (c + LPT * j) * 8) * 2);
+                    const float2 k0 = pa::bf16x2_to_float2(w.x), k1 = pa::bf16x2_to_float2(w.y);
+                    const float2 k2 = pa::bf16x2_to_float2(w.z), k3 = pa::bf16x2_to_float2(w.w);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        acc[h] = __ffma2_rn(qf[h][j][0], k0, acc[h]);
+                        acc[h] = __ffma2_rn(qf[h][j][1], k1, acc[h]);
+                        acc[h] = __ffma2_rn(qf[h][j][2], k2, acc[h]);
+                        acc[h] = __ffma2_rn(qf[h][j][3], k3, acc[h]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) sc[h * NPASS + ip] = acc[h].x + acc[h].y;
+            }
+            TransposeReduce<NV, LPT / 2>::run(sc, lane);
+
+            // ---- online softmax for this lane's head
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < NKEEP; ++k) {
+                const int t = (ip0 + k) * TPP + tg;
+                sc[k] = (tok0 + t < ctx) ? sc[k] : -INFINITY;
+                tmax = fmaxf(tmax, sc[k]);
+            }
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1)
+                if (NONHEAD & m) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, m));
+            const float m_new = fmaxf(m_run, tmax);
+            const bool changed = m_new > m_run;
+            const float alpha = pa::fast_exp2(m_run - m_new);
+            float psum = 0.f;
+#pragma unroll
+            for (int k = 0; k < NKEEP; ++k) {
+                const float pk = pa::fast_exp2(sc[k] - m_new);
+                psum += pk;
+                pbuf[h_own * kBS + tg * NPASS + ip0 + k] = pk;
+            }
+            l_run = l_run * alpha + psum;
+            m_run = m_new;
+            if (alpha_writer) abuf[h_own] = alpha;
+            const bool any_changed = __any_sync(kFull, changed);
+            __syncwarp();
+
+            // ---- rescale and accumulate p . V
+            if (any_changed) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float a = abuf[h];
+                    const float2 a2 = make_float2(a, a);
+#pragma unroll
+                    for (int j = 0; j < NCH; ++j)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) o[h][j][k] = __fmul2_rn(o[h][j][k], a2);
+                }
+            }
+            float pl[G][NPASS];
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int ip = 0; ip < NPASS; ip += 4) {
+                    const float4 v4 = *reinterpret_cast<const float4*>(pbuf + h * kBS + tg * NPASS + ip);
+                    pl[h][ip] = v4.x;
+                    pl[h][ip + 1] = v4.y;
+                    pl[h][ip + 2] = v4.z;
+                    pl[h][ip + 3] = v4.w;
+                }
+#pragma unroll
+            for (int ip = 0; ip < NPASS; ++ip) {
+                const int t = ip * TPP + tg;
+                if (tok0 + t < ctx) {
+#pragma unroll
+                    for (int j = 0; j < NCH; ++j) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(sV + (t * D + (c + LPT * j) * 8) * 2);
+                        const float2 v0 = pa::bf16x2_to_float2(w.x), v1 = pa::bf16x2_to_float2(w.y);
+                        const float2 v2 = pa::bf16x2_to_float2(w.z), v3 = pa::bf16x2_to_float2(w.w);
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            const float2 pp = make_float2(pl[h][ip], pl[h][ip]);
+                            o[h][j][0] = __ffma2_rn(pp, v0, o[h][j][0]);
+                            o[h][j][1] = __ffma2_rn(pp, v1, o[h][j][1]);
+                            o[h][j][2] = __ffma2_rn(pp, v2, o[h][j][2]);
+                            o[h][j][3] = __ffma2_rn(pp, v3, o[h][j][3]);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (i + S < my_n) issue(i + S);
+    }
+    if (aborted) {
+        // drain copies still in flight (bounded) before the stage memory is reused
+        for (int i = consumed; i < my_n && i < consumed + S; ++i)
+            pa::mbar_wait(&my_bars[i % S], (uint32_t)((i / S) & 1), P.err, 10000000ull);
+    }
+
+    // ---- merge within the warp: sum o over token groups, l over head lanes
+#pragma unroll
+    for (int m = LPT; m < 32; m <<= 1)
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int j = 0; j < NCH; ++j)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    o[h][j][k].x += __shfl_xor_sync(kFull, o[h][j][k].x, m);
+                    o[h][j][k].y += __shfl_xor_sync(kFull, o[h][j][k].y, m);
+                }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1)
+        if (LSUM & m) l_run += __shfl_xor_sync(kFull, l_run, m);
+
+    __syncthreads();  // every warp is done with its ring: reuse it for the merge
+    float* mo = reinterpret_cast<float*>(stages);            // [NW][G][D]
+    float* mm = mo + NW * G * D;                               // [NW][G] max
+    float* ml = mm + NW * G;                                   // [NW][G] sum
+    if (tg == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+                float* dst = mo + ((size_t)warp * G + h) * D + (c + LPT * j) * 8;
+                reinterpret_cast<float4*>(dst)[0] =
+                    make_float4(o[h][j][0].x, o[h][j][0].y, o[h][j][1].x, o[h][j][1].y);
+                reinterpret_cast<float4*>(dst)[1] =
+                    make_float4(o[h][j][2].x, o[h][j][2].y, o[h][j][3].x, o[h][j][3].y);
+            }
+    }
+    if (alpha_writer) {
+        mm[warp * G + h_own] = m_run;
+        ml[warp * G + h_own] = l_run;
+    }
+    __syncthreads();
+
+    const bool single = (nparts == 1);
+    for (int e = threadIdx.x; e < G * D / 2; e += NW * 32) {
+        const int h = e / (D / 2), d = (e % (D / 2)) * 2;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * G + h]);
+        float L = 0.f, O0 = 0.f, O1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float f = (mm[w * G + h] == -INFINITY) ? 0.f : pa::fast_exp2(mm[w * G + h] - M);
+            L += ml[w * G + h] * f;
+            const float2 ov = *reinterpret_cast<const float2*>(mo + ((size_t)w * G + h) * D + d);
+            O0 += ov.x * f;
+            O1 += ov.y * f;
+        }
+        const size_t row = (size_t)b * H + h0 + h;
+        if (single) {
+            const float inv = 1.f / L;
+            reinterpret_cast<uint32_t*>(P.out + row * D)[d / 2] = pa::float2_to_bf16x2(O0 * inv, O1 * inv);
+        } else {
+            const size_t slot = row * P.max_parts + p;
+            *reinterpret_cast<float2*>(P.ws_o + slot * D + d) = make_float2(O0, O1);
+            if (d == 0) *reinterpret_cast<float2*>(P.ws_ml + slot * 2) = make_float2(M, L);
+        }
+    }
+}
+
+}  // namespace
+
+namespace {
+
+// Split-K merge: one warp per (sequence, query head) row.
+template <int D>
+__global__ void __launch_bounds__(128)
+pa_decode_merge_kernel(const DecodeParams P, int n_rows) {
+    constexpr int PER = D / 32;
+    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);  // (seq, head) row
+    const int lane = threadIdx.x & 31;
+    if (row >= n_rows) return;
+    const int H = P.n_heads;
+    const int b = row / H;
+    const int ctx = P.ctx[b];
+    if (ctx <= 0) return;
+    const int nblk = min((ctx + kBS - 1) / kBS, P.max_blocks);
+    const int nparts = min((nblk + P.part_blocks - 1) / P.part_blocks, P.max_parts);
+    if (nparts <= 1) return;  // the partition kernel wrote this row
+    const size_t slot0 = (size_t)row * P.max_parts;
+    float M = -INFINITY;
+    for (int p = 0; p < nparts; ++p) M = fmaxf(M, P.ws_ml[(slot0 + p) * 2]);
+    float L = 0.f;
+    float acc[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+        const float2 ml = *reinterpret_cast<const float2*>(P.ws_ml + (slot0 + p) * 2);
+        const float f = pa::fast_exp2(ml.x - M);
+        L += ml.y * f;
+        const float* op = P.ws_o + (slot0 + p) * D + lane * PER;
+        if constexpr (PER == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(op);
+            acc[0] += v.x * f; acc[1] += v.y * f; acc[2] += v.z * f; acc[3] += v.w * f;
+        } else {
+            const float2 v = *reinterpret_cast<const float2*>(op);
+            acc[0] += v.x * f; acc[1] += v.y * f;
+        }
+    }
+    const float inv = 1.f / L;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(P.out + (size_t)row * D + lane * PER);
+#pragma unroll
+    for (int k = 0; k < PER; k += 2) dst[k / 2] = pa::float2_to_bf16x2(acc[k] * inv, acc[k + 1] * inv);
+}
+
+constexpr int kNW = 4;  // warps per CTA
+
+template <int D>
+struct StagesFor {
+    static constexpr int S = D == 128 ? 3 : 4;
+};
+
+template <int D, int G>
+struct LptFor {
+    static constexpr int LPT = (D == 128 && G == 8) ? 16 : 8;
+};
+
+template <int D, int G>
+int launch_partition(const DecodeParams& P, int n_seqs, cudaStream_t stream) {
+    constexpr int LPT = LptFor<D, G>::LPT;
+    constexpr int S = StagesFor<D>::S;
+    using SM = Smem<D, G, LPT, kNW, S>;
+    auto kern = pa_decode_partition_kernel<D, G, LPT, kNW, S>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::TOTAL) !=
+            cudaSuccess)
+            return PA_ERR_CUDA;
+        attr_done[dev] = true;
+    }
+    dim3 grid(P.max_parts, P.n_kv_heads, n_seqs);
+    kern<<<grid, kNW * 32, SM::TOTAL, stream>>>(P);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+template <int D>
+int dispatch_group(int G, const DecodeParams& P, int n_seqs, cudaStream_t stream) {
+    switch (G) {
+        case 1: return launch_partition<D, 1>(P, n_seqs, stream);
+        case 2: return launch_partition<D, 2>(P, n_seqs, stream);
+        case 4: return launch_partition<D, 4>(P, n_seqs, stream);
+        case 8: return launch_partition<D, 8>(P, n_seqs, stream);
+        default: return PA_ERR_UNSUPPORTED;
+    }
+}
+
+constexpr int kDefaultPartitionTokens = 512;
+
+int resolve_partition_tokens(int pt) {
+    if (pt == 0) return kDefaultPartitionTokens;
+    if (pt < 64 || pt > 2048 || pt % 64 != 0) return -1;
+    return pt;
+}
+
+size_t workspace_bytes_for(int n_seqs, int n_heads, int head_dim, int max_parts) {
+    if (max_parts <= 1) return 0;
+    const size_t rows = (size_t)n_seqs * n_heads * max_parts;
+    const size_t ml = (rows * 2 * sizeof(float) + 255) & ~(size_t)255;
+    return ml + rows * head_dim * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" size_t pa_decode_workspace_bytes(int n_seqs, int n_heads, int head_dim,
+                                            int max_context_len, int partition_tokens) {
+    const int pt = resolve_partition_tokens(partition_tokens);
+    if (pt < 0 || n_seqs <= 0 || n_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return 0;
+    const int max_parts = (max_context_len + pt - 1) / pt;
+    return workspace_bytes_for(n_seqs, n_heads, head_dim, max_parts);
+}
+
+extern "C" int pa_decode_ex(void* out, const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, const int32_t* context_lens, float scale,
+                            int n_heads, int n_kv_heads, int head_dim, int block_size, int n_seqs,
+                            int max_blocks_per_seq, int max_context_len, int num_blocks,
+                            int partition_tokens, void* workspace, size_t workspace_bytes,
+                            pa_stream_t stream) {
+    if (n_seqs < 0 || max_context_len < 0 || num_blocks < 0 || max_blocks_per_seq < 0 ||
+        n_heads <= 0 || n_kv_heads <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (block_size != kBS) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (n_heads % n_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int G = n_heads / n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
+    if (n_kv_heads > 65535 || n_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    if ((long long)max_blocks_per_seq * kBS < (long long)max_context_len) return PA_ERR_INVALID_ARG;
+    const int pt = resolve_partition_tokens(partition_tokens);
+    if (pt < 0) return PA_ERR_INVALID_ARG;
+    if (pt / kBS > 32 * kNW) return PA_ERR_INVALID_ARG;  // one table entry per lane
+    if (n_seqs == 0) return PA_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (!pa_aligned16(out) || !pa_aligned16(q) || !pa_aligned16(k_pool) || !pa_aligned16(v_pool))
+        return PA_ERR_INVALID_ARG;
+    if (out == q) return PA_ERR_INVALID_ARG;
+    const int max_parts = max_context_len > 0 ? (max_context_len + pt - 1) / pt : 1;
+    const size_t need = workspace_bytes_for(n_seqs, n_heads, head_dim, max_parts);
+    if (need > 0 && (!workspace || workspace_bytes < need || !pa_aligned16(workspace)))
+        return PA_ERR_WORKSPACE;
+    unsigned int* err = pa_device_error_ptr();
+    if (!err) return PA_ERR_CUDA;
+
+    DecodeParams P;
+    P.out = static_cast<uint16_t*>(out);
+    P.q = static_cast<const uint16_t*>(q);
+    P.k_pool = static_cast<const uint16_t*>(k_pool);
+    P.v_pool = static_cast<const uint16_t*>(v_pool);
+    P.tables = block_tables;
+    P.ctx = context_lens;
+    const size_t rows = (size_t)n_seqs * n_heads * max_parts;
+    P.ws_ml = need ? static_cast<float*>(workspace) : nullptr;
+    P.ws_o = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             ((rows * 2 * sizeof(float) + 255) & ~(size_t)255))
+                  : nullptr;
+    P.scale_log2 = scale * 1.4426950408889634f;
+    P.n_heads = n_heads;
+    P.n_kv_heads = n_kv_heads;
+    P.max_blocks = max_blocks_per_seq;
+    P.num_blocks = num_blocks;
+    P.part_blocks = pt / kBS;
+    P.max_parts = max_parts;
+    P.err = err;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int st = head_dim == 128 ? dispatch_group<128>(G, P, n_seqs, s) : dispatch_group<64>(G, P, n_seqs, s);
+    if (st != PA_OK || max_parts <= 1) return st;
+    const int n_rows = n_seqs * n_heads;
+    dim3 grid((n_rows + 3) / 4);
+    if (head_dim == 128)
+        pa_decode_merge_kernel<128><<<grid, 128, 0, s>>>(P, n_rows);
+    else
+        pa_decode_merge_kernel<64><<<grid, 128, 0, s>>>(P, n_rows);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" int pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                         int n_heads, int n_kv_heads, int head_dim, int block_size, int n_seqs,
+                         int max_blocks_per_seq, int max_context_len, int num_blocks, void* workspace,
+                         size_t workspace_bytes, pa_stream_t stream) {
+    return pa_decode_ex(out, q, k_pool, v_pool, block_tables, context_lens, scale, n_heads, n_kv_heads,
+                        head_dim, block_size, n_seqs, max_blocks_per_seq, max_context_len, num_blocks, 0,
+                        workspace, workspace_bytes, stream);
+}

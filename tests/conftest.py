@@ -27,3 +27,12 @@ def read_golden(name: str):
                 continue
             rows.append(line.split())
     return rows
+
+
+@pytest.fixture(scope="session")
+def capi():
+    """The built C-ABI library (built in-tree on first use)."""
+    from paged_kv_cache_59_gb300 import build as _b
+    from paged_kv_cache_59_gb300 import _capi
+    _b.build()
+    return _capi.load()

@@ -1,0 +1,160 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+the header declares, validates arguments before touching the device, and the
+host block manager matches the reference model."""
+import ctypes as C
+import os
+import random
+import re
+
+import pytest
+
+from oracle.block_manager import BlockManagerModel, OutOfBlocks
+from tests.conftest import ROOT
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for must in ["pa_decode", "pa_decode_ex", "pa_decode_workspace_bytes", "pa_reshape_and_cache",
+                 "pa_copy_blocks", "pa_prefill_paged", "pa_get_device_error", "pa_status_string",
+                 "pa_bm_create", "pa_bm_append_tokens", "pa_bm_fork", "pa_bm_free_seq"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(capi):
+    from paged_kv_cache_59_gb300 import _capi
+    for name in _declared_functions():
+        assert hasattr(capi, name), name
+        assert name in _capi.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(capi):
+    assert capi.pa_status_string(0) == b"ok"
+    assert b"unsupported" in capi.pa_status_string(-2)
+
+
+def test_workspace_size_formula(capi):
+    # 64 seqs x 32 heads, context up to 4096, 512-token partitions -> 8 partitions
+    rows = 64 * 32 * 8
+    ml = (rows * 8 + 255) // 256 * 256
+    assert capi.pa_decode_workspace_bytes(64, 32, 128, 4096, 512) == ml + rows * 128 * 4
+    assert capi.pa_decode_workspace_bytes(4, 4, 64, 37, 512) == 0      # one partition
+    assert capi.pa_decode_workspace_bytes(4, 4, 64, 37, 100) == 0      # invalid size -> 0
+
+
+def _decode_args(**over):
+    a = dict(out=C.c_void_p(16), q=C.c_void_p(32), k=C.c_void_p(64), v=C.c_void_p(128),
+             tab=C.c_void_p(256), ctx=C.c_void_p(512), scale=0.125, H=4, Hk=4, D=64, bs=16,
+             B=4, maxb=4, maxctx=64, nblk=32, pt=0, ws=C.c_void_p(None), wsb=0, stream=None)
+    a.update(over)
+    return a
+
+
+def _call_decode(capi, a):
+    return capi.pa_decode_ex(a["out"], a["q"], a["k"], a["v"], a["tab"], a["ctx"], a["scale"],
+                             a["H"], a["Hk"], a["D"], a["bs"], a["B"], a["maxb"], a["maxctx"],
+                             a["nblk"], a["pt"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(D=96), -2), (dict(bs=32), -2), (dict(H=6, Hk=4), -1), (dict(H=48, Hk=3), -2),
+    (dict(B=-1), -1), (dict(maxb=2), -1), (dict(pt=100), -1), (dict(pt=4096), -1),
+    (dict(q=C.c_void_p(33)), -1), (dict(out=C.c_void_p(32)), -1), (dict(k=C.c_void_p(None)), -1),
+    (dict(maxctx=1000, maxb=100), -3),
+])
+def test_decode_argument_errors_need_no_device(capi, over, status):
+    assert _call_decode(capi, _decode_args(**over)) == status
+
+
+def test_decode_empty_batch_is_ok(capi):
+    assert _call_decode(capi, _decode_args(B=0)) == 0
+
+
+def test_cache_ops_argument_errors(capi):
+    p = C.c_void_p(64)
+    assert capi.pa_reshape_and_cache(p, p, p, p, p, 4, 2, 64, 8, 16, None) == -2
+    assert capi.pa_reshape_and_cache(p, p, p, p, p, -1, 2, 64, 16, 16, None) == -1
+    assert capi.pa_reshape_and_cache(p, p, p, p, p, 0, 2, 64, 16, 16, None) == 0
+    assert capi.pa_reshape_and_cache(C.c_void_p(8), p, p, p, p, 4, 2, 64, 16, 16, None) == -1
+    assert capi.pa_copy_blocks(p, p, p, 3, 2, 64, 4, 16, None) == -2
+    assert capi.pa_copy_blocks(p, p, p, 0, 2, 64, 16, 16, None) == 0
+    assert capi.pa_copy_blocks(p, p, C.c_void_p(12), 3, 2, 64, 16, 16, None) == -1
+
+
+# ----------------------------------------------------------- block manager --
+
+def test_block_manager_matches_model_on_random_operations(capi):
+    from paged_kv_cache_59_gb300 import BlockManager, PagedKVError
+    rng = random.Random(7)
+    for trial in range(25):
+        nb = rng.randint(3, 48)
+        model = BlockManagerModel(nb, 16)
+        bm = BlockManager(nb, 16)
+        live, next_id = [], 0
+        for _ in range(250):
+            op = rng.random()
+            if op < 0.2 or not live:
+                model.add_seq(next_id); bm.add_seq(next_id); live.append(next_id); next_id += 1
+            elif op < 0.6:
+                s, n = rng.choice(live), rng.randint(0, 40)
+                try:
+                    want = model.append_tokens(s, n)
+                except OutOfBlocks:
+                    with pytest.raises(PagedKVError) as e:
+                        bm.append_tokens(s, n)
+                    assert e.value.status == -6
+                else:
+                    assert bm.append_tokens(s, n) == want
+            elif op < 0.72:
+                model.fork(live[0], next_id); bm.fork(live[0], next_id)
+                live.append(next_id); next_id += 1
+            elif op < 0.82:
+                s = rng.choice(live)
+                if model.block_table(s):
+                    lb = rng.randrange(len(model.block_table(s)))
+                    try:
+                        want = model.make_private(s, lb)
+                    except OutOfBlocks:
+                        with pytest.raises(PagedKVError):
+                            bm.make_private(s, lb)
+                    else:
+                        assert bm.make_private(s, lb) == want
+            else:
+                s = rng.choice(live)
+                model.free_seq(s); bm.free_seq(s); live.remove(s)
+            model.check_invariants()
+            assert bm.num_free() == model.num_free()
+            for s in live:
+                assert bm.block_table(s) == model.block_table(s)
+                assert bm.seq_len(s) == model.seq_len(s)
+            for b in range(nb):
+                assert bm.refcount(b) == model.refcount(b)
+
+
+def test_block_manager_errors_and_batch_tables(capi):
+    from paged_kv_cache_59_gb300 import BlockManager, PagedKVError
+    bm = BlockManager(8, 16)
+    bm.add_seq(1)
+    with pytest.raises(PagedKVError):
+        bm.add_seq(1)
+    with pytest.raises(PagedKVError):
+        bm.free_seq(2)
+    with pytest.raises(PagedKVError):
+        bm.fork(5, 6)
+    bm.append_tokens(1, 40)
+    bm.add_seq(2)
+    bm.append_tokens(2, 3)
+    tabs, lens = bm.build_batch([1, 2], 4)
+    assert list(lens) == [40, 3]
+    assert list(tabs[0][:3]) == bm.block_table(1) and tabs[0][3] == -1
+    assert list(tabs[1][:1]) == bm.block_table(2) and list(tabs[1][1:]) == [-1, -1, -1]
+    with pytest.raises(PagedKVError):
+        bm.build_batch([1], 2)
+    assert bm.refcount(0) >= 0
+    with pytest.raises(PagedKVError):
+        bm.refcount(8)
