@@ -1,0 +1,523 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV decode hot path on GB300.
+
+One step = the whole hot path for one batch: pa_reshape_and_cache of every
+sequence's new token, then pa_decode (partition kernel + split-K merge) over
+the paged cache. Default workload: the Llama-3-8B-shaped GQA decode batch
+(64 sequences, context U{128..4096} seeded, 32 q / 8 KV heads, head_dim 128,
+bf16, block 16, random block placement in a pool 1.25x the blocks needed).
+
+value = KV bytes read per step (K and V of every attended token) / device
+time per step, whole job (all ranks). The KV pool and the step's inputs are
+resident in HBM when the timed region starts; the 586 MB KV stream is 4.5x
+the 129 MB L2, so no flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       python bench.py --impl reference ...   (the fp64 CPU oracle arm)
+Under torchrun (N > 1) each rank runs an independent replica of the workload
+(decode shards by sequence with no exchange), timing is bracketed by a
+barrier and synchronize, and the max time over ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV-read HBM GB/s (fraction of peak), tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "gqa_8b"
+WORKLOAD_LAYERS = {"tiny_mha": 1, "mha_7b": 32, "gqa_8b": 32, "gqa_70b_cow": 80, "mixed": 32}
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_decode_partition_gqa8b.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=["tiny_mha", "mha_7b", "gqa_8b", "gqa_70b_cow", "mixed"])
+    ap.add_argument("--partition-tokens", type=int, default=0,
+                    help="decode context partition size (0 = library default)")
+    ap.add_argument("--skip-baselines", action="store_true",
+                    help="skip the CPU oracle and end-to-end legs (profiling runs)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cu", "pa_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_59_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    vals = {}
+    with open(PROFILE_SUMMARY) as f:
+        for line in f:
+            if line.startswith("bench_traffic:"):
+                for kv in line.split(":", 1)[1].split():
+                    k, _, v = kv.partition("=")
+                    vals[k] = v
+    if vals.get("source_sha") != kernel_source_sha():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        deadline = time.time() + 5
+        while not self.rows and time.time() < deadline:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [r for t, r in self.rows if self.t0 is not None and self.t0 <= t <= (self.t1 or t)]
+        used = inside
+        if not used and self.rows:                    # region shorter than one sample period
+            ref = self.t1 or self.t0 or 0
+            used = [min(self.rows, key=lambda tr: abs(tr[0] - ref))[1]]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in used:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples_in_region": len(inside)}
+
+
+# ------------------------------------------------------------- our arm ------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_59_gb300 as pk
+    from paged_kv_cache_59_gb300 import build as pk_build
+    from workloads import make_workload
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        pk_build.build()
+    if world > 1:
+        dist.barrier()
+    pk.load()
+    dev = torch.device("cuda", local)
+
+    wl = make_workload(args.workload, fill="zero", keep_logical=False)
+    H, Hk, D = wl.n_heads, wl.n_kv_heads, wl.head_dim
+    B = len(wl.dec_ctx)
+    max_ctx = int(wl.dec_ctx.max())
+    sum_ctx = int(wl.dec_ctx.sum())
+    kv_bytes = sum_ctx * Hk * D * 2 * 2
+    alg_bytes = (kv_bytes + 2 * wl.q.nbytes + wl.dec_tables.nbytes + wl.dec_ctx.nbytes)
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    # decode-step inputs only: new token k/v are those of the decode sequences
+    n_dec_new = min(B, len(wl.slot_mapping)) if wl.slot_mapping is not None else 0
+    new_k, new_v = wl.new_k[:n_dec_new], wl.new_v[:n_dec_new]
+    slots = wl.slot_mapping[:n_dec_new]
+    kp, vp = to_dev(wl.k_pool), to_dev(wl.v_pool)
+    del wl.k_pool, wl.v_pool
+    q = to_dev(wl.q)
+    out = torch.empty_like(q)
+    nk, nv, sl = to_dev(new_k), to_dev(new_v), to_dev(slots)
+    tabs, ctx = to_dev(wl.dec_tables), to_dev(wl.dec_ctx)
+    pt = args.partition_tokens
+    ws = pk.decode_workspace(q, max_ctx, pt)
+    stream = torch.cuda.current_stream()
+    launches_per_step = (1 if n_dec_new else 0) + 1 + (1 if pk.pa_decode_workspace_bytes(B, H, D, max_ctx, pt) else 0)
+
+    def step(ev_pair=None):
+        if n_dec_new:
+            pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
+        if ev_pair is not None:
+            ev_pair[0].record(stream)
+        pk.pa_decode(out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws, partition_tokens=pt)
+        if ev_pair is not None:
+            ev_pair[1].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert pk.pa_get_device_error() == 0
+
+    def timed_region():
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        sampler.mark("begin")
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        sampler.mark("end")
+        if world > 1:
+            dist.barrier()
+        total_ms = t_start.elapsed_time(t_end)
+        dec_ms = [a.elapsed_time(b) for a, b in evs]
+        return total_ms, dec_ms
+
+    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    sampler = ClockSampler(vis[local] if local < len(vis) else str(local))
+    sampler.start()
+    total_ms, dec_ms = timed_region()
+    clocks = sampler.stop()
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    if bad & set(clocks.get("reasons", [])):
+        sampler = ClockSampler(sampler.gpu)
+        sampler.start()
+        total_ms, dec_ms = timed_region()
+        clocks = sampler.stop()
+        clocks["remeasured"] = True
+
+    t_max = total_ms
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    ms_per_step = t_max / args.steps
+    value = world * kv_bytes * args.steps / (t_max / 1e3) / 1e9
+
+    # roofline of the decode call (partition kernel + merge kernel)
+    dec_ms_sorted = sorted(dec_ms)
+    dec_avg = sum(dec_ms) / len(dec_ms)
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (dec_avg / 1e3) / 1e9
+    traffic = profiled_traffic() if args.workload == DEFAULT_WORKLOAD and pt == 0 else None
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) q/K/V rounded to bf16, seeded context lengths, "
+                "random physical block placement",
+        "config": {
+            "workload": wl.name,
+            "n_seqs": B, "n_heads": H, "n_kv_heads": Hk, "head_dim": D, "block_size": 16,
+            "sum_context_tokens": sum_ctx, "max_context": max_ctx, "num_blocks": wl.num_blocks,
+            "kv_bytes_per_step": kv_bytes,
+            "step": "pa_reshape_and_cache (1 new token/seq) + pa_decode (partition kernel + split-K merge)",
+            "l2": f"no flush: the KV stream ({kv_bytes / 1e6:.0f} MB/step) exceeds the 129 MB L2",
+            "partition_tokens": pt or 512,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "tokens_per_s": round(world * B / (ms_per_step / 1e3), 1),
+        "kv_tokens_per_s": round(world * sum_ctx / (ms_per_step / 1e3), 1),
+        "attention_only_model_tokens_per_s": round(
+            world * B / (ms_per_step / 1e3) / WORKLOAD_LAYERS[args.workload], 1),
+        "hbm_frac_of_measured": round(value / world / peak, 4),
+        "hbm_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pa_decode_partition_kernel + pa_decode_merge_kernel (one pa_decode call)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": f"{peak_kind} HBM copy GB/s",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "launch_ms_avg": round(dec_avg, 5),
+            "launch_ms_p10_p90": [round(dec_ms_sorted[len(dec_ms) // 10], 5),
+                                  round(dec_ms_sorted[(9 * len(dec_ms)) // 10], 5)],
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+
+    if not args.skip_baselines:
+        result["e2e"] = run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world,
+                                dist if world > 1 else None)
+        if rank == 0:
+            result["cpu_baseline"] = run_cpu_baseline(args.workload, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dist):
+    """Same metric through the public API with host buffers: each step copies
+    its inputs (q, new K/V, slots, tables, context lengths) from pinned host
+    memory, runs the hot path, and reads the output back."""
+    import numpy as np
+    import torch
+
+    def pinned(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).pin_memory()
+
+    h_in = [pinned(x) for x in (wl.q, new_k, new_v, slots, wl.dec_tables, wl.dec_ctx)]
+    d_in = [torch.empty_like(x, device=dev) for x in h_in]
+    h_out = torch.empty(wl.q.shape, dtype=torch.int16).pin_memory()
+    d_out = torch.empty(wl.q.shape, dtype=torch.int16, device=dev)
+    max_ctx = int(wl.dec_ctx.max())
+    ws = pk.decode_workspace(d_in[0], max_ctx, args.partition_tokens)
+    stream = torch.cuda.current_stream()
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+
+    def step():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        q, nk, nv, sl, tabs, ctx = d_in
+        if len(slots):
+            pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
+        pk.pa_decode(d_out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws,
+                     partition_tokens=args.partition_tokens)
+        h_out.copy_(d_out, non_blocking=True)
+        stream.synchronize()                       # the host reads this step's result
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    n = args.steps
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([dt], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    return {"value": round(world * kv_bytes * n / dt / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(dt * 1e3 / n, 5),
+            "how": "wall clock over K steps; each step: pinned H2D of inputs, "
+                   "reshape_and_cache + decode, D2H of out, stream sync"}
+
+
+# ------------------------------------------------------ CPU oracle timing ---
+
+_CPU_CHILD = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+from workloads import make_workload
+from oracle.attention import paged_decode
+from oracle.cache_ops import reshape_and_cache
+wl = make_workload({workload!r}, fill="zero", keep_logical=False)
+B = len(wl.dec_ctx)
+n = min(B, len(wl.slot_mapping)) if wl.slot_mapping is not None else 0
+budget, per_step = {seconds}, {per_step}
+kv_tok = wl.n_kv_heads * wl.head_dim * 2 * 2
+done_tok = 0
+seqs = 0
+t0 = time.perf_counter()
+b = 0
+while True:
+    sel = [(b + i) % B for i in range(per_step)]
+    b = (b + per_step) % B
+    if n:
+        sel_new = [i for i in sel if i < n]
+        kp, vp = reshape_and_cache(wl.new_k[sel_new], wl.new_v[sel_new], wl.k_pool, wl.v_pool,
+                                   wl.slot_mapping[sel_new])
+    else:
+        kp, vp = wl.k_pool, wl.v_pool
+    paged_decode(wl.q[sel], kp, vp, wl.dec_tables[sel], wl.dec_ctx[sel], wl.scale)
+    done_tok += int(wl.dec_ctx[sel].sum())
+    seqs += len(sel)
+    if {fixed_steps} and seqs >= {fixed_steps} * per_step:
+        break
+    if not {fixed_steps} and time.perf_counter() - t0 >= budget:
+        break
+dt = time.perf_counter() - t0
+print(json.dumps({{"seconds": dt, "tokens": done_tok, "seqs": seqs, "kv_bytes": done_tok * kv_tok}}))
+"""
+
+
+def _oracle_child(workload, seconds, per_step, fixed_steps=0):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = _CPU_CHILD.format(root=ROOT, workload=workload, seconds=seconds, per_step=per_step,
+                             fixed_steps=fixed_steps)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle child failed:\n{r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def run_cpu_baseline(workload, seconds):
+    try:
+        res = _oracle_child(workload, seconds, per_step=1)
+    except Exception as e:  # report, do not hide
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "error": str(e)[-300:]}
+    return {"value": round(res["kv_bytes"] / res["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{res['seqs']} sequences of the {workload} batch (cycled in order, "
+                      f"{res['tokens']} context tokens) through the fp64 numpy oracle in "
+                      f"{res['seconds']:.1f} s on 1 host thread (BLAS pinned to 1 thread)",
+            "host_logical_cores": os.cpu_count()}
+
+
+# --------------------------------------------------------- reference arm ----
+
+def run_reference(args):
+    """The oracle as the reference arm: the same metric and unit on the host
+    cores, each step a bounded sample (whole sequences) of the workload."""
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return
+    # size the per-step sample so that warmup + steps stay within ~2 minutes
+    calib = _oracle_child(args.workload, 2.0, per_step=1)
+    sec_per_seq = calib["seconds"] / max(calib["seqs"], 1)
+    budget = 120.0
+    total_steps = args.steps + args.warmup
+    per_step = max(1, int(budget / total_steps / sec_per_seq))
+    per_step = min(per_step, 64)
+    if args.warmup:
+        _oracle_child(args.workload, 0, per_step=per_step, fixed_steps=args.warmup)
+    res = _oracle_child(args.workload, 0, per_step=per_step, fixed_steps=args.steps)
+    value = res["kv_bytes"] / res["seconds"] / 1e9
+    sample = (f"each step: {per_step} sequence(s) of the {args.workload} batch, cycled in order, "
+              f"through the fp64 numpy oracle (reshape_and_cache + decode) on 1 host thread")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(res["seconds"] * 1e3 / max(args.steps, 1), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic: the same seeded workload as the GPU arm",
+        "config": {"workload": args.workload, "sample_sequences_per_step": per_step},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -20,7 +20,7 @@ from . import _capi
 from ._capi import PagedKVError, check, load  # noqa: F401
 
 __all__ = [
-    "pa_decode", "pa_decode_workspace_bytes", "pa_reshape_and_cache", "pa_copy_blocks",
+    "pa_decode", "pa_decode_workspace_bytes", "decode_workspace", "pa_reshape_and_cache", "pa_copy_blocks",
     "pa_prefill_paged", "pa_get_device_error", "BlockManager", "load", "PagedKVError",
 ]
 
@@ -61,6 +61,14 @@ def pa_decode_workspace_bytes(n_seqs: int, n_heads: int, head_dim: int, max_cont
                               partition_tokens: int = 0) -> int:
     return int(load().pa_decode_workspace_bytes(n_seqs, n_heads, head_dim, max_context_len,
                                                 partition_tokens))
+
+
+def decode_workspace(q, max_context_len: int, partition_tokens: int = 0):
+    """A workspace tensor sized for pa_decode on this q shape and context bound."""
+    torch = _torch()
+    n_seqs, n_heads, head_dim = q.shape
+    nbytes = pa_decode_workspace_bytes(n_seqs, n_heads, head_dim, max_context_len, partition_tokens)
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
 
 
 def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,

@@ -129,8 +129,8 @@ struct Smem {
     static constexpr size_t TOTAL = STAGES + BARS + PBUF + ABUF;
 };
 
-template <int D, int G, int LPT, int NW, int S>
-__global__ void __launch_bounds__(NW * 32, 1)
+template <int D, int G, int LPT, int NW, int S, int MINB>
+__global__ void __launch_bounds__(NW * 32, MINB)
 pa_decode_partition_kernel(const DecodeParams P) {
     using SH = Shape<D, G, LPT>;
     using SM = Smem<D, G, LPT, NW, S>;
@@ -491,22 +491,26 @@ pa_decode_merge_kernel(const DecodeParams P, int n_rows) {
 
 constexpr int kNW = 4;  // warps per CTA
 
-template <int D>
-struct StagesFor {
-    static constexpr int S = D == 128 ? 3 : 4;
-};
-
+// Per (head_dim, group) launch shape. Twelve resident warps per SM (three
+// CTAs of four warps, three warps per scheduler) hide the latency of the
+// per-tile dependency chains best; that caps a thread at 168 registers, so
+// G = 4 at head_dim 128 spreads a token row over 16 lanes (q and the
+// accumulators then take 32 registers each). G = 8 needs more registers and
+// runs two CTAs per SM. S stages of K+V tiles per warp fill the shared memory
+// of the resident CTAs (2 or 3 stages of 8 KiB at head_dim 128, 4 or 6 of
+// 4 KiB at head_dim 64).
 template <int D, int G>
-struct LptFor {
-    static constexpr int LPT = (D == 128 && G == 8) ? 16 : 8;
+struct Launch {
+    static constexpr int LPT = (D == 128 && G >= 4) ? 16 : 8;
+    static constexpr int MINB = G == 8 ? 2 : 3;
+    static constexpr int S = (D == 128 ? 2 : 4) * (MINB == 3 ? 1 : 3) / (MINB == 3 ? 1 : 2);
 };
 
 template <int D, int G>
 int launch_partition(const DecodeParams& P, int n_seqs, cudaStream_t stream) {
-    constexpr int LPT = LptFor<D, G>::LPT;
-    constexpr int S = StagesFor<D>::S;
-    using SM = Smem<D, G, LPT, kNW, S>;
-    auto kern = pa_decode_partition_kernel<D, G, LPT, kNW, S>;
+    using LC = Launch<D, G>;
+    using SM = Smem<D, G, LC::LPT, kNW, LC::S>;
+    auto kern = pa_decode_partition_kernel<D, G, LC::LPT, kNW, LC::S, LC::MINB>;
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
