@@ -128,6 +128,30 @@ int pa_decode_ex(void* out, const void* q, const void* k_pool, const void* v_poo
                  int partition_tokens, void* workspace, size_t workspace_bytes,
                  pa_stream_t stream);
 
+/*
+ * Allocation-free pa_decode. The pages have no counterpart: this entry point
+ * exists for callers that cannot allocate device memory for pa_decode's
+ * workspace - a runtime that gave all free HBM to its KV pool, a decode loop
+ * that must not call cudaMalloc/cudaFree (they can synchronize the device),
+ * or a host that only holds raw pointers. Same arguments and result as
+ * pa_decode (default partition size), minus the workspace: the split-K
+ * scratch is a fixed 32 MiB device array inside the library, held by every
+ * device that loads it until the process exits. The call allocates nothing.
+ *  - Returns PA_ERR_WORKSPACE, launching nothing, when
+ *    pa_decode_workspace_bytes(n_seqs, n_heads, head_dim, max_context_len, 0)
+ *    exceeds 32 MiB.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents (nothing in it needs to start at zero); calls whose kernels
+ *    overlap on the GPU race on it.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ */
+int pa_decode_noalloc(void* out, const void* q, const void* k_pool, const void* v_pool,
+                      const int32_t* block_tables, const int32_t* context_lens, float scale,
+                      int n_heads, int n_kv_heads, int head_dim, int block_size,
+                      int n_seqs, int max_blocks_per_seq, int max_context_len, int num_blocks,
+                      pa_stream_t stream);
+
 /* --------------------------------------------------------- cache upkeep */
 
 /*

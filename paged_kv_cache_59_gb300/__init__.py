@@ -20,7 +20,7 @@ from . import _capi
 from ._capi import PagedKVError, check, load  # noqa: F401
 
 __all__ = [
-    "pa_decode", "pa_decode_workspace_bytes", "decode_workspace", "pa_reshape_and_cache", "pa_copy_blocks",
+    "pa_decode", "pa_decode_workspace_bytes", "decode_workspace", "pa_decode_noalloc", "pa_reshape_and_cache", "pa_copy_blocks",
     "pa_prefill_paged", "pa_get_device_error", "BlockManager", "load", "PagedKVError",
 ]
 
@@ -93,6 +93,28 @@ def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,
         head_dim, block_size, n_seqs, block_tables.shape[1], int(max_context_len), num_blocks,
         int(partition_tokens), ws_ptr, ws_bytes, _stream(stream))
     check("pa_decode", st)
+
+
+def pa_decode_noalloc(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,
+                      max_context_len: int, stream=None) -> None:
+    """pa_decode without a caller workspace, for callers that cannot allocate
+    device memory: the split-K scratch is a fixed 32 MiB array inside the
+    library shared by all calls on a device (calls that overlap on the GPU
+    race on it). Batches needing more scratch raise (PA_ERR_WORKSPACE)."""
+    torch = _torch()
+    n_seqs, n_heads, head_dim = q.shape
+    num_blocks, n_kv_heads, block_size, hd2 = k_pool.shape
+    if hd2 != head_dim or tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if block_tables.dim() != 2 or block_tables.shape[0] != n_seqs or context_lens.numel() != n_seqs:
+        raise ValueError("block_tables must be [n_seqs][max_blocks], context_lens [n_seqs]")
+    st = load().pa_decode_noalloc(
+        _ptr(out, "out", bf16=True), _ptr(q, "q", bf16=True), _ptr(k_pool, "k_pool", bf16=True),
+        _ptr(v_pool, "v_pool", bf16=True), _ptr(block_tables, "block_tables", dtype=torch.int32),
+        _ptr(context_lens, "context_lens", dtype=torch.int32), float(scale), n_heads, n_kv_heads,
+        head_dim, block_size, n_seqs, block_tables.shape[1], int(max_context_len), num_blocks,
+        _stream(stream))
+    check("pa_decode_noalloc", st)
 
 
 def pa_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, stream=None) -> None:

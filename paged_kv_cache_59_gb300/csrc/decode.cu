@@ -634,3 +634,52 @@ extern "C" int pa_decode(void* out, const void* q, const void* k_pool, const voi
                         head_dim, block_size, n_seqs, max_blocks_per_seq, max_context_len, num_blocks, 0,
                         workspace, workspace_bytes, stream);
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode (pa_decode_noalloc).
+//
+// pa_decode needs a caller-provided scratch workspace for its split-K
+// partials. Some callers cannot allocate one: a serving runtime that has
+// handed all free HBM to its KV-cache pool, an integration that must not call
+// cudaMalloc/cudaFree on its decode loop because those calls can synchronize
+// the device and stall every stream, or a host that only passes raw pointers
+// and has no allocator to offer. For them the scratch lives in the fixed
+// array below, which every device that loads this library holds until the
+// process exits.
+//
+// Limits and sharing: the array is kNoAllocScratchBytes (32 MiB); a batch
+// whose decode workspace would be larger is rejected with PA_ERR_WORKSPACE
+// before anything is launched. Every call on a device uses the same array
+// and it keeps the previous call's contents; nothing in it has to start at
+// zero (each call writes every partial it later reads). Two calls whose
+// kernels overlap on the GPU (for example on two streams without ordering
+// between them) race on the array and may produce wrong outputs.
+//
+// Host code cannot use the array's name as a device address (on the host it
+// only names a stand-in). The first call on each device, with that device
+// current, resolves the real address with cudaGetSymbolAddress and caches
+// it; make that first call before any stream capture on that device.
+static constexpr size_t kNoAllocScratchBytes = 32ull << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static void* g_noalloc_scratch_addr[64] = {nullptr};
+
+extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_tables, const int32_t* context_lens, float scale,
+                                 int n_heads, int n_kv_heads, int head_dim, int block_size, int n_seqs,
+                                 int max_blocks_per_seq, int max_context_len, int num_blocks,
+                                 pa_stream_t stream) {
+    if (n_seqs < 0 || n_heads <= 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
+    if (n_seqs > 0 && max_context_len > 0 &&
+        pa_decode_workspace_bytes(n_seqs, n_heads, head_dim, max_context_len, 0) > kNoAllocScratchBytes)
+        return PA_ERR_WORKSPACE;  // this batch needs more scratch than the fixed array holds
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+    if (!g_noalloc_scratch_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return PA_ERR_CUDA;
+        g_noalloc_scratch_addr[dev] = ptr;
+    }
+    return pa_decode_ex(out, q, k_pool, v_pool, block_tables, context_lens, scale, n_heads, n_kv_heads,
+                        head_dim, block_size, n_seqs, max_blocks_per_seq, max_context_len, num_blocks, 0,
+                        g_noalloc_scratch_addr[dev], kNoAllocScratchBytes, stream);
+}
