@@ -1,16 +1,447 @@
-// Chunked causal prefill over the paged cache (tcgen05 path): placeholder
-// until the tensor-core kernel lands; reports the configuration as
-// unsupported so no caller mistakes it for a result.
-#include "pa_common.cuh"
+// Chunked causal prefill over the paged KV cache on the tcgen05 tensor cores.
+//
+// What is computed ("Modern AI Infrastructure and Agentic System Design",
+// 9.1 "Two workloads wearing one name": a long prompt is processed in chunks
+// interleaved with decode; "KV Cache Explained Like You're an LLM Engineer",
+// "Prefill Phase vs. Decode Phase"; causal masking as in "What Happens Inside
+// an LLM During Inference ...", "Self-Attention Mechanism"): sequence s's
+// chunk of L new tokens occupies the last L of its context_lens[s] cached
+// positions; chunk row i sits at position p = ctx - L + i and
+//     out[i][h] = sum_{t <= p} softmax_t(scale * q[i][h] . K[t]) V[t].
+//
+// Design (GB300): one CTA per (query tile, KV head, sequence). The CTA's 128
+// matrix rows are QT = 128/G chunk tokens x the G query heads of the KV
+// head's group, so every K/V byte staged in shared memory feeds all G heads.
+// Per key tile of 128 keys (8 blocks of 16):
+//   - an issuer warp moves the 8 K and 8 V blocks with 2-D TMA loads into
+//     128B-swizzled shared memory (double buffered; blocks past the end of
+//     the sequence load out of bounds and arrive as zeros);
+//   - the same warp issues S = Q K^T (tcgen05.mma kind::f16, bf16 in, fp32
+//     accumulator in tensor memory, M = N = 128, 8 x K=16 steps) and, once
+//     the softmax warps have written P, O += P V (V as an MN-major operand);
+//   - four softmax warps (thread = row) read S from tensor memory, apply the
+//     scale, the causal mask and an online softmax in fp32 (base 2) with a
+//     lazily updated row maximum: O in tensor memory is rescaled only when a
+//     row's maximum grows by more than 8 (so un-normalised p <= 2^8), then
+//     write P as two bf16 terms, P = P_hi + P_lo (P_lo = the rounding
+//     residual), into swizzled shared-memory operands; O += P_hi V + P_lo V.
+//     A single bf16 P would cost up to ~2^-9 relative per weight, which on
+//     short causal rows with cancelling values exceeds an absolute error of
+//     2e-3; the two-term P is accurate to ~2^-16.
+// The normalised output O / l is written once at the end.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "tc_sm100.cuh"
+
+namespace {
+
+constexpr int kD = 128;       // head_dim (the only one built)
+constexpr int kBS = 16;       // tokens per block
+constexpr int kKT = 128;      // keys per key tile
+constexpr int kBPT = kKT / kBS;  // blocks per key tile
+constexpr int kRows = 128;    // MMA M
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t kQ = 0;
+constexpr uint32_t kK0 = 32768;
+constexpr uint32_t kV0 = kK0 + 2 * 32768;
+constexpr uint32_t kP = kV0 + 2 * 32768;     // P_hi
+constexpr uint32_t kPlo = kP + 32768;         // P_lo
+constexpr uint32_t kBars = kPlo + 32768;  // 8 mbarriers
+constexpr uint32_t kMisc = kBars + 64;  // tmem slot, abort flag
+constexpr uint32_t kSmemBytes = kMisc + 64 + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 256;     // S: 0..127, O: 128..255
+
+struct PrefillParams {
+    uint16_t* out;
+    const uint16_t* q;
+    const int32_t* tables;
+    const int32_t* ctx;
+    const int32_t* qsl;
+    float scale_log2;
+    int n_heads;
+    int n_kv_heads;
+    int max_blocks;
+    int num_blocks;
+    int oob_row;  // a TMA row coordinate past the end of the pool (zero fill)
+    unsigned int* err;
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                         volatile int* abort_flag) {
+    if (*abort_flag) return false;
+    if (pa::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = pa::globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (pa::mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (pa::globaltimer_ns() - t0 > PA_WAIT_LIMIT_NS) {
+                pa::set_error(err, PA_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(160, 1)
+pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV) {
+    constexpr int QT = kRows / G;  // chunk tokens per CTA
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024u - (pa::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+    uint64_t* kv_full = bars;      // [2]
+    uint64_t* s_full = bars + 2;
+    uint64_t* p_full = bars + 3;   // 4 arrivals: one per softmax warp
+    uint64_t* pv_done = bars + 4;
+    uint64_t* drain = bars + 5;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
+
+    const int qt = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = P.n_heads, Hk = P.n_kv_heads, h0 = kvh * G;
+    const int q0 = P.qsl[s];
+    const int L = P.qsl[s + 1] - q0;
+    const int i0 = qt * QT;
+    if (i0 >= L) return;  // CTA-uniform, before any barrier or TMEM use
+    const int ctx = P.ctx[s];
+    if (ctx < L) {  // the chunk must be in the cache already
+        if (threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_CONTEXT);
+        return;
+    }
+    const int nblk = min((ctx + kBS - 1) / kBS, P.max_blocks);
+    const int first_pos = ctx - L;
+    const int p_last = first_pos + min(i0 + QT, L) - 1;
+    const int n_kt = p_last / kKT + 1;
+
+    if (threadIdx.x == 0) {
+        pa::mbar_init(&kv_full[0], 1);
+        pa::mbar_init(&kv_full[1], 1);
+        pa::mbar_init(s_full, 1);
+        pa::mbar_init(p_full, 4);
+        pa::mbar_init(pv_done, 1);
+        pa::mbar_init(drain, 1);
+        *abort_flag = 0;
+        pa::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tslot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    // ---- Q tile: row r = (chunk token i0 + r / G, head h0 + r % G), swizzled K-major
+    if (warp < 4) {
+        const int r = threadIdx.x;
+        const int i = i0 + r / G;
+        const uint4* src = reinterpret_cast<const uint4*>(P.q + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const uint4 v = i < L ? src[c] : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sm + kQ + (c >> 3) * 16384 + tc::sw128_offset(r, c & 7)) = v;
+        }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tbase = *tslot;
+    const uint32_t tS = tbase, tO = tbase + 128;
+
+    constexpr uint32_t ID_QK = tc::idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t ID_PV = tc::idesc_bf16_f32(128, 128, 0, 1);
+
+    if (warp == 4) {
+        // ------------------------------------------------------- issuer
+        const int32_t* trow = P.tables + (size_t)s * P.max_blocks;
+        int ids = -1;  // lane l: block id of block 32*group + l
+        auto load_ids = [&](int group) {
+            const int blk = group * 32 + lane;
+            ids = blk < nblk ? trow[blk] : -1;
+        };
+        auto issue_tma = [&](int j) {  // warp-collective
+            const int st = j & 1;
+            int y[kBPT];
+#pragma unroll
+            for (int b = 0; b < kBPT; ++b) {
+                const int bid = __shfl_sync(kFull, ids, (j & 3) * kBPT + b);
+                const int blk = j * kBPT + b;
+                bool ok = blk < nblk;
+                if (ok && (bid < 0 || bid >= P.num_blocks)) {
+                    if (lane == 0) pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
+                    ok = false;
+                }
+                y[b] = ok ? (bid * Hk + kvh) * kBS : P.oob_row;
+            }
+            if (lane == 0) {
+                pa::mbar_arrive_expect_tx(&kv_full[st], 2 * 32768);
+                unsigned char* ks = sm + kK0 + st * 32768;
+                unsigned char* vs = sm + kV0 + st * 32768;
+#pragma unroll
+                for (int b = 0; b < kBPT; ++b)
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        tc::tma_load_2d(ks + g * 16384 + b * 2048, &tmK, g * 64, y[b], &kv_full[st]);
+                        tc::tma_load_2d(vs + g * 16384 + b * 2048, &tmV, g * 64, y[b], &kv_full[st]);
+                    }
+            }
+            __syncwarp();
+        };
+        auto issue_pv = [&](int j) {  // O += P_hi,j V_j + P_lo,j V_j
+            if (lane == 0) {
+                const uint32_t vs = pa::smem_u32(sm + kV0 + (j & 1) * 32768);
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t ps = pa::smem_u32(sm + (part ? kPlo : kP));
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t ad = tc::smem_desc(ps + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc(vs + ks * 2048, 16384, 1024);
+                        tc::mma_bf16(tO, ad, bd, ID_PV, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+                    }
+                }
+                tc::mma_commit(pv_done);
+            }
+            __syncwarp();
+        };
+        load_ids(0);
+        issue_tma(0);
+        if (n_kt > 1) issue_tma(1);
+        bool ok = true;
+        for (int j = 0; j < n_kt && ok; ++j) {
+            ok = wait_bar(&kv_full[j & 1], (uint32_t)((j >> 1) & 1), P.err, abort_flag);
+            if (ok && j > 0) ok = wait_bar(p_full, (uint32_t)((j - 1) & 1), P.err, abort_flag);
+            if (!ok) break;
+            tc::fence_after_sync();
+            if (j > 0) issue_pv(j - 1);
+            if (lane == 0) {  // S = Q K_j^T
+                const uint32_t qs = pa::smem_u32(sm + kQ);
+                const uint32_t kst = pa::smem_u32(sm + kK0 + (j & 1) * 32768);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t ad = tc::smem_desc(qs + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc(kst + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                    tc::mma_bf16(tS, ad, bd, ID_QK, ks > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(s_full);
+            }
+            __syncwarp();
+            if (j >= 1 && j + 1 < n_kt) {
+                // stage (j+1)&1 was last read by PV_{j-1}: wait for it, then refill
+                ok = wait_bar(pv_done, (uint32_t)((j - 1) & 1), P.err, abort_flag);
+                if (!ok) break;
+                if (((j + 1) & 3) == 0) load_ids((j + 1) >> 2);
+                issue_tma(j + 1);
+            }
+        }
+        if (ok) ok = wait_bar(p_full, (uint32_t)((n_kt - 1) & 1), P.err, abort_flag);
+        if (ok) {
+            tc::fence_after_sync();
+            issue_pv(n_kt - 1);
+        }
+        // drain: every issued MMA has completed before the CTA can release its
+        // shared and tensor memory (bounded wait)
+        if (lane == 0) tc::mma_commit(drain);
+        __syncwarp();
+        pa::mbar_wait(drain, 0, nullptr, 10000000ull);
+        if (!ok) {  // TMA copies may still be landing: bounded waits on both stages
+            pa::mbar_wait(&kv_full[0], 0, nullptr, 10000000ull);
+            pa::mbar_wait(&kv_full[1], 0, nullptr, 10000000ull);
+        }
+    } else {
+        // ------------------------------------------------- softmax warps
+        const int r = threadIdx.x;  // matrix row = TMEM lane
+        const int i = i0 + r / G;
+        const int pos = first_pos + i;  // this row's position (padding rows: beyond the chunk)
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kt; ++j) {
+            if (ok) ok = wait_bar(s_full, (uint32_t)(j & 1), P.err, abort_flag);
+            ok = __all_sync(kFull, ok);
+            if (!ok) break;
+            tc::fence_after_sync();
+            float sv[kKT];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t raw[32];
+                tc::tmem_ld32(tS + lane_base + c * 32, raw);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) sv[c * 32 + k] = __uint_as_float(raw[k]);
+            }
+            // V rows of the sequence's last, partial block hold whatever the pool
+            // has there: zero them so that p = 0 never meets a NaN
+            const int kb = j * kKT;
+            if ((ctx & (kBS - 1)) && ctx > kb && ctx < kb + kKT) {
+                const int z0 = ctx - kb, z1 = min(((ctx + kBS - 1) & ~(kBS - 1)) - kb, kKT);
+                unsigned char* vs = sm + kV0 + (j & 1) * 32768;
+                for (int e = r; e < (z1 - z0) * 16; e += 128) {
+                    const int row = z0 + (e >> 4), g = (e >> 3) & 1, c = e & 7;
+                    *reinterpret_cast<uint4*>(vs + g * 16384 + tc::sw128_offset(row, c)) = make_uint4(0, 0, 0, 0);
+                }
+                tc::fence_async_smem();
+            }
+            // scale, causal mask, tile maximum
+            float tmax = -INFINITY;
+            const bool need_mask = kb + kKT - 1 > pos;
+#pragma unroll
+            for (int c = 0; c < kKT; ++c) {
+                float x = sv[c] * P.scale_log2;
+                if (need_mask && kb + c > pos) x = -INFINITY;
+                sv[c] = x;
+                tmax = fmaxf(tmax, x);
+            }
+            const bool rescale = tmax > m_used + kRescaleThreshold;
+            float alpha = 1.f;
+            if (rescale) {
+                alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
+                m_used = tmax;
+            }
+            // PV_{j-1} must be done before P is overwritten or O is rescaled
+            if (j > 0) {
+                if (ok) ok = wait_bar(pv_done, (uint32_t)((j - 1) & 1), P.err, abort_flag);
+                ok = __all_sync(kFull, ok);
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (__any_sync(kFull, rescale)) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t raw[32];
+                        tc::tmem_ld32(tO + lane_base + c * 32, raw);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) raw[k] = __float_as_uint(__uint_as_float(raw[k]) * alpha);
+                        tc::tmem_st32(tO + lane_base + c * 32, raw);
+                    }
+                    tc::tmem_wait_st();
+                }
+            }
+            // p = 2^(s - m), written as P_hi + P_lo (bf16 each), 8 keys per 16-byte chunk
+            float psum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float a = pa::fast_exp2(sv[c * 8 + 2 * k] - m_used);
+                    const float b = pa::fast_exp2(sv[c * 8 + 2 * k + 1] - m_used);
+                    psum += a + b;
+                    hi[k] = pa::float2_to_bf16x2(a, b);
+                    const float2 h2 = pa::bf16x2_to_float2(hi[k]);
+                    lo[k] = pa::float2_to_bf16x2(a - h2.x, b - h2.y);
+                }
+                const uint32_t off = (c >> 3) * 16384 + tc::sw128_offset(r, c & 7);
+                *reinterpret_cast<uint4*>(sm + kP + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(sm + kPlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            l = l * alpha + psum;
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) pa::mbar_arrive(p_full);
+        }
+        if (ok) ok = wait_bar(pv_done, (uint32_t)((n_kt - 1) & 1), P.err, abort_flag);
+        ok = __all_sync(kFull, ok);
+        if (ok) {
+            tc::fence_after_sync();
+            const float inv = 1.f / l;
+            uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t raw[32];
+                tc::tmem_ld32(tO + lane_base + c * 32, raw);
+                tc::tmem_wait_ld();
+                if (i < L) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 8) {
+                        uint4 w;
+                        w.x = pa::float2_to_bf16x2(__uint_as_float(raw[k]) * inv, __uint_as_float(raw[k + 1]) * inv);
+                        w.y = pa::float2_to_bf16x2(__uint_as_float(raw[k + 2]) * inv, __uint_as_float(raw[k + 3]) * inv);
+                        w.z = pa::float2_to_bf16x2(__uint_as_float(raw[k + 4]) * inv, __uint_as_float(raw[k + 5]) * inv);
+                        w.w = pa::float2_to_bf16x2(__uint_as_float(raw[k + 6]) * inv, __uint_as_float(raw[k + 7]) * inv);
+                        dst[(c * 32 + k) / 8] = w;
+                    }
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
+}
+
+template <int G>
+int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtensorMap& tv, int n_seqs,
+                   int max_chunk_len, cudaStream_t stream) {
+    auto kern = pa_prefill_tc_kernel<G>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess)
+            return PA_ERR_CUDA;
+        attr_done[dev] = true;
+    }
+    constexpr int QT = kRows / G;
+    dim3 grid((max_chunk_len + QT - 1) / QT, Pp.n_kv_heads, n_seqs);
+    kern<<<grid, 160, kSmemBytes, stream>>>(Pp, tk, tv);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
 
 extern "C" int pa_prefill_paged(void* out, const void* q, const void* k_pool, const void* v_pool,
                                 const int32_t* block_tables, const int32_t* context_lens,
                                 const int32_t* q_start_loc, float scale, int n_heads, int n_kv_heads,
                                 int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
                                 int max_chunk_len, int num_blocks, pa_stream_t stream) {
-    (void)out; (void)q; (void)k_pool; (void)v_pool; (void)block_tables; (void)context_lens;
-    (void)q_start_loc; (void)scale; (void)n_heads; (void)n_kv_heads; (void)head_dim;
-    (void)block_size; (void)n_seqs; (void)max_blocks_per_seq; (void)max_chunk_len;
-    (void)num_blocks; (void)stream;
-    return PA_ERR_UNSUPPORTED;
+    if (n_seqs < 0 || max_chunk_len < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || n_heads <= 0 ||
+        n_kv_heads <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != kD || block_size != kBS) return PA_ERR_UNSUPPORTED;
+    if (n_heads % n_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int G = n_heads / n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
+    if (n_seqs == 0 || max_chunk_len == 0) return PA_OK;
+    if (n_kv_heads > 65535 || n_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens || !q_start_loc)
+        return PA_ERR_INVALID_ARG;
+    if (!pa_aligned16(out) || !pa_aligned16(q) || !pa_aligned16(k_pool) || !pa_aligned16(v_pool))
+        return PA_ERR_INVALID_ARG;
+    if (out == q) return PA_ERR_INVALID_ARG;
+    const long long rows = (long long)num_blocks * n_kv_heads * kBS;
+    if (rows + kBS > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+    unsigned int* err = pa_device_error_ptr();
+    if (!err) return PA_ERR_CUDA;
+    CUtensorMap tk, tv;
+    if (!pa_make_tmap_2d_bf16(&tk, k_pool, kD, (uint64_t)rows, kD * 2, 64, kBS) ||
+        !pa_make_tmap_2d_bf16(&tv, v_pool, kD, (uint64_t)rows, kD * 2, 64, kBS))
+        return PA_ERR_CUDA;
+    PrefillParams Pp;
+    Pp.out = static_cast<uint16_t*>(out);
+    Pp.q = static_cast<const uint16_t*>(q);
+    Pp.tables = block_tables;
+    Pp.ctx = context_lens;
+    Pp.qsl = q_start_loc;
+    Pp.scale_log2 = scale * 1.4426950408889634f;
+    Pp.n_heads = n_heads;
+    Pp.n_kv_heads = n_kv_heads;
+    Pp.max_blocks = max_blocks_per_seq;
+    Pp.num_blocks = num_blocks;
+    Pp.oob_row = (int)rows;
+    Pp.err = err;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    switch (G) {
+        case 1: return launch_prefill<1>(Pp, tk, tv, n_seqs, max_chunk_len, st);
+        case 2: return launch_prefill<2>(Pp, tk, tv, n_seqs, max_chunk_len, st);
+        case 4: return launch_prefill<4>(Pp, tk, tv, n_seqs, max_chunk_len, st);
+        default: return launch_prefill<8>(Pp, tk, tv, n_seqs, max_chunk_len, st);
+    }
 }

@@ -158,3 +158,15 @@ def test_block_manager_errors_and_batch_tables(capi):
     assert bm.refcount(0) >= 0
     with pytest.raises(PagedKVError):
         bm.refcount(8)
+
+
+def test_prefill_argument_errors_need_no_device(capi):
+    p = C.c_void_p(4096)
+    args = [p, p, p, p, p, p, p, C.c_float(0.1)]
+    # head_dim 64 is not built for prefill; block size 8 unsupported; group 3 unsupported
+    assert capi.pa_prefill_paged(*args, 8, 8, 64, 16, 2, 4, 64, 16, None) == -2
+    assert capi.pa_prefill_paged(*args, 8, 8, 128, 8, 2, 4, 64, 16, None) == -2
+    assert capi.pa_prefill_paged(*args, 12, 4, 128, 16, 2, 4, 64, 16, None) == -2
+    assert capi.pa_prefill_paged(*args, 8, 8, 128, 16, -1, 4, 64, 16, None) == -1
+    assert capi.pa_prefill_paged(*args, 8, 8, 128, 16, 0, 4, 64, 16, None) == 0
+    assert capi.pa_prefill_paged(C.c_void_p(4100), *args[1:], 8, 8, 128, 16, 2, 4, 64, 16, None) == -1

@@ -1,0 +1,81 @@
+"""GPU parity for the tcgen05 chunked causal prefill against the fp64 oracle.
+
+Tolerance (per element): |gpu - ref| <= 2e-3 + 1e-2 * |ref|. Cases cover a
+whole prompt as one chunk, chunks at an offset with ragged lengths and
+partial last blocks (NaN-poisoned slots past the context), several key
+tiles, every group size, padding rows of a partial query tile, and sampled
+rows of the full mixed workload (4 chunks of 512 at 32K context).
+"""
+import numpy as np
+import pytest
+
+from oracle.attention import paged_prefill
+from oracle.cache_ops import reshape_and_cache as o_rac
+from tests._gpu import assert_attention_close, check_device_error, dev, host_bits, torch_cuda
+from workloads import make_prefill_case, make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pk(capi):
+    torch_cuda()
+    import paged_kv_cache_59_gb300 as m
+    m.pa_get_device_error()
+    return m
+
+
+def _run(pk, wl):
+    torch = torch_cuda()
+    kp, vp = dev(wl.k_pool), dev(wl.v_pool)
+    pk.pa_reshape_and_cache(dev(wl.new_k), dev(wl.new_v), kp, vp, dev(wl.slot_mapping))
+    q = dev(wl.q_pf)
+    out = torch.full_like(q, 0x7FC0)
+    max_chunk = int(np.max(np.diff(wl.q_start_loc)))
+    pk.pa_prefill_paged(out, q, kp, vp, dev(wl.pf_tables), dev(wl.pf_ctx), dev(wl.q_start_loc), wl.scale,
+                        max_chunk)
+    torch.cuda.synchronize()
+    return host_bits(out)
+
+
+@pytest.mark.parametrize("case", [
+    dict(ctx=[40], lens=[40], H=4, Hk=4),                 # G=1, whole prompt, one key tile
+    dict(ctx=[300, 129], lens=[37, 129], H=32, Hk=8),     # G=4, offsets, partial blocks
+    dict(ctx=[520, 77], lens=[200, 5], H=16, Hk=8),       # G=2, several query tiles
+    dict(ctx=[700], lens=[33], H=64, Hk=8),               # G=8, 6 key tiles
+    dict(ctx=[256, 255, 17], lens=[256, 1, 17], H=32, Hk=8),  # exact tiles, single-row chunk
+])
+def test_prefill_matches_oracle(pk, case):
+    wl = make_prefill_case(700 + sum(case["ctx"]), case["ctx"], case["lens"], [], case["H"], case["Hk"], 128)
+    got = _run(pk, wl)
+    ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
+    stats = assert_attention_close(got, ref, f"prefill {case}")
+    check_device_error(0)
+    print(case, stats)
+
+
+def test_prefill_hot_logits(pk):
+    """q x 16: row maxima grow tile after tile, exercising the O rescale path."""
+    wl = make_prefill_case(731, [600], [64], [], 32, 8, 128)
+    qf = (wl.q_pf.astype(np.uint32) << 16).view(np.float32) * 16.0
+    wl.q_pf = ((qf.view(np.uint32) + 0x8000) >> 16).astype(np.uint16)
+    got = _run(pk, wl)
+    ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
+    assert_attention_close(got, ref, "prefill hot")
+    check_device_error(0)
+
+
+def test_prefill_mixed_workload_sampled_rows(pk):
+    wl = make_workload("mixed")
+    got = _run(pk, wl)
+    ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    rng = np.random.default_rng(4)
+    n_rows = int(wl.q_start_loc[-1])
+    rows = [(int(r), int(h)) for r, h in zip(rng.integers(0, n_rows, 24), rng.integers(0, 32, 24))]
+    rows += [(0, 0), (511, 31), (512, 5), (n_rows - 1, 7)]   # chunk edges
+    ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale, rows=rows)
+    for r, h in rows:
+        assert_attention_close(got[r, h], ref[r, h], f"mixed prefill row {(r, h)}")
+    check_device_error(0)
