@@ -74,6 +74,16 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak():
+    """Sustained dense bf16 TFLOP/s (a kernel timed inside a long step)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("bf16_tflops_sustained", 1700.0)), "measured sustained bf16 TFLOP/s"
+    return 1700.0, "fallback sustained bf16 TFLOP/s"
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     for f in ("decode.cu", "pa_common.cuh"):
@@ -209,24 +219,44 @@ def run_ours(args):
             a = a.view(np.int16)
         return torch.from_numpy(a).to(dev)
 
-    # decode-step inputs only: new token k/v are those of the decode sequences
-    n_dec_new = min(B, len(wl.slot_mapping)) if wl.slot_mapping is not None else 0
+    # this step's new tokens: one per decode sequence, plus every chunk token
+    # of the prefill sequences (mixed workload)
+    has_pf = wl.q_pf is not None
+    n_dec_new = len(wl.slot_mapping) if wl.slot_mapping is not None else 0
     new_k, new_v = wl.new_k[:n_dec_new], wl.new_v[:n_dec_new]
     slots = wl.slot_mapping[:n_dec_new]
+    pf_flops = pf_kv_bytes = 0
+    if has_pf:
+        for si in range(len(wl.pf_ctx)):
+            L = int(wl.q_start_loc[si + 1] - wl.q_start_loc[si]); c = int(wl.pf_ctx[si])
+            pf_flops += 4 * D * H * sum(c - L + i + 1 for i in range(L))
+            pf_kv_bytes += c * Hk * D * 2 * 2
+        kv_bytes += pf_kv_bytes
     kp, vp = to_dev(wl.k_pool), to_dev(wl.v_pool)
     del wl.k_pool, wl.v_pool
     q = to_dev(wl.q)
     out = torch.empty_like(q)
     nk, nv, sl = to_dev(new_k), to_dev(new_v), to_dev(slots)
     tabs, ctx = to_dev(wl.dec_tables), to_dev(wl.dec_ctx)
+    if has_pf:
+        q_pf, pf_tabs, pf_ctx, qsl = to_dev(wl.q_pf), to_dev(wl.pf_tables), to_dev(wl.pf_ctx), to_dev(wl.q_start_loc)
+        out_pf = torch.empty_like(q_pf)
+        max_chunk = int(np.max(np.diff(wl.q_start_loc)))
     pt = args.partition_tokens
     ws = pk.decode_workspace(q, max_ctx, pt)
     stream = torch.cuda.current_stream()
-    launches_per_step = (1 if n_dec_new else 0) + 1 + (1 if pk.pa_decode_workspace_bytes(B, H, D, max_ctx, pt) else 0)
+    launches_per_step = ((1 if n_dec_new else 0) + (1 if has_pf else 0) + 1
+                         + (1 if pk.pa_decode_workspace_bytes(B, H, D, max_ctx, pt) else 0))
 
-    def step(ev_pair=None):
+    def step(ev_pair=None, pf_pair=None):
         if n_dec_new:
             pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
+        if has_pf:
+            if pf_pair is not None:
+                pf_pair[0].record(stream)
+            pk.pa_prefill_paged(out_pf, q_pf, kp, vp, pf_tabs, pf_ctx, qsl, wl.scale, max_chunk)
+            if pf_pair is not None:
+                pf_pair[1].record(stream)
         if ev_pair is not None:
             ev_pair[0].record(stream)
         pk.pa_decode(out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws, partition_tokens=pt)
@@ -241,6 +271,8 @@ def run_ours(args):
     def timed_region():
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
+        pfe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] if has_pf else [None] * args.steps
         t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
@@ -248,7 +280,7 @@ def run_ours(args):
         sampler.mark("begin")
         t_start.record(stream)
         for i in range(args.steps):
-            step(evs[i])
+            step(evs[i], pfe[i])
         t_end.record(stream)
         torch.cuda.synchronize()
         sampler.mark("end")
@@ -256,6 +288,7 @@ def run_ours(args):
             dist.barrier()
         total_ms = t_start.elapsed_time(t_end)
         dec_ms = [a.elapsed_time(b) for a, b in evs]
+        timed_region.pf_ms = [a.elapsed_time(b) for a, b in pfe] if has_pf else []
         return total_ms, dec_ms
 
     vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
@@ -333,6 +366,21 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if has_pf:
+        pf_ms = timed_region.pf_ms
+        pf_avg = sum(pf_ms) / len(pf_ms)
+        tpk, tpk_kind = measured_tensor_peak()
+        result["config"]["step"] = ("pa_reshape_and_cache (decode tokens + chunk tokens) + "
+                                    "pa_prefill_paged (tcgen05) + pa_decode")
+        result["config"]["prefill_flop_per_step"] = pf_flops
+        result["prefill_roofline"] = {
+            "bound": "tensor", "kernel": "pa_prefill_tc_kernel",
+            "achieved": round(pf_flops / (pf_avg / 1e3) / 1e12, 1), "peak": tpk,
+            "peak_source": tpk_kind, "unit": "TFLOP/s",
+            "frac": round(pf_flops / (pf_avg / 1e3) / 1e12 / tpk, 4),
+            "launch_ms_avg": round(pf_avg, 4),
+            "note": "algorithmic FLOPs 4*D*H*sum(positions attended); the kernel also runs the "
+                    "P_lo correction MMA (1.5x the PV FLOPs) and the masked diagonal tiles"}
 
     if not args.skip_baselines:
         result["e2e"] = run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world,
@@ -359,25 +407,36 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
             a = a.view(np.int16)
         return torch.from_numpy(a).pin_memory()
 
-    h_in = [pinned(x) for x in (wl.q, new_k, new_v, slots, wl.dec_tables, wl.dec_ctx)]
+    has_pf = wl.q_pf is not None
+    srcs = [wl.q, new_k, new_v, slots, wl.dec_tables, wl.dec_ctx]
+    if has_pf:
+        srcs += [wl.q_pf, wl.pf_tables, wl.pf_ctx, wl.q_start_loc]
+    h_in = [pinned(x) for x in srcs]
     d_in = [torch.empty_like(x, device=dev) for x in h_in]
-    h_out = torch.empty(wl.q.shape, dtype=torch.int16).pin_memory()
-    d_out = torch.empty(wl.q.shape, dtype=torch.int16, device=dev)
+    h_out = [torch.empty(wl.q.shape, dtype=torch.int16).pin_memory()]
+    if has_pf:
+        h_out.append(torch.empty(wl.q_pf.shape, dtype=torch.int16).pin_memory())
+    d_out = [torch.empty_like(h, device=dev) for h in h_out]
     max_ctx = int(wl.dec_ctx.max())
+    max_chunk = int(np.max(np.diff(wl.q_start_loc))) if has_pf else 0
     ws = pk.decode_workspace(d_in[0], max_ctx, args.partition_tokens)
     stream = torch.cuda.current_stream()
     h2d = sum(x.numel() * x.element_size() for x in h_in)
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
 
     def step():
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
-        q, nk, nv, sl, tabs, ctx = d_in
+        q, nk, nv, sl, tabs, ctx = d_in[:6]
         if len(slots):
             pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
-        pk.pa_decode(d_out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws,
+        if has_pf:
+            q_pf, pf_tabs, pf_ctx, qsl = d_in[6:]
+            pk.pa_prefill_paged(d_out[1], q_pf, kp, vp, pf_tabs, pf_ctx, qsl, wl.scale, max_chunk)
+        pk.pa_decode(d_out[0], q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws,
                      partition_tokens=args.partition_tokens)
-        h_out.copy_(d_out, non_blocking=True)
+        for h, d in zip(h_out, d_out):
+            h.copy_(d, non_blocking=True)
         stream.synchronize()                       # the host reads this step's result
 
     for _ in range(max(args.warmup, 3)):
@@ -398,8 +457,8 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
     return {"value": round(world * kv_bytes * n / dt / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(dt * 1e3 / n, 5),
-            "how": "wall clock over K steps; each step: pinned H2D of inputs, "
-                   "reshape_and_cache + decode, D2H of out, stream sync"}
+            "how": "wall clock over K steps; each step: pinned H2D of inputs, the step's "
+                   "kernels, D2H of the outputs, stream sync"}
 
 
 # ------------------------------------------------------ CPU oracle timing ---

@@ -72,8 +72,11 @@ enum pa_device_error {
     PA_DEVERR_SLOT = 2,     /* a slot >= num_blocks * block_size */
     PA_DEVERR_TIMEOUT = 4,  /* an mbarrier / async-copy wait ran out */
     PA_DEVERR_PAIR = 8,     /* a copy_blocks pair outside the pool */
-    PA_DEVERR_CONTEXT = 16  /* a context length beyond 16*max_blocks_per_seq or
-                               max_context_len (the excess is not attended) */
+    PA_DEVERR_CONTEXT = 16, /* a context length beyond 16*max_blocks_per_seq or
+                               max_context_len (the excess is not attended), or a
+                               prefill chunk longer than its context */
+    PA_DEVERR_LAYOUT = 32   /* the shared-memory base was not 1024-byte aligned
+                               (prefill; nothing computed) */
 };
 
 /* ------------------------------------------------------------------ decode */

@@ -12,22 +12,25 @@
 // Design (GB300): one CTA per (query tile, KV head, sequence). The CTA's 128
 // matrix rows are QT = 128/G chunk tokens x the G query heads of the KV
 // head's group, so every K/V byte staged in shared memory feeds all G heads.
-// Per key tile of 128 keys (8 blocks of 16):
+// Per key tile j of 128 keys (8 blocks of 16):
 //   - an issuer warp moves the 8 K and 8 V blocks with 2-D TMA loads into
-//     128B-swizzled shared memory (double buffered; blocks past the end of
-//     the sequence load out of bounds and arrive as zeros);
-//   - the same warp issues S = Q K^T (tcgen05.mma kind::f16, bf16 in, fp32
-//     accumulator in tensor memory, M = N = 128, 8 x K=16 steps) and, once
-//     the softmax warps have written P, O += P V (V as an MN-major operand);
-//   - four softmax warps (thread = row) read S from tensor memory, apply the
-//     scale, the causal mask and an online softmax in fp32 (base 2) with a
-//     lazily updated row maximum: O in tensor memory is rescaled only when a
-//     row's maximum grows by more than 8 (so un-normalised p <= 2^8), then
-//     write P as two bf16 terms, P = P_hi + P_lo (P_lo = the rounding
-//     residual), into swizzled shared-memory operands; O += P_hi V + P_lo V.
-//     A single bf16 P would cost up to ~2^-9 relative per weight, which on
-//     short causal rows with cancelling values exceeds an absolute error of
-//     2e-3; the two-term P is accurate to ~2^-16.
+//     128B-swizzled shared memory (3 stages; blocks past the end of the
+//     sequence load out of bounds and arrive as zeros), and issues the MMAs:
+//     S_j = Q K_j^T (tcgen05.mma kind::f16, bf16 in, fp32 accumulator in
+//     tensor memory, M = N = 128) into one of two S buffers, so that QK of
+//     tile j+1 runs while the softmax warps work on tile j; then
+//     O += P_j V_j with P read from tensor memory and V as an MN-major
+//     shared-memory operand;
+//   - eight softmax warps read S_j: a row's 128 key columns are split
+//     between two threads of two warpgroups (64 each; partial row maxima
+//     are exchanged through shared memory). They apply the scale, the causal
+//     mask and an online softmax in fp32 (base 2) with a lazily updated row
+//     maximum (O in tensor memory is rescaled only when a row's maximum grows
+//     by more than 8, so un-normalised p <= 2^8), and write P back into the
+//     S_j columns as two bf16 terms, P = P_hi + P_lo (P_lo = the rounding
+//     residual), consumed by two MMAs. A single bf16 P costs up to ~2^-9
+//     relative per weight, which on short causal rows with cancelling values
+//     exceeds an absolute error of 2e-3; the two-term P is accurate to ~2^-16.
 // The normalised output O / l is written once at the end.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -44,16 +47,20 @@ constexpr int kRows = 128;    // MMA M
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+constexpr int kStages = 3;   // K/V tile stages
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t kQ = 0;
 constexpr uint32_t kK0 = 32768;
-constexpr uint32_t kV0 = kK0 + 2 * 32768;
-constexpr uint32_t kP = kV0 + 2 * 32768;     // P_hi
-constexpr uint32_t kPlo = kP + 32768;         // P_lo
-constexpr uint32_t kBars = kPlo + 32768;  // 8 mbarriers
-constexpr uint32_t kMisc = kBars + 64;  // tmem slot, abort flag
-constexpr uint32_t kSmemBytes = kMisc + 64 + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 256;     // S: 0..127, O: 128..255
+constexpr uint32_t kV0 = kK0 + kStages * 32768;
+constexpr uint32_t kBars = kV0 + kStages * 32768;  // 16 mbarriers
+constexpr uint32_t kMisc = kBars + 128;            // tmem slot, abort flag
+constexpr uint32_t kXch = kMisc + 64;              // [2][2][128] floats: row-maximum exchange
+                                                   // by tile parity (then the row sums)
+// The dynamic shared memory base must be 1024-byte aligned (the swizzle atoms
+// of TMA and of the matrix descriptors); the kernel checks it.
+constexpr uint32_t kSmemBytes = kXch + 2048;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+constexpr uint32_t kTmemCols = 512;  // S0: 0..127, S1: 128..255, O: 256..383
 
 struct PrefillParams {
     uint16_t* out;
@@ -88,25 +95,33 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigne
     }
 }
 
+__device__ __forceinline__ void named_bar(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 template <int G>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(288, 1)
 pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
     constexpr int QT = kRows / G;  // chunk tokens per CTA
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char* sm = smem_raw + ((1024u - (pa::smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char* sm = smem_raw;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-    uint64_t* kv_full = bars;      // [2]
-    uint64_t* s_full = bars + 2;
-    uint64_t* p_full = bars + 3;   // 4 arrivals: one per softmax warp
-    uint64_t* pv_done = bars + 4;
-    uint64_t* drain = bars + 5;
+    uint64_t* kv_full = bars;      // [kStages]
+    uint64_t* s_full = bars + 4;   // [2]
+    uint64_t* p_full = bars + 6;   // [2], 8 arrivals each (one per softmax warp)
+    uint64_t* pv_done = bars + 8;
+    uint64_t* drain = bars + 9;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
 
     const int qt = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = P.n_heads, Hk = P.n_kv_heads, h0 = kvh * G;
+    if (pa::smem_u32(smem_raw) & 1023u) {  // never expected; refuse rather than mis-swizzle
+        if (threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_LAYOUT);
+        return;
+    }
     const int q0 = P.qsl[s];
     const int L = P.qsl[s + 1] - q0;
     const int i0 = qt * QT;
@@ -122,10 +137,11 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     const int n_kt = p_last / kKT + 1;
 
     if (threadIdx.x == 0) {
-        pa::mbar_init(&kv_full[0], 1);
-        pa::mbar_init(&kv_full[1], 1);
-        pa::mbar_init(s_full, 1);
-        pa::mbar_init(p_full, 4);
+        for (int i = 0; i < kStages; ++i) pa::mbar_init(&kv_full[i], 1);
+        pa::mbar_init(&s_full[0], 1);
+        pa::mbar_init(&s_full[1], 1);
+        pa::mbar_init(&p_full[0], 8);
+        pa::mbar_init(&p_full[1], 8);
         pa::mbar_init(pv_done, 1);
         pa::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -151,21 +167,23 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = *tslot;
-    const uint32_t tS = tbase, tO = tbase + 128;
+    const uint32_t tO = tbase + 256;
 
     constexpr uint32_t ID_QK = tc::idesc_bf16_f32(128, 128, 0, 0);
     constexpr uint32_t ID_PV = tc::idesc_bf16_f32(128, 128, 0, 1);
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------- issuer
         const int32_t* trow = P.tables + (size_t)s * P.max_blocks;
         int ids = -1;  // lane l: block id of block 32*group + l
-        auto load_ids = [&](int group) {
-            const int blk = group * 32 + lane;
-            ids = blk < nblk ? trow[blk] : -1;
-        };
+        int ids_group = -1;
         auto issue_tma = [&](int j) {  // warp-collective
-            const int st = j & 1;
+            if ((j >> 2) != ids_group) {
+                ids_group = j >> 2;
+                const int blk = ids_group * 32 + lane;
+                ids = blk < nblk ? trow[blk] : -1;
+            }
+            const int st = j % kStages;
             int y[kBPT];
 #pragma unroll
             for (int b = 0; b < kBPT; ++b) {
@@ -192,85 +210,94 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             }
             __syncwarp();
         };
-        auto issue_pv = [&](int j) {  // O += P_hi,j V_j + P_lo,j V_j
+        auto issue_qk = [&](int j) {  // S_{j&1} = Q K_j^T
             if (lane == 0) {
-                const uint32_t vs = pa::smem_u32(sm + kV0 + (j & 1) * 32768);
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint32_t ps = pa::smem_u32(sm + (part ? kPlo : kP));
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t ad = tc::smem_desc(ps + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                        const uint64_t bd = tc::smem_desc(vs + ks * 2048, 16384, 1024);
-                        tc::mma_bf16(tO, ad, bd, ID_PV, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
-                    }
-                }
-                tc::mma_commit(pv_done);
-            }
-            __syncwarp();
-        };
-        load_ids(0);
-        issue_tma(0);
-        if (n_kt > 1) issue_tma(1);
-        bool ok = true;
-        for (int j = 0; j < n_kt && ok; ++j) {
-            ok = wait_bar(&kv_full[j & 1], (uint32_t)((j >> 1) & 1), P.err, abort_flag);
-            if (ok && j > 0) ok = wait_bar(p_full, (uint32_t)((j - 1) & 1), P.err, abort_flag);
-            if (!ok) break;
-            tc::fence_after_sync();
-            if (j > 0) issue_pv(j - 1);
-            if (lane == 0) {  // S = Q K_j^T
                 const uint32_t qs = pa::smem_u32(sm + kQ);
-                const uint32_t kst = pa::smem_u32(sm + kK0 + (j & 1) * 32768);
+                const uint32_t kst = pa::smem_u32(sm + kK0 + (j % kStages) * 32768);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t ad = tc::smem_desc(qs + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
                     const uint64_t bd = tc::smem_desc(kst + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                    tc::mma_bf16(tS, ad, bd, ID_QK, ks > 0 ? 1u : 0u);
+                    tc::mma_bf16(tbase + (j & 1) * 128, ad, bd, ID_QK, ks > 0 ? 1u : 0u);
                 }
-                tc::mma_commit(s_full);
+                tc::mma_commit(&s_full[j & 1]);
             }
             __syncwarp();
-            if (j >= 1 && j + 1 < n_kt) {
-                // stage (j+1)&1 was last read by PV_{j-1}: wait for it, then refill
-                ok = wait_bar(pv_done, (uint32_t)((j - 1) & 1), P.err, abort_flag);
-                if (!ok) break;
-                if (((j + 1) & 3) == 0) load_ids((j + 1) >> 2);
-                issue_tma(j + 1);
+        };
+        auto issue_pv = [&](int j) {  // O += P_hi,j V_j + P_lo,j V_j, P in the S_{j&1} columns
+            if (lane == 0) {
+                const uint32_t vs = pa::smem_u32(sm + kV0 + (j % kStages) * 32768);
+                const uint32_t pcol = tbase + (j & 1) * 128;
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t bd = tc::smem_desc(vs + ks * 2048, 16384, 1024);
+                        tc::mma_bf16_ts(tO, pcol + part * 64 + ks * 8, bd, ID_PV,
+                                        (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+                    }
+                tc::mma_commit(pv_done);
             }
-        }
-        if (ok) ok = wait_bar(p_full, (uint32_t)((n_kt - 1) & 1), P.err, abort_flag);
+            __syncwarp();
+        };
+        for (int j = 0; j < kStages && j < n_kt; ++j) issue_tma(j);
+        bool ok = wait_bar(&kv_full[0], 0, P.err, abort_flag);
         if (ok) {
             tc::fence_after_sync();
-            issue_pv(n_kt - 1);
+            issue_qk(0);
+        }
+        for (int j = 0; j < n_kt && ok; ++j) {
+            if (j + 1 < n_kt) {  // S_{(j+1)&1} was freed by PV_{j-1} (waited below)
+                ok = wait_bar(&kv_full[(j + 1) % kStages], (uint32_t)(((j + 1) / kStages) & 1), P.err, abort_flag);
+                if (!ok) break;
+                tc::fence_after_sync();
+                issue_qk(j + 1);
+            }
+            ok = wait_bar(&p_full[j & 1], (uint32_t)((j >> 1) & 1), P.err, abort_flag);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_pv(j);
+            ok = wait_bar(pv_done, (uint32_t)(j & 1), P.err, abort_flag);
+            if (!ok) break;
+            if (j + kStages < n_kt) issue_tma(j + kStages);  // stage j%3 is free: QK_j and PV_j done
         }
         // drain: every issued MMA has completed before the CTA can release its
         // shared and tensor memory (bounded wait)
         if (lane == 0) tc::mma_commit(drain);
         __syncwarp();
         pa::mbar_wait(drain, 0, nullptr, 10000000ull);
-        if (!ok) {  // TMA copies may still be landing: bounded waits on both stages
-            pa::mbar_wait(&kv_full[0], 0, nullptr, 10000000ull);
-            pa::mbar_wait(&kv_full[1], 0, nullptr, 10000000ull);
+        if (!ok) {  // TMA copies may still be landing: bounded waits on every stage
+            for (int i = 0; i < kStages; ++i) {
+                pa::mbar_wait(&kv_full[i], 0, nullptr, 5000000ull);
+                pa::mbar_wait(&kv_full[i], 1, nullptr, 5000000ull);
+            }
         }
     } else {
         // ------------------------------------------------- softmax warps
-        const int r = threadIdx.x;  // matrix row = TMEM lane
+        // warp w (0..7) serves TMEM lanes 32*(w%4).. (rows) and key columns
+        // 64*(w/4) .. +63 of every S tile; the two threads of a row exchange
+        // their partial maxima through shared memory. After a failed wait
+        // (timeout) the warps keep iterating without waiting, so that all of
+        // them pass the same named barriers.
+        const int r = threadIdx.x & 127;  // matrix row = TMEM lane
+        const int half = warp >> 2;       // which 64 key columns
         const int i = i0 + r / G;
         const int pos = first_pos + i;  // this row's position (padding rows: beyond the chunk)
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        float m_used = -INFINITY, l = 0.f;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        float* xch = reinterpret_cast<float*>(sm + kXch);  // [2][2][128]
+        const float sc = P.scale_log2;
+        float m_used = -INFINITY, l = 0.f;  // l: partial sum over this thread's columns
         bool ok = true;
         for (int j = 0; j < n_kt; ++j) {
-            if (ok) ok = wait_bar(s_full, (uint32_t)(j & 1), P.err, abort_flag);
+            if (ok) ok = wait_bar(&s_full[j & 1], (uint32_t)((j >> 1) & 1), P.err, abort_flag);
             ok = __all_sync(kFull, ok);
-            if (!ok) break;
             tc::fence_after_sync();
-            float sv[kKT];
+            const uint32_t tS = tbase + (j & 1) * 128 + lane_base;
+            float sv[64];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t raw[32];
-                tc::tmem_ld32(tS + lane_base + c * 32, raw);
+                tc::tmem_ld32(tS + half * 64 + c * 32, raw);
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int k = 0; k < 32; ++k) sv[c * 32 + k] = __uint_as_float(raw[k]);
@@ -280,72 +307,76 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             const int kb = j * kKT;
             if ((ctx & (kBS - 1)) && ctx > kb && ctx < kb + kKT) {
                 const int z0 = ctx - kb, z1 = min(((ctx + kBS - 1) & ~(kBS - 1)) - kb, kKT);
-                unsigned char* vs = sm + kV0 + (j & 1) * 32768;
-                for (int e = r; e < (z1 - z0) * 16; e += 128) {
+                unsigned char* vs = sm + kV0 + (j % kStages) * 32768;
+                for (int e = threadIdx.x; e < (z1 - z0) * 16; e += 256) {
                     const int row = z0 + (e >> 4), g = (e >> 3) & 1, c = e & 7;
                     *reinterpret_cast<uint4*>(vs + g * 16384 + tc::sw128_offset(row, c)) = make_uint4(0, 0, 0, 0);
                 }
                 tc::fence_async_smem();
             }
-            // scale, causal mask, tile maximum
+            // causal mask (raw scores; scale > 0 keeps the order), partial maximum
+            const int kc = kb + half * 64;
+            const bool need_mask = kc + 63 > pos;
             float tmax = -INFINITY;
-            const bool need_mask = kb + kKT - 1 > pos;
 #pragma unroll
-            for (int c = 0; c < kKT; ++c) {
-                float x = sv[c] * P.scale_log2;
-                if (need_mask && kb + c > pos) x = -INFINITY;
-                sv[c] = x;
-                tmax = fmaxf(tmax, x);
+            for (int c = 0; c < 64; ++c) {
+                if (need_mask && kc + c > pos) sv[c] = -INFINITY;
+                tmax = fmaxf(tmax, sv[c]);
             }
+            float* xj = xch + (j & 1) * 256;
+            xj[half * 128 + r] = tmax;
+            named_bar(1, 256);
+            tmax = fmaxf(tmax, xj[(half ^ 1) * 128 + r]) * sc;
             const bool rescale = tmax > m_used + kRescaleThreshold;
             float alpha = 1.f;
             if (rescale) {
                 alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
                 m_used = tmax;
             }
-            // PV_{j-1} must be done before P is overwritten or O is rescaled
-            if (j > 0) {
+            // p = 2^(s*scale - m) as P_hi + P_lo (packed bf16 pairs) into the S_j columns
+            float psum = 0.f;
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int w = 0; w < 32; ++w) {
+                const float a = pa::fast_exp2(fmaf(sv[2 * w], sc, -m_used));
+                const float b = pa::fast_exp2(fmaf(sv[2 * w + 1], sc, -m_used));
+                psum += a + b;
+                hi[w] = pa::float2_to_bf16x2(a, b);
+                const float2 h2 = pa::bf16x2_to_float2(hi[w]);
+                lo[w] = pa::float2_to_bf16x2(a - h2.x, b - h2.y);
+            }
+            tc::tmem_st32(tS + half * 32, hi);
+            tc::tmem_st32(tS + 64 + half * 32, lo);
+            l = l * alpha + psum;
+            // a larger maximum rescales O (each half of the row's O columns by
+            // one thread): PV_{j-1} must have landed in O first
+            if (j > 0 && __any_sync(kFull, rescale)) {
                 if (ok) ok = wait_bar(pv_done, (uint32_t)((j - 1) & 1), P.err, abort_flag);
                 ok = __all_sync(kFull, ok);
-                if (!ok) break;
                 tc::fence_after_sync();
-                if (__any_sync(kFull, rescale)) {
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t raw[32];
-                        tc::tmem_ld32(tO + lane_base + c * 32, raw);
-                        tc::tmem_wait_ld();
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t raw[32];
+                    const uint32_t ta = tO + lane_base + half * 64 + c * 32;
+                    tc::tmem_ld32(ta, raw);
+                    tc::tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) raw[k] = __float_as_uint(__uint_as_float(raw[k]) * alpha);
-                        tc::tmem_st32(tO + lane_base + c * 32, raw);
-                    }
-                    tc::tmem_wait_st();
+                    for (int k = 0; k < 32; ++k) raw[k] = __float_as_uint(__uint_as_float(raw[k]) * alpha);
+                    tc::tmem_st32(ta, raw);
                 }
             }
-            // p = 2^(s - m), written as P_hi + P_lo (bf16 each), 8 keys per 16-byte chunk
-            float psum = 0.f;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float a = pa::fast_exp2(sv[c * 8 + 2 * k] - m_used);
-                    const float b = pa::fast_exp2(sv[c * 8 + 2 * k + 1] - m_used);
-                    psum += a + b;
-                    hi[k] = pa::float2_to_bf16x2(a, b);
-                    const float2 h2 = pa::bf16x2_to_float2(hi[k]);
-                    lo[k] = pa::float2_to_bf16x2(a - h2.x, b - h2.y);
-                }
-                const uint32_t off = (c >> 3) * 16384 + tc::sw128_offset(r, c & 7);
-                *reinterpret_cast<uint4*>(sm + kP + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(sm + kPlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-            l = l * alpha + psum;
-            tc::fence_async_smem();
+            tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) pa::mbar_arrive(p_full);
+            if (lane == 0) pa::mbar_arrive(&p_full[j & 1]);
         }
+        tc::tmem_wait_st();  // no store may be pending when the columns are released
+        // combine the two partial sums of each row (in the exchange slot of
+        // tile n_kt - 2, whose readers have all passed the last barrier)
+        float* xl = xch + (n_kt & 1) * 256;
+        xl[half * 128 + r] = l;
+        named_bar(1, 256);
+        l += xl[(half ^ 1) * 128 + r];
         if (ok) ok = wait_bar(pv_done, (uint32_t)((n_kt - 1) & 1), P.err, abort_flag);
         ok = __all_sync(kFull, ok);
         if (ok) {
@@ -353,9 +384,9 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             const float inv = 1.f / l;
             uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t raw[32];
-                tc::tmem_ld32(tO + lane_base + c * 32, raw);
+                tc::tmem_ld32(tO + lane_base + half * 64 + c * 32, raw);
                 tc::tmem_wait_ld();
                 if (i < L) {
 #pragma unroll
@@ -365,7 +396,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                         w.y = pa::float2_to_bf16x2(__uint_as_float(raw[k + 2]) * inv, __uint_as_float(raw[k + 3]) * inv);
                         w.z = pa::float2_to_bf16x2(__uint_as_float(raw[k + 4]) * inv, __uint_as_float(raw[k + 5]) * inv);
                         w.w = pa::float2_to_bf16x2(__uint_as_float(raw[k + 6]) * inv, __uint_as_float(raw[k + 7]) * inv);
-                        dst[(c * 32 + k) / 8] = w;
+                        dst[(half * 64 + c * 32 + k) / 8] = w;
                     }
                 }
             }
@@ -391,7 +422,7 @@ int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtenso
     }
     constexpr int QT = kRows / G;
     dim3 grid((max_chunk_len + QT - 1) / QT, Pp.n_kv_heads, n_seqs);
-    kern<<<grid, 160, kSmemBytes, stream>>>(Pp, tk, tv);
+    kern<<<grid, 288, kSmemBytes, stream>>>(Pp, tk, tv);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

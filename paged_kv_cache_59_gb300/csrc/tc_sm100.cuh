@@ -151,3 +151,17 @@ __host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t chunk
 // Returns false if the driver entry point is unavailable or rejects it.
 bool pa_make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                           uint64_t row_stride_bytes, uint32_t box_x, uint32_t box_y);
+
+namespace tc {
+// D[tmem] (+)= A[tmem] x B[smem]^T, K = 16, A read from tensor memory: row i
+// of A in lane i, two bf16 of consecutive k packed per 32-bit column.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+}  // namespace tc
