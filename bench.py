@@ -65,6 +65,23 @@ def dist_env():
     return world, rank, local
 
 
+def reduce_max_ms(local_ms: float, dist_mod=None, device=None) -> float:
+    """Slowest rank's elapsed time (the whole job ends when the last rank
+    does). A host-side timing reduction only: no data of the hot path crosses
+    ranks."""
+    if dist_mod is None or not dist_mod.is_initialized() or dist_mod.get_world_size() == 1:
+        return float(local_ms)
+    import torch
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device or "cpu")
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(bytes_per_step_per_rank: int, steps: int, world: int, t_max_ms: float) -> float:
+    """Weak scaling: every rank processes its own replica of the batch."""
+    return world * bytes_per_step_per_rank * steps / (t_max_ms / 1e3) / 1e9
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -304,13 +321,9 @@ def run_ours(args):
         clocks = sampler.stop()
         clocks["remeasured"] = True
 
-    t_max = total_ms
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = reduce_max_ms(total_ms, dist if world > 1 else None, dev)
     ms_per_step = t_max / args.steps
-    value = world * kv_bytes * args.steps / (t_max / 1e3) / 1e9
+    value = whole_job_gbps(kv_bytes, args.steps, world, t_max)
 
     # roofline of the decode call (partition kernel + merge kernel)
     dec_ms_sorted = sorted(dec_ms)
@@ -449,11 +462,7 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
     for _ in range(n):
         step()
     torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([dt], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
+    dt = reduce_max_ms((time.perf_counter() - t0) * 1e3, dist, dev) / 1e3
     return {"value": round(world * kv_bytes * n / dt / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(dt * 1e3 / n, 5),

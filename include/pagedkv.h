@@ -214,6 +214,13 @@ int pa_prefill_paged(void* out, const void* q, const void* k_pool, const void* v
  * and clears it. Synchronises with the device. */
 int pa_get_device_error(int* flags_out);
 
+/* Self-test of failure detection (no counterpart on the pages): launches a
+ * one-thread kernel that waits on an mbarrier nothing arrives on, bounded to
+ * limit_us microseconds (1 .. 10^7). The wait gives up, sets PA_DEVERR_TIMEOUT
+ * in the device error word and returns; the context stays usable. Used by
+ * the tests to show that every bounded wait ends without a fault or hang. */
+int pa_selftest_wait_timeout(int limit_us, pa_stream_t stream);
+
 /* Static string for a status code. */
 const char* pa_status_string(int status);
 

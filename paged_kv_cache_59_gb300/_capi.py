@@ -48,6 +48,7 @@ SIGNATURES = {
     "pa_prefill_paged": (i32, [vp, vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32,
                                i32, i32, vp]),
     "pa_get_device_error": (i32, [C.POINTER(C.c_int)]),
+    "pa_selftest_wait_timeout": (i32, [i32, vp]),
     "pa_status_string": (C.c_char_p, [i32]),
     "pa_bm_create": (vp, [i32, i32]),
     "pa_bm_destroy": (None, [vp]),

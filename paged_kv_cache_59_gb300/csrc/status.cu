@@ -50,3 +50,22 @@ extern "C" const char* pa_status_string(int status) {
         default: return "unknown status";
     }
 }
+
+// Self-test of the bounded waits: one thread waits on an mbarrier that
+// nothing arrives on, with a limit of `limit_us` microseconds. The wait must
+// give up, set PA_DEVERR_TIMEOUT and return, leaving the context usable.
+__global__ void pa_selftest_wait_kernel(unsigned long long limit_ns, unsigned int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    pa::mbar_init(&bar, 1);
+    pa::fence_mbar_init();
+    pa::mbar_wait(&bar, 0, err, limit_ns);  // phase 0 never completes
+}
+
+extern "C" int pa_selftest_wait_timeout(int limit_us, pa_stream_t stream) {
+    if (limit_us <= 0 || limit_us > 10000000) return PA_ERR_INVALID_ARG;
+    unsigned int* err = pa_device_error_ptr();
+    if (!err) return PA_ERR_CUDA;
+    pa_selftest_wait_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        (unsigned long long)limit_us * 1000ull, err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
