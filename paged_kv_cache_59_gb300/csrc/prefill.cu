@@ -9,28 +9,29 @@
 // positions; chunk row i sits at position p = ctx - L + i and
 //     out[i][h] = sum_{t <= p} softmax_t(scale * q[i][h] . K[t]) V[t].
 //
-// Design (GB300): one CTA per (query tile, KV head, sequence). The CTA's 128
-// matrix rows are QT = 128/G chunk tokens x the G query heads of the KV
-// head's group, so every K/V byte staged in shared memory feeds all G heads.
-// Per key tile j of 128 keys (8 blocks of 16):
+// Design (GB300). A query tile is 128 matrix rows = QT = 128/G chunk tokens x
+// the G query heads of one KV head's group, so every K/V byte staged in
+// shared memory feeds all G heads. One CTA owns two query tiles (A and B) of
+// the same (sequence, KV head): both use every K/V tile it loads, and the
+// tensor core alternates between them so that one tile's MMAs run while the
+// other tile's softmax works. Per key tile j of 128 keys (8 blocks of 16):
 //   - an issuer warp moves the 8 K and 8 V blocks with 2-D TMA loads into
-//     128B-swizzled shared memory (3 stages; blocks past the end of the
-//     sequence load out of bounds and arrive as zeros), and issues the MMAs:
-//     S_j = Q K_j^T (tcgen05.mma kind::f16, bf16 in, fp32 accumulator in
-//     tensor memory, M = N = 128) into one of two S buffers, so that QK of
-//     tile j+1 runs while the softmax warps work on tile j; then
-//     O += P_j V_j with P read from tensor memory and V as an MN-major
-//     shared-memory operand;
-//   - eight softmax warps read S_j: a row's 128 key columns are split
-//     between two threads of two warpgroups (64 each; partial row maxima
-//     are exchanged through shared memory). They apply the scale, the causal
-//     mask and an online softmax in fp32 (base 2) with a lazily updated row
-//     maximum (O in tensor memory is rescaled only when a row's maximum grows
-//     by more than 8, so un-normalised p <= 2^8), and write P back into the
-//     S_j columns as two bf16 terms, P = P_hi + P_lo (P_lo = the rounding
-//     residual), consumed by two MMAs. A single bf16 P costs up to ~2^-9
-//     relative per weight, which on short causal rows with cancelling values
-//     exceeds an absolute error of 2e-3; the two-term P is accurate to ~2^-16.
+//     128B-swizzled shared memory (two stages; blocks past the end of the
+//     sequence load out of bounds and arrive as zeros) and issues, per query
+//     tile X, S_X = Q_X K_j^T (tcgen05.mma kind::f16, bf16 in, fp32
+//     accumulator in tensor memory, M = N = 128) and, once X's softmax has
+//     written P, O_X += P V_j (P read from tensor memory, V as an MN-major
+//     shared-memory operand);
+//   - one softmax warpgroup per query tile (thread = row) reads S_X from
+//     tensor memory twice (row maximum, then exponentials), applies the
+//     scale, the causal mask and an online softmax in fp32 (base 2) with a
+//     lazily updated maximum (O_X is rescaled in tensor memory only when a
+//     row's maximum grows by more than 8, so un-normalised p <= 2^8), and
+//     writes P back into S_X's columns as two bf16 terms, P = P_hi + P_lo
+//     (P_lo = the rounding residual), consumed by two MMAs. A single bf16 P
+//     costs up to ~2^-9 relative per weight, which on short causal rows with
+//     cancelling values exceeds an absolute error of 2e-3; the two-term P is
+//     accurate to ~2^-16.
 // The normalised output O / l is written once at the end.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -39,28 +40,25 @@
 
 namespace {
 
-constexpr int kD = 128;       // head_dim (the only one built)
-constexpr int kBS = 16;       // tokens per block
-constexpr int kKT = 128;      // keys per key tile
+constexpr int kD = 128;          // head_dim (the only one built)
+constexpr int kBS = 16;          // tokens per block
+constexpr int kKT = 128;         // keys per key tile
 constexpr int kBPT = kKT / kBS;  // blocks per key tile
-constexpr int kRows = 128;    // MMA M
+constexpr int kRows = 128;       // MMA M
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-constexpr int kStages = 3;   // K/V tile stages
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t kQ = 0;
-constexpr uint32_t kK0 = 32768;
-constexpr uint32_t kV0 = kK0 + kStages * 32768;
-constexpr uint32_t kBars = kV0 + kStages * 32768;  // 16 mbarriers
+constexpr int kStages = 2;  // K/V tile stages
+// shared memory map; the dynamic shared memory base must be 1024-byte
+// aligned (swizzle atoms of TMA and of the matrix descriptors): checked
+constexpr uint32_t kQ = 0;                         // Q_A, Q_B: 2 x 32 KiB
+constexpr uint32_t kK0 = 2 * 32768;                // K stages
+constexpr uint32_t kV0 = kK0 + kStages * 32768;    // V stages
+constexpr uint32_t kBars = kV0 + kStages * 32768;  // mbarriers
 constexpr uint32_t kMisc = kBars + 128;            // tmem slot, abort flag
-constexpr uint32_t kXch = kMisc + 64;              // [2][2][128] floats: row-maximum exchange
-                                                   // by tile parity (then the row sums)
-// The dynamic shared memory base must be 1024-byte aligned (the swizzle atoms
-// of TMA and of the matrix descriptors); the kernel checks it.
-constexpr uint32_t kSmemBytes = kXch + 2048;
+constexpr uint32_t kSmemBytes = kMisc + 64;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-constexpr uint32_t kTmemCols = 512;  // S0: 0..127, S1: 128..255, O: 256..383
+constexpr uint32_t kTmemCols = 512;  // tile X: S at 256X, O at 256X + 128
 
 struct PrefillParams {
     uint16_t* out;
@@ -95,37 +93,32 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigne
     }
 }
 
-__device__ __forceinline__ void named_bar(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 template <int G>
 __global__ void __launch_bounds__(288, 1)
 pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
-    constexpr int QT = kRows / G;  // chunk tokens per CTA
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char* sm = smem_raw;
+    constexpr int QT = kRows / G;  // chunk tokens per query tile
+    extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
     uint64_t* kv_full = bars;      // [kStages]
-    uint64_t* s_full = bars + 4;   // [2]
-    uint64_t* p_full = bars + 6;   // [2], 8 arrivals each (one per softmax warp)
-    uint64_t* pv_done = bars + 8;
-    uint64_t* drain = bars + 9;
+    uint64_t* s_full = bars + 2;   // [2] per query tile
+    uint64_t* p_full = bars + 4;   // [2] per query tile, 4 arrivals (one per warp)
+    uint64_t* pv_done = bars + 6;  // [2] per query tile
+    uint64_t* drain = bars + 8;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
 
-    const int qt = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int qp = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = P.n_heads, Hk = P.n_kv_heads, h0 = kvh * G;
-    if (pa::smem_u32(smem_raw) & 1023u) {  // never expected; refuse rather than mis-swizzle
+    if (pa::smem_u32(sm) & 1023u) {  // never expected; refuse rather than mis-swizzle
         if (threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_LAYOUT);
         return;
     }
     const int q0 = P.qsl[s];
     const int L = P.qsl[s + 1] - q0;
-    const int i0 = qt * QT;
-    if (i0 >= L) return;  // CTA-uniform, before any barrier or TMEM use
+    const int i0 = qp * 2 * QT;  // first chunk token of query tile A; tile B follows
+    if (i0 >= L) return;         // CTA-uniform, before any barrier or TMEM use
     const int ctx = P.ctx[s];
     if (ctx < L) {  // the chunk must be in the cache already
         if (threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_CONTEXT);
@@ -133,16 +126,18 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     }
     const int nblk = min((ctx + kBS - 1) / kBS, P.max_blocks);
     const int first_pos = ctx - L;
-    const int p_last = first_pos + min(i0 + QT, L) - 1;
+    // both tiles walk the key tiles up to the last row of the pair (tile A's
+    // extra tiles beyond its own rows are fully masked)
+    const int p_last = first_pos + min(i0 + 2 * QT, L) - 1;
     const int n_kt = p_last / kKT + 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) pa::mbar_init(&kv_full[i], 1);
-        pa::mbar_init(&s_full[0], 1);
-        pa::mbar_init(&s_full[1], 1);
-        pa::mbar_init(&p_full[0], 8);
-        pa::mbar_init(&p_full[1], 8);
-        pa::mbar_init(pv_done, 1);
+        for (int x = 0; x < 2; ++x) {
+            pa::mbar_init(&s_full[x], 1);
+            pa::mbar_init(&p_full[x], 4);
+            pa::mbar_init(&pv_done[x], 1);
+        }
         pa::mbar_init(drain, 1);
         *abort_flag = 0;
         pa::fence_mbar_init();
@@ -151,15 +146,15 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         tc::tmem_alloc(tslot, kTmemCols);
         tc::tmem_relinquish();
     }
-    // ---- Q tile: row r = (chunk token i0 + r / G, head h0 + r % G), swizzled K-major
-    if (warp < 4) {
-        const int r = threadIdx.x;
-        const int i = i0 + r / G;
+    // ---- Q tiles: tile X row r = (chunk token i0 + X*QT + r/G, head h0 + r%G)
+    if (warp < 8) {
+        const int x = warp >> 2, r = threadIdx.x & 127;
+        const int i = i0 + x * QT + r / G;
         const uint4* src = reinterpret_cast<const uint4*>(P.q + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             const uint4 v = i < L ? src[c] : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sm + kQ + (c >> 3) * 16384 + tc::sw128_offset(r, c & 7)) = v;
+            *reinterpret_cast<uint4*>(sm + kQ + x * 32768 + (c >> 3) * 16384 + tc::sw128_offset(r, c & 7)) = v;
         }
     }
     tc::fence_async_smem();
@@ -167,7 +162,6 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = *tslot;
-    const uint32_t tO = tbase + 256;
 
     constexpr uint32_t ID_QK = tc::idesc_bf16_f32(128, 128, 0, 0);
     constexpr uint32_t ID_PV = tc::idesc_bf16_f32(128, 128, 0, 1);
@@ -210,33 +204,33 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             }
             __syncwarp();
         };
-        auto issue_qk = [&](int j) {  // S_{j&1} = Q K_j^T
+        auto issue_qk = [&](int x, int j) {  // S_x = Q_x K_j^T
             if (lane == 0) {
-                const uint32_t qs = pa::smem_u32(sm + kQ);
+                const uint32_t qs = pa::smem_u32(sm + kQ + x * 32768);
                 const uint32_t kst = pa::smem_u32(sm + kK0 + (j % kStages) * 32768);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t ad = tc::smem_desc(qs + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
                     const uint64_t bd = tc::smem_desc(kst + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                    tc::mma_bf16(tbase + (j & 1) * 128, ad, bd, ID_QK, ks > 0 ? 1u : 0u);
+                    tc::mma_bf16(tbase + x * 256, ad, bd, ID_QK, ks > 0 ? 1u : 0u);
                 }
-                tc::mma_commit(&s_full[j & 1]);
+                tc::mma_commit(&s_full[x]);
             }
             __syncwarp();
         };
-        auto issue_pv = [&](int j) {  // O += P_hi,j V_j + P_lo,j V_j, P in the S_{j&1} columns
+        auto issue_pv = [&](int x, int j) {  // O_x += P_hi V_j + P_lo V_j, P in S_x's columns
             if (lane == 0) {
                 const uint32_t vs = pa::smem_u32(sm + kV0 + (j % kStages) * 32768);
-                const uint32_t pcol = tbase + (j & 1) * 128;
+                const uint32_t pcol = tbase + x * 256;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint64_t bd = tc::smem_desc(vs + ks * 2048, 16384, 1024);
-                        tc::mma_bf16_ts(tO, pcol + part * 64 + ks * 8, bd, ID_PV,
+                        tc::mma_bf16_ts(tbase + x * 256 + 128, pcol + part * 64 + ks * 8, bd, ID_PV,
                                         (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
                     }
-                tc::mma_commit(pv_done);
+                tc::mma_commit(&pv_done[x]);
             }
             __syncwarp();
         };
@@ -244,22 +238,37 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         bool ok = wait_bar(&kv_full[0], 0, P.err, abort_flag);
         if (ok) {
             tc::fence_after_sync();
-            issue_qk(0);
+            issue_qk(0, 0);
+            issue_qk(1, 0);
         }
         for (int j = 0; j < n_kt && ok; ++j) {
-            if (j + 1 < n_kt) {  // S_{(j+1)&1} was freed by PV_{j-1} (waited below)
-                ok = wait_bar(&kv_full[(j + 1) % kStages], (uint32_t)(((j + 1) / kStages) & 1), P.err, abort_flag);
-                if (!ok) break;
-                tc::fence_after_sync();
-                issue_qk(j + 1);
-            }
-            ok = wait_bar(&p_full[j & 1], (uint32_t)((j >> 1) & 1), P.err, abort_flag);
+            const uint32_t par = (uint32_t)(j & 1);
+            // tile A: PV_A(j) once its P is written, then QK_A(j+1) once PV_A(j)
+            // has read P out of S_A
+            ok = wait_bar(&p_full[0], par, P.err, abort_flag);
             if (!ok) break;
             tc::fence_after_sync();
-            issue_pv(j);
-            ok = wait_bar(pv_done, (uint32_t)(j & 1), P.err, abort_flag);
+            issue_pv(0, j);
+            if (j + 1 < n_kt) {
+                ok = wait_bar(&kv_full[(j + 1) % kStages], (uint32_t)(((j + 1) / kStages) & 1), P.err,
+                              abort_flag);
+                if (ok) ok = wait_bar(&pv_done[0], par, P.err, abort_flag);
+                if (!ok) break;
+                issue_qk(0, j + 1);
+            }
+            // tile B likewise
+            ok = wait_bar(&p_full[1], par, P.err, abort_flag);
             if (!ok) break;
-            if (j + kStages < n_kt) issue_tma(j + kStages);  // stage j%3 is free: QK_j and PV_j done
+            tc::fence_after_sync();
+            issue_pv(1, j);
+            if (j + 1 < n_kt) {
+                ok = wait_bar(&pv_done[1], par, P.err, abort_flag);
+                if (!ok) break;
+                issue_qk(1, j + 1);
+            }
+            // stage j%2 is free: both PVs of tile j are done (waited above,
+            // since j + 2 < n_kt implies j + 1 < n_kt)
+            if (j + kStages < n_kt) issue_tma(j + kStages);
         }
         // drain: every issued MMA has completed before the CTA can release its
         // shared and tensor memory (bounded wait)
@@ -273,120 +282,142 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             }
         }
     } else {
-        // ------------------------------------------------- softmax warps
-        // warp w (0..7) serves TMEM lanes 32*(w%4).. (rows) and key columns
-        // 64*(w/4) .. +63 of every S tile; the two threads of a row exchange
-        // their partial maxima through shared memory. After a failed wait
-        // (timeout) the warps keep iterating without waiting, so that all of
-        // them pass the same named barriers.
+        // --------------------------------------- softmax warpgroup of tile x
+        // warp w serves TMEM lanes 32*(w%4) .. +31 (rows). After a failed wait
+        // (timeout) the warps keep iterating without waiting.
+        const int x = warp >> 2;
         const int r = threadIdx.x & 127;  // matrix row = TMEM lane
-        const int half = warp >> 2;       // which 64 key columns
-        const int i = i0 + r / G;
+        const int i = i0 + x * QT + r / G;
         const int pos = first_pos + i;  // this row's position (padding rows: beyond the chunk)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        float* xch = reinterpret_cast<float*>(sm + kXch);  // [2][2][128]
+        const uint32_t tS = tbase + x * 256 + lane_base;
+        const uint32_t tO = tS + 128;
         const float sc = P.scale_log2;
-        float m_used = -INFINITY, l = 0.f;  // l: partial sum over this thread's columns
+        float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kt; ++j) {
-            if (ok) ok = wait_bar(&s_full[j & 1], (uint32_t)((j >> 1) & 1), P.err, abort_flag);
+            if (ok) ok = wait_bar(&s_full[x], (uint32_t)(j & 1), P.err, abort_flag);
             ok = __all_sync(kFull, ok);
             tc::fence_after_sync();
-            const uint32_t tS = tbase + (j & 1) * 128 + lane_base;
-            float sv[64];
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t raw[32];
-                tc::tmem_ld32(tS + half * 64 + c * 32, raw);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 32; ++k) sv[c * 32 + k] = __uint_as_float(raw[k]);
-            }
-            // V rows of the sequence's last, partial block hold whatever the pool
-            // has there: zero them so that p = 0 never meets a NaN
             const int kb = j * kKT;
-            if ((ctx & (kBS - 1)) && ctx > kb && ctx < kb + kKT) {
+            // V rows of the sequence's last, partial block hold whatever the pool
+            // has there: zero them so that p = 0 never meets a NaN (tile A's
+            // warpgroup, before PV_A(j), the first PV reading V_j)
+            if (x == 0 && (ctx & (kBS - 1)) && ctx > kb && ctx < kb + kKT) {
                 const int z0 = ctx - kb, z1 = min(((ctx + kBS - 1) & ~(kBS - 1)) - kb, kKT);
                 unsigned char* vs = sm + kV0 + (j % kStages) * 32768;
-                for (int e = threadIdx.x; e < (z1 - z0) * 16; e += 256) {
+                for (int e = r; e < (z1 - z0) * 16; e += 128) {
                     const int row = z0 + (e >> 4), g = (e >> 3) & 1, c = e & 7;
                     *reinterpret_cast<uint4*>(vs + g * 16384 + tc::sw128_offset(row, c)) = make_uint4(0, 0, 0, 0);
                 }
                 tc::fence_async_smem();
             }
-            // causal mask (raw scores; scale > 0 keeps the order), partial maximum
-            const int kc = kb + half * 64;
-            const bool need_mask = kc + 63 > pos;
+            const bool need_mask = kb + kKT - 1 > pos;
+            // pass 1: causal mask and row maximum of the raw scores (only the
+            // key tiles that reach past a row's position need the mask)
             float tmax = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                if (need_mask && kc + c > pos) sv[c] = -INFINITY;
-                tmax = fmaxf(tmax, sv[c]);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t raw[32];
+                tc::tmem_ld32(tS + c * 32, raw);
+                tc::tmem_wait_ld();
+                if (need_mask) {
+                    const int lim = pos - kb - c * 32;  // keys k <= lim are visible
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        if (k <= lim) tmax = fmaxf(tmax, __uint_as_float(raw[k]));
+                } else {
+                    float m0 = __uint_as_float(raw[0]), m1 = __uint_as_float(raw[1]);
+#pragma unroll
+                    for (int k = 2; k < 32; k += 2) {
+                        m0 = fmaxf(m0, __uint_as_float(raw[k]));
+                        m1 = fmaxf(m1, __uint_as_float(raw[k + 1]));
+                    }
+                    tmax = fmaxf(tmax, fmaxf(m0, m1));
+                }
             }
-            float* xj = xch + (j & 1) * 256;
-            xj[half * 128 + r] = tmax;
-            named_bar(1, 256);
-            tmax = fmaxf(tmax, xj[(half ^ 1) * 128 + r]) * sc;
+            tmax *= sc;
             const bool rescale = tmax > m_used + kRescaleThreshold;
             float alpha = 1.f;
             if (rescale) {
                 alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
                 m_used = tmax;
             }
-            // p = 2^(s*scale - m) as P_hi + P_lo (packed bf16 pairs) into the S_j columns
+            // pass 2: p = 2^(s*scale - m). P_hi of key chunk c (32 keys) goes to
+            // columns 16c.. (scores already read); P_lo of chunk c goes to
+            // columns 64 + 16c, which hold score chunks 2 and 3: it is written
+            // once those have been read (chunks 0, 1 after reading chunk 2;
+            // chunks 2, 3 after reading chunk 3).
             float psum = 0.f;
-            uint32_t hi[32], lo[32];
+            uint32_t lo_a[32], lo_b[16];
+            auto exps = [&](int c, uint32_t* hi, uint32_t* lo) {
+                uint32_t raw[32];
+                tc::tmem_ld32(tS + c * 32, raw);
+                tc::tmem_wait_ld();
 #pragma unroll
-            for (int w = 0; w < 32; ++w) {
-                const float a = pa::fast_exp2(fmaf(sv[2 * w], sc, -m_used));
-                const float b = pa::fast_exp2(fmaf(sv[2 * w + 1], sc, -m_used));
-                psum += a + b;
-                hi[w] = pa::float2_to_bf16x2(a, b);
-                const float2 h2 = pa::bf16x2_to_float2(hi[w]);
-                lo[w] = pa::float2_to_bf16x2(a - h2.x, b - h2.y);
+                const int lim = pos - kb - c * 32;  // keys k <= lim are visible
+                for (int w = 0; w < 16; ++w) {
+                    float a = fmaf(__uint_as_float(raw[2 * w]), sc, -m_used);
+                    float b = fmaf(__uint_as_float(raw[2 * w + 1]), sc, -m_used);
+                    if (need_mask) {
+                        if (2 * w > lim) a = -INFINITY;
+                        if (2 * w + 1 > lim) b = -INFINITY;
+                    }
+                    a = pa::fast_exp2(a);
+                    b = pa::fast_exp2(b);
+                    psum += a + b;
+                    hi[w] = pa::float2_to_bf16x2(a, b);
+                    const float2 h2 = pa::bf16x2_to_float2(hi[w]);
+                    lo[w] = pa::float2_to_bf16x2(a - h2.x, b - h2.y);
+                }
+            };
+            {
+                uint32_t hi[16];
+                exps(0, hi, lo_a);
+                tc::tmem_st16(tS + 0, hi);
+                exps(1, hi, lo_a + 16);
+                tc::tmem_st16(tS + 16, hi);
+                exps(2, hi, lo_b);  // score chunk 2 (columns 64..95) is now read
+                tc::tmem_st16(tS + 32, hi);
+                tc::tmem_st16(tS + 64, lo_a);
+                tc::tmem_st16(tS + 80, lo_a + 16);
+                exps(3, hi, lo_a);  // score chunk 3 (columns 96..127) is now read
+                tc::tmem_st16(tS + 48, hi);
+                tc::tmem_st16(tS + 96, lo_b);
+                tc::tmem_st16(tS + 112, lo_a);
             }
-            tc::tmem_st32(tS + half * 32, hi);
-            tc::tmem_st32(tS + 64 + half * 32, lo);
             l = l * alpha + psum;
-            // a larger maximum rescales O (each half of the row's O columns by
-            // one thread): PV_{j-1} must have landed in O first
+            // a larger maximum rescales O_x: PV_x(j-1) must have landed first
             if (j > 0 && __any_sync(kFull, rescale)) {
-                if (ok) ok = wait_bar(pv_done, (uint32_t)((j - 1) & 1), P.err, abort_flag);
+                if (ok) ok = wait_bar(&pv_done[x], (uint32_t)((j - 1) & 1), P.err, abort_flag);
                 ok = __all_sync(kFull, ok);
                 tc::fence_after_sync();
 #pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t raw[32];
-                    const uint32_t ta = tO + lane_base + half * 64 + c * 32;
-                    tc::tmem_ld32(ta, raw);
+                    tc::tmem_ld32(tO + c * 32, raw);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int k = 0; k < 32; ++k) raw[k] = __float_as_uint(__uint_as_float(raw[k]) * alpha);
-                    tc::tmem_st32(ta, raw);
+                    tc::tmem_st32(tO + c * 32, raw);
                 }
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) pa::mbar_arrive(&p_full[j & 1]);
+            if (lane == 0) pa::mbar_arrive(&p_full[x]);
         }
         tc::tmem_wait_st();  // no store may be pending when the columns are released
-        // combine the two partial sums of each row (in the exchange slot of
-        // tile n_kt - 2, whose readers have all passed the last barrier)
-        float* xl = xch + (n_kt & 1) * 256;
-        xl[half * 128 + r] = l;
-        named_bar(1, 256);
-        l += xl[(half ^ 1) * 128 + r];
-        if (ok) ok = wait_bar(pv_done, (uint32_t)((n_kt - 1) & 1), P.err, abort_flag);
+        if (ok) ok = wait_bar(&pv_done[x], (uint32_t)((n_kt - 1) & 1), P.err, abort_flag);
         ok = __all_sync(kFull, ok);
         if (ok) {
             tc::fence_after_sync();
             const float inv = 1.f / l;
             uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t raw[32];
-                tc::tmem_ld32(tO + lane_base + half * 64 + c * 32, raw);
+                tc::tmem_ld32(tO + c * 32, raw);
                 tc::tmem_wait_ld();
                 if (i < L) {
 #pragma unroll
@@ -396,7 +427,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                         w.y = pa::float2_to_bf16x2(__uint_as_float(raw[k + 2]) * inv, __uint_as_float(raw[k + 3]) * inv);
                         w.z = pa::float2_to_bf16x2(__uint_as_float(raw[k + 4]) * inv, __uint_as_float(raw[k + 5]) * inv);
                         w.w = pa::float2_to_bf16x2(__uint_as_float(raw[k + 6]) * inv, __uint_as_float(raw[k + 7]) * inv);
-                        dst[(half * 64 + c * 32 + k) / 8] = w;
+                        dst[(c * 32 + k) / 8] = w;
                     }
                 }
             }
@@ -421,7 +452,7 @@ int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtenso
         attr_done[dev] = true;
     }
     constexpr int QT = kRows / G;
-    dim3 grid((max_chunk_len + QT - 1) / QT, Pp.n_kv_heads, n_seqs);
+    dim3 grid((max_chunk_len + 2 * QT - 1) / (2 * QT), Pp.n_kv_heads, n_seqs);
     kern<<<grid, 288, kSmemBytes, stream>>>(Pp, tk, tv);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
