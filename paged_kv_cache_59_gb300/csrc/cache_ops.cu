@@ -25,6 +25,8 @@ reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ 
                          const int64_t* __restrict__ slots, long long n_chunks, int n_kv_heads,
                          int chunks_per_head, long long pool_slots, unsigned int* err) {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    pa::launch_dependents();     // the next kernel (decode, prefill) may be scheduled
+    pa::grid_dependency_wait();  // earlier readers of the pool are complete
     if (i >= n_chunks) return;
     const int per_token = n_kv_heads * chunks_per_head;
     const long long t = i / per_token;
@@ -85,11 +87,11 @@ extern "C" int pa_reshape_and_cache(const void* k, const void* v, void* k_pool, 
     const int threads = 256;
     const long long blocks = (n_chunks + threads - 1) / threads;
     if (blocks > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_pool),
-        static_cast<uint4*>(v_pool), slot_mapping, n_chunks, n_kv_heads, cph,
-        (long long)num_blocks * kBS, err);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return pa_launch_pdl(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                         reinterpret_cast<cudaStream_t>(stream), static_cast<const uint4*>(k),
+                         static_cast<const uint4*>(v), static_cast<uint4*>(k_pool),
+                         static_cast<uint4*>(v_pool), slot_mapping, n_chunks, n_kv_heads, cph,
+                         (long long)num_blocks * kBS, err);
 }
 
 extern "C" int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs,

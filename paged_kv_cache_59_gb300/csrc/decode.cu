@@ -149,6 +149,8 @@ pa_decode_partition_kernel(const DecodeParams P) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = P.n_heads, Hk = P.n_kv_heads;
     const int h0 = kvh * G;
+    pa::launch_dependents();     // the merge kernel may be scheduled now
+    pa::grid_dependency_wait();  // the previous kernel (e.g. the cache write) is complete
     const int ctx = P.ctx[b];
 
     if (ctx <= 0) {  // empty sequence: zero output rows, written once
@@ -455,6 +457,7 @@ pa_decode_merge_kernel(const DecodeParams P, int n_rows) {
     constexpr int PER = D / 32;
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);  // (seq, head) row
     const int lane = threadIdx.x & 31;
+    pa::grid_dependency_wait();  // every partition's partial is written
     if (row >= n_rows) return;
     const int H = P.n_heads;
     const int b = row / H;
@@ -491,6 +494,7 @@ pa_decode_merge_kernel(const DecodeParams P, int n_rows) {
 
 constexpr int kNW = 4;  // warps per CTA
 
+
 // Per (head_dim, group) launch shape. Twelve resident warps per SM (three
 // CTAs of four warps, three warps per scheduler) hide the latency of the
 // per-tile dependency chains best; that caps a thread at 168 registers, so
@@ -521,8 +525,7 @@ int launch_partition(const DecodeParams& P, int n_seqs, cudaStream_t stream) {
         attr_done[dev] = true;
     }
     dim3 grid(P.max_parts, P.n_kv_heads, n_seqs);
-    kern<<<grid, kNW * 32, SM::TOTAL, stream>>>(P);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return pa_launch_pdl(kern, grid, dim3(kNW * 32), SM::TOTAL, stream, P);
 }
 
 template <int D>
@@ -618,11 +621,8 @@ extern "C" int pa_decode_ex(void* out, const void* q, const void* k_pool, const 
     if (st != PA_OK || max_parts <= 1) return st;
     const int n_rows = n_seqs * n_heads;
     dim3 grid((n_rows + 3) / 4);
-    if (head_dim == 128)
-        pa_decode_merge_kernel<128><<<grid, 128, 0, s>>>(P, n_rows);
-    else
-        pa_decode_merge_kernel<64><<<grid, 128, 0, s>>>(P, n_rows);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (head_dim == 128) return pa_launch_pdl(pa_decode_merge_kernel<128>, grid, dim3(128), 0, s, P, n_rows);
+    return pa_launch_pdl(pa_decode_merge_kernel<64>, grid, dim3(128), 0, s, P, n_rows);
 }
 
 extern "C" int pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,

@@ -19,6 +19,26 @@ unsigned int* pa_device_error_ptr();
 // Host-side helpers shared by the entry points.
 static inline bool pa_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Host: launches `kern` with programmatic stream serialization, so its launch
+// and prologue overlap the tail of the previous kernel in the stream. The
+// kernel must call pa::grid_dependency_wait() before it touches memory that
+// earlier work in the stream reads or writes.
+template <typename... KArgs, typename... Args>
+static inline int pa_launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 namespace pa {
 
 __device__ __forceinline__ void set_error(unsigned int* err, unsigned int bit) {
@@ -118,6 +138,14 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float a, float b) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
     return r;
 }
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream serialization attribute may start while the previous kernel in the
+// stream is still running; grid_dependency_wait() blocks until that kernel
+// has completed and its memory is visible (a no-op for ordinary launches).
+// launch_dependents() lets the next such kernel be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
