@@ -14,24 +14,28 @@
 // shared memory feeds all G heads. One CTA owns two query tiles (A and B) of
 // the same (sequence, KV head): both use every K/V tile it loads, and the
 // tensor core alternates between them so that one tile's MMAs run while the
-// other tile's softmax works. Per key tile j of 128 keys (8 blocks of 16):
-//   - an issuer warp moves the 8 K and 8 V blocks with 2-D TMA loads into
-//     128B-swizzled shared memory (two stages; blocks past the end of the
-//     sequence load out of bounds and arrive as zeros) and issues, per query
-//     tile X, S_X = Q_X K_j^T (tcgen05.mma kind::f16, bf16 in, fp32
-//     accumulator in tensor memory, M = N = 128) and, once X's softmax has
-//     written P, O_X += P V_j (P read from tensor memory, V as an MN-major
-//     shared-memory operand);
+// other tile's softmax works. Per key tile j of 128 keys (8 blocks of 16),
+// four roles, each waiting only on mbarriers:
+//   - a producer warp moves the 8 K and 8 V blocks with 2-D TMA loads into
+//     128B-swizzled shared memory: three K stages and two V stages, each
+//     refilled as soon as the tensor core is done with it (blocks past the
+//     end of the sequence load out of bounds and arrive as zeros);
+//   - an MMA warp issues, per query tile X, S_X = Q_X K_j^T (tcgen05.mma
+//     kind::f16, bf16 in, fp32 accumulator in tensor memory, M = N = 128)
+//     and, once X's softmax has written P, O_X += P V_j (P read from tensor
+//     memory, V as an MN-major shared-memory operand). The MMAs of one
+//     thread execute in issue order, so S_X(j+1) is issued right behind the
+//     PV MMA that still reads P(j) out of the same columns;
 //   - one softmax warpgroup per query tile (thread = row) reads S_X from
-//     tensor memory twice (row maximum, then exponentials), applies the
-//     scale, the causal mask and an online softmax in fp32 (base 2) with a
-//     lazily updated maximum (O_X is rescaled in tensor memory only when a
-//     row's maximum grows by more than 8, so un-normalised p <= 2^8), and
-//     writes P back into S_X's columns as two bf16 terms, P = P_hi + P_lo
-//     (P_lo = the rounding residual), consumed by two MMAs. A single bf16 P
-//     costs up to ~2^-9 relative per weight, which on short causal rows with
-//     cancelling values exceeds an absolute error of 2e-3; the two-term P is
-//     accurate to ~2^-16.
+//     tensor memory (once whole for the row maximum, then by halves for the
+//     exponentials), applies the scale, the causal mask and an online
+//     softmax in fp32 (base 2) with a lazily updated maximum (O_X is
+//     rescaled in tensor memory only when a row's maximum grows by more than
+//     8, so un-normalised p <= 2^8), and writes P back into S_X's columns as
+//     two bf16 terms, P = P_hi + P_lo (P_lo = the rounding residual),
+//     consumed by two MMAs. A single bf16 P costs up to ~2^-9 relative per
+//     weight, which on short causal rows with cancelling values exceeds an
+//     absolute error of 2e-3; the two-term P is accurate to ~2^-16.
 // The normalised output O / l is written once at the end.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -48,14 +52,15 @@ constexpr int kRows = 128;       // MMA M
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-constexpr int kStages = 2;  // K/V tile stages
+constexpr int kKS = 3;  // K tile stages
+constexpr int kVS = 2;  // V tile stages
 // shared memory map; the dynamic shared memory base must be 1024-byte
 // aligned (swizzle atoms of TMA and of the matrix descriptors): checked
-constexpr uint32_t kQ = 0;                         // Q_A, Q_B: 2 x 32 KiB
-constexpr uint32_t kK0 = 2 * 32768;                // K stages
-constexpr uint32_t kV0 = kK0 + kStages * 32768;    // V stages
-constexpr uint32_t kBars = kV0 + kStages * 32768;  // mbarriers
-constexpr uint32_t kMisc = kBars + 128;            // tmem slot, abort flag
+constexpr uint32_t kQ = 0;                      // Q_A, Q_B: 2 x 32 KiB
+constexpr uint32_t kK0 = 2 * 32768;             // K stages
+constexpr uint32_t kV0 = kK0 + kKS * 32768;     // V stages
+constexpr uint32_t kBars = kV0 + kVS * 32768;   // mbarriers
+constexpr uint32_t kMisc = kBars + 256;            // tmem slot, abort flag
 constexpr uint32_t kSmemBytes = kMisc + 64;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr uint32_t kTmemCols = 512;  // tile X: S at 256X, O at 256X + 128
@@ -74,6 +79,13 @@ struct PrefillParams {
     int oob_row;  // a TMA row coordinate past the end of the pool (zero fill)
     unsigned int* err;
 };
+
+// max of three floats in one instruction (sm_100 family)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigned int* err,
                                          volatile int* abort_flag) {
@@ -94,17 +106,20 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigne
 }
 
 template <int G>
-__global__ void __launch_bounds__(288, 1)
+__global__ void __launch_bounds__(320, 1)
 pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
     constexpr int QT = kRows / G;  // chunk tokens per query tile
     extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-    uint64_t* kv_full = bars;      // [kStages]
-    uint64_t* s_full = bars + 2;   // [2] per query tile
-    uint64_t* p_full = bars + 4;   // [2] per query tile, 4 arrivals (one per warp)
-    uint64_t* pv_done = bars + 6;  // [2] per query tile
-    uint64_t* drain = bars + 8;
+    uint64_t* k_full = bars;        // [kKS] K tile landed
+    uint64_t* k_free = bars + 3;    // [kKS] both QKs that read the K stage are done
+    uint64_t* v_full = bars + 6;    // [kVS] V tile landed
+    uint64_t* v_free = bars + 8;    // [kVS] PV_B, the last reader of the V stage, is done
+    uint64_t* s_full = bars + 10;   // [2] per query tile
+    uint64_t* p_full = bars + 12;   // [2] per query tile, 4 arrivals (one per warp)
+    uint64_t* pv_done = bars + 14;  // [2] per query tile
+    uint64_t* drain = bars + 16;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
 
@@ -132,7 +147,14 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     const int n_kt = p_last / kKT + 1;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) pa::mbar_init(&kv_full[i], 1);
+        for (int i = 0; i < kKS; ++i) {
+            pa::mbar_init(&k_full[i], 1);
+            pa::mbar_init(&k_free[i], 1);
+        }
+        for (int i = 0; i < kVS; ++i) {
+            pa::mbar_init(&v_full[i], 1);
+            pa::mbar_init(&v_free[i], 1);
+        }
         for (int x = 0; x < 2; ++x) {
             pa::mbar_init(&s_full[x], 1);
             pa::mbar_init(&p_full[x], 4);
@@ -166,48 +188,70 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     constexpr uint32_t ID_QK = tc::idesc_bf16_f32(128, 128, 0, 0);
     constexpr uint32_t ID_PV = tc::idesc_bf16_f32(128, 128, 0, 1);
 
-    if (warp == 8) {
-        // ------------------------------------------------------- issuer
+    if (warp == 9) {
+        // ------------------------------------------------------- TMA producer
+        // K(j) goes to K stage j%3 once both QKs of K(j-3) are done (k_free);
+        // V(j) to V stage j%2 once PV_B(j-2), the last reader of V(j-2), is
+        // done. K(j+1) is issued before V(j): its stage frees first.
         const int32_t* trow = P.tables + (size_t)s * P.max_blocks;
-        int ids = -1;  // lane l: block id of block 32*group + l
-        int ids_group = -1;
-        auto issue_tma = [&](int j) {  // warp-collective
-            if ((j >> 2) != ids_group) {
-                ids_group = j >> 2;
-                const int blk = ids_group * 32 + lane;
-                ids = blk < nblk ? trow[blk] : -1;
+        struct Ids { int ids = -1, group = -1; };  // block ids of key tiles 4g..4g+3, one per lane
+        Ids idk, idv;
+        auto issue_tile = [&](Ids& w, const CUtensorMap* map, unsigned char* dst, uint64_t* bar, int j) {
+            if ((j >> 2) != w.group) {  // warp-collective
+                w.group = j >> 2;
+                const int blk = w.group * 32 + lane;
+                w.ids = blk < nblk ? trow[blk] : -1;
             }
-            const int st = j % kStages;
             int y[kBPT];
 #pragma unroll
             for (int b = 0; b < kBPT; ++b) {
-                const int bid = __shfl_sync(kFull, ids, (j & 3) * kBPT + b);
+                const int bid = __shfl_sync(kFull, w.ids, (j & 3) * kBPT + b);
                 const int blk = j * kBPT + b;
                 bool ok = blk < nblk;
                 if (ok && (bid < 0 || bid >= P.num_blocks)) {
                     if (lane == 0) pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
                     ok = false;
                 }
-                y[b] = ok ? (bid * Hk + kvh) * kBS : P.oob_row;
+                y[b] = ok ? (bid * Hk + kvh) * kBS : P.oob_row;  // out of range: zero fill
             }
             if (lane == 0) {
-                pa::mbar_arrive_expect_tx(&kv_full[st], 2 * 32768);
-                unsigned char* ks = sm + kK0 + st * 32768;
-                unsigned char* vs = sm + kV0 + st * 32768;
+                pa::mbar_arrive_expect_tx(bar, 32768);
 #pragma unroll
                 for (int b = 0; b < kBPT; ++b)
 #pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        tc::tma_load_2d(ks + g * 16384 + b * 2048, &tmK, g * 64, y[b], &kv_full[st]);
-                        tc::tma_load_2d(vs + g * 16384 + b * 2048, &tmV, g * 64, y[b], &kv_full[st]);
-                    }
+                    for (int g = 0; g < 2; ++g) tc::tma_load_2d(dst + g * 16384 + b * 2048, map, g * 64, y[b], bar);
             }
             __syncwarp();
         };
+        auto issue_k = [&](int j) { issue_tile(idk, &tmK, sm + kK0 + (j % kKS) * 32768, &k_full[j % kKS], j); };
+        auto issue_v = [&](int j) { issue_tile(idv, &tmV, sm + kV0 + (j % kVS) * 32768, &v_full[j % kVS], j); };
+        int nk = 0, nv = 0;  // loads issued
+        bool ok = true;
+        for (; nk < kKS && nk < n_kt; ++nk) issue_k(nk);
+        for (; nv < kVS && nv < n_kt; ++nv) issue_v(nv);
+        while (ok && (nk < n_kt || nv < n_kt)) {
+            if (nk < n_kt && nk <= nv + 1) {  // K(nk) replaces K(nk-3)
+                ok = wait_bar(&k_free[nk % kKS], (uint32_t)(((nk - kKS) / kKS) & 1), P.err, abort_flag);
+                if (!ok) break;
+                issue_k(nk++);
+            } else {  // V(nv) replaces V(nv-2)
+                ok = wait_bar(&v_free[nv % kVS], (uint32_t)(((nv - kVS) / kVS) & 1), P.err, abort_flag);
+                if (!ok) break;
+                issue_v(nv++);
+            }
+        }
+        // every issued copy has landed before the CTA may exit (bounded; in
+        // the normal case the MMA warp has already consumed them all)
+        for (int t = (nk > kKS ? nk - kKS : 0); t < nk; ++t)
+            pa::mbar_wait(&k_full[t % kKS], (uint32_t)((t / kKS) & 1), nullptr, 5000000ull);
+        for (int t = (nv > kVS ? nv - kVS : 0); t < nv; ++t)
+            pa::mbar_wait(&v_full[t % kVS], (uint32_t)((t / kVS) & 1), nullptr, 5000000ull);
+    } else if (warp == 8) {
+        // ---------------------------------------------------------- MMA issuer
         auto issue_qk = [&](int x, int j) {  // S_x = Q_x K_j^T
             if (lane == 0) {
                 const uint32_t qs = pa::smem_u32(sm + kQ + x * 32768);
-                const uint32_t kst = pa::smem_u32(sm + kK0 + (j % kStages) * 32768);
+                const uint32_t kst = pa::smem_u32(sm + kK0 + (j % kKS) * 32768);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t ad = tc::smem_desc(qs + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
@@ -215,27 +259,31 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                     tc::mma_bf16(tbase + x * 256, ad, bd, ID_QK, ks > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&s_full[x]);
+                if (x == 1) tc::mma_commit(&k_free[j % kKS]);  // the stage's last reader
             }
             __syncwarp();
         };
         auto issue_pv = [&](int x, int j) {  // O_x += P_hi V_j + P_lo V_j, P in S_x's columns
             if (lane == 0) {
-                const uint32_t vs = pa::smem_u32(sm + kV0 + (j % kStages) * 32768);
+                const uint32_t vs = pa::smem_u32(sm + kV0 + (j % kVS) * 32768);
                 const uint32_t pcol = tbase + x * 256;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint64_t bd = tc::smem_desc(vs + ks * 2048, 16384, 1024);
-                        tc::mma_bf16_ts(tbase + x * 256 + 128, pcol + part * 64 + ks * 8, bd, ID_PV,
+                        tc::mma_bf16_ts(tbase + x * 256 + 128, pcol + (ks >> 2) * 64 + part * 32 + (ks & 3) * 8, bd, ID_PV,
                                         (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
                     }
                 tc::mma_commit(&pv_done[x]);
+                if (x == 1) tc::mma_commit(&v_free[j % kVS]);  // the stage's last reader
             }
             __syncwarp();
         };
-        for (int j = 0; j < kStages && j < n_kt; ++j) issue_tma(j);
-        bool ok = wait_bar(&kv_full[0], 0, P.err, abort_flag);
+        // The tensor core runs the MMAs of this thread in issue order, so
+        // QK_x(j+1) may follow PV_x(j) (which reads P out of S_x's columns)
+        // without a wait.
+        bool ok = wait_bar(&k_full[0], 0, P.err, abort_flag);
         if (ok) {
             tc::fence_after_sync();
             issue_qk(0, 0);
@@ -243,44 +291,27 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         }
         for (int j = 0; j < n_kt && ok; ++j) {
             const uint32_t par = (uint32_t)(j & 1);
-            // tile A: PV_A(j) once its P is written, then QK_A(j+1) once PV_A(j)
-            // has read P out of S_A
             ok = wait_bar(&p_full[0], par, P.err, abort_flag);
+            if (ok) ok = wait_bar(&v_full[j % kVS], (uint32_t)((j / kVS) & 1), P.err, abort_flag);
             if (!ok) break;
             tc::fence_after_sync();
             issue_pv(0, j);
             if (j + 1 < n_kt) {
-                ok = wait_bar(&kv_full[(j + 1) % kStages], (uint32_t)(((j + 1) / kStages) & 1), P.err,
-                              abort_flag);
-                if (ok) ok = wait_bar(&pv_done[0], par, P.err, abort_flag);
+                ok = wait_bar(&k_full[(j + 1) % kKS], (uint32_t)(((j + 1) / kKS) & 1), P.err, abort_flag);
                 if (!ok) break;
                 issue_qk(0, j + 1);
             }
-            // tile B likewise
             ok = wait_bar(&p_full[1], par, P.err, abort_flag);
             if (!ok) break;
             tc::fence_after_sync();
             issue_pv(1, j);
-            if (j + 1 < n_kt) {
-                ok = wait_bar(&pv_done[1], par, P.err, abort_flag);
-                if (!ok) break;
-                issue_qk(1, j + 1);
-            }
-            // stage j%2 is free: both PVs of tile j are done (waited above,
-            // since j + 2 < n_kt implies j + 1 < n_kt)
-            if (j + kStages < n_kt) issue_tma(j + kStages);
+            if (j + 1 < n_kt) issue_qk(1, j + 1);
         }
         // drain: every issued MMA has completed before the CTA can release its
         // shared and tensor memory (bounded wait)
         if (lane == 0) tc::mma_commit(drain);
         __syncwarp();
         pa::mbar_wait(drain, 0, nullptr, 10000000ull);
-        if (!ok) {  // TMA copies may still be landing: bounded waits on every stage
-            for (int i = 0; i < kStages; ++i) {
-                pa::mbar_wait(&kv_full[i], 0, nullptr, 5000000ull);
-                pa::mbar_wait(&kv_full[i], 1, nullptr, 5000000ull);
-            }
-        }
     } else {
         // --------------------------------------- softmax warpgroup of tile x
         // warp w serves TMEM lanes 32*(w%4) .. +31 (rows). After a failed wait
@@ -302,10 +333,13 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             const int kb = j * kKT;
             // V rows of the sequence's last, partial block hold whatever the pool
             // has there: zero them so that p = 0 never meets a NaN (tile A's
-            // warpgroup, before PV_A(j), the first PV reading V_j)
+            // warpgroup, once V_j has landed and before PV_A(j), the first PV
+            // reading it)
             if (x == 0 && (ctx & (kBS - 1)) && ctx > kb && ctx < kb + kKT) {
+                if (ok) ok = wait_bar(&v_full[j % kVS], (uint32_t)((j / kVS) & 1), P.err, abort_flag);
+                ok = __all_sync(kFull, ok);
                 const int z0 = ctx - kb, z1 = min(((ctx + kBS - 1) & ~(kBS - 1)) - kb, kKT);
-                unsigned char* vs = sm + kV0 + (j % kStages) * 32768;
+                unsigned char* vs = sm + kV0 + (j % kVS) * 32768;
                 for (int e = r; e < (z1 - z0) * 16; e += 128) {
                     const int row = z0 + (e >> 4), g = (e >> 3) & 1, c = e & 7;
                     *reinterpret_cast<uint4*>(vs + g * 16384 + tc::sw128_offset(row, c)) = make_uint4(0, 0, 0, 0);
@@ -313,28 +347,30 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 tc::fence_async_smem();
             }
             const bool need_mask = kb + kKT - 1 > pos;
-            // pass 1: causal mask and row maximum of the raw scores (only the
-            // key tiles that reach past a row's position need the mask)
-            float tmax = -INFINITY;
+            // pass 1: row maximum over the 128 scores (four loads, one wait)
+            float tmax;
+            {
+                uint32_t sr[kKT];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t raw[32];
-                tc::tmem_ld32(tS + c * 32, raw);
+                for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
                 tc::tmem_wait_ld();
-                if (need_mask) {
-                    const int lim = pos - kb - c * 32;  // keys k <= lim are visible
+                if (need_mask) {  // causal mask: keys k > pos - kb are not visible
+                    const int lim = pos - kb;
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        if (k <= lim) tmax = fmaxf(tmax, __uint_as_float(raw[k]));
-                } else {
-                    float m0 = __uint_as_float(raw[0]), m1 = __uint_as_float(raw[1]);
-#pragma unroll
-                    for (int k = 2; k < 32; k += 2) {
-                        m0 = fmaxf(m0, __uint_as_float(raw[k]));
-                        m1 = fmaxf(m1, __uint_as_float(raw[k + 1]));
-                    }
-                    tmax = fmaxf(tmax, fmaxf(m0, m1));
+                    for (int k = 0; k < kKT; ++k)
+                        if (k > lim) sr[k] = __float_as_uint(-INFINITY);
                 }
+                float mx[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mx[c] = __uint_as_float(sr[c]);
+#pragma unroll
+                for (int k = 4; k + 8 <= kKT; k += 8)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        mx[c] = max3f(mx[c], __uint_as_float(sr[k + 2 * c]), __uint_as_float(sr[k + 2 * c + 1]));
+                tmax = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+#pragma unroll
+                for (int k = kKT - 4; k < kKT; ++k) tmax = fmaxf(tmax, __uint_as_float(sr[k]));
             }
             tmax *= sc;
             const bool rescale = tmax > m_used + kRescaleThreshold;
@@ -343,49 +379,40 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
                 m_used = tmax;
             }
-            // pass 2: p = 2^(s*scale - m). P_hi of key chunk c (32 keys) goes to
-            // columns 16c.. (scores already read); P_lo of chunk c goes to
-            // columns 64 + 16c, which hold score chunks 2 and 3: it is written
-            // once those have been read (chunks 0, 1 after reading chunk 2;
-            // chunks 2, 3 after reading chunk 3).
-            float psum = 0.f;
-            uint32_t lo_a[32], lo_b[16];
-            auto exps = [&](int c, uint32_t* hi, uint32_t* lo) {
-                uint32_t raw[32];
-                tc::tmem_ld32(tS + c * 32, raw);
-                tc::tmem_wait_ld();
+            // pass 2, per half of 64 keys: p = 2^(s*scale - m) as P_hi + P_lo.
+            // Half h's scores sit in columns 64h..64h+63; P_hi of its keys
+            // 2w, 2w+1 goes to column 64h + w and P_lo to 64h + 32 + w, so a
+            // half only overwrites columns it has already read.
+            float2 psum2 = make_float2(0.f, 0.f);
+            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_used, -m_used);
+            const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
-                const int lim = pos - kb - c * 32;  // keys k <= lim are visible
-                for (int w = 0; w < 16; ++w) {
-                    float a = fmaf(__uint_as_float(raw[2 * w]), sc, -m_used);
-                    float b = fmaf(__uint_as_float(raw[2 * w + 1]), sc, -m_used);
-                    if (need_mask) {
-                        if (2 * w > lim) a = -INFINITY;
-                        if (2 * w + 1 > lim) b = -INFINITY;
+            for (int half = 0; half < 2; ++half) {
+                uint32_t raw[64];
+                tc::tmem_ld32(tS + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(raw));
+                tc::tmem_ld32(tS + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
+                tc::tmem_wait_ld();
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int w = 0; w < 32; ++w) {
+                    const int k = 64 * half + 2 * w;
+                    float2 e = __ffma2_rn(make_float2(__uint_as_float(raw[2 * w]), __uint_as_float(raw[2 * w + 1])),
+                                          sc2, nm2);
+                    if (need_mask) {  // masked keys give p = 0 (also for a zero scale)
+                        if (k > pos - kb) e.x = -INFINITY;
+                        if (k + 1 > pos - kb) e.y = -INFINITY;
                     }
-                    a = pa::fast_exp2(a);
-                    b = pa::fast_exp2(b);
-                    psum += a + b;
-                    hi[w] = pa::float2_to_bf16x2(a, b);
-                    const float2 h2 = pa::bf16x2_to_float2(hi[w]);
-                    lo[w] = pa::float2_to_bf16x2(a - h2.x, b - h2.y);
+                    e.x = pa::fast_exp2(e.x);
+                    e.y = pa::fast_exp2(e.y);
+                    psum2 = __fadd2_rn(psum2, e);
+                    hi[w] = pa::float2_to_bf16x2(e.x, e.y);
+                    const float2 r = __ffma2_rn(pa::bf16x2_to_float2(hi[w]), neg1, e);
+                    lo[w] = pa::float2_to_bf16x2(r.x, r.y);
                 }
-            };
-            {
-                uint32_t hi[16];
-                exps(0, hi, lo_a);
-                tc::tmem_st16(tS + 0, hi);
-                exps(1, hi, lo_a + 16);
-                tc::tmem_st16(tS + 16, hi);
-                exps(2, hi, lo_b);  // score chunk 2 (columns 64..95) is now read
-                tc::tmem_st16(tS + 32, hi);
-                tc::tmem_st16(tS + 64, lo_a);
-                tc::tmem_st16(tS + 80, lo_a + 16);
-                exps(3, hi, lo_a);  // score chunk 3 (columns 96..127) is now read
-                tc::tmem_st16(tS + 48, hi);
-                tc::tmem_st16(tS + 96, lo_b);
-                tc::tmem_st16(tS + 112, lo_a);
+                tc::tmem_st32(tS + 64 * half, hi);
+                tc::tmem_st32(tS + 64 * half + 32, lo);
             }
+            const float psum = psum2.x + psum2.y;
             l = l * alpha + psum;
             // a larger maximum rescales O_x: PV_x(j-1) must have landed first
             if (j > 0 && __any_sync(kFull, rescale)) {
@@ -453,7 +480,7 @@ int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtenso
     }
     constexpr int QT = kRows / G;
     dim3 grid((max_chunk_len + 2 * QT - 1) / (2 * QT), Pp.n_kv_heads, n_seqs);
-    kern<<<grid, 288, kSmemBytes, stream>>>(Pp, tk, tv);
+    kern<<<grid, 320, kSmemBytes, stream>>>(Pp, tk, tv);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
