@@ -474,37 +474,55 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
 
 _CPU_CHILD = r"""
 import json, sys, time
+import numpy as np
 sys.path.insert(0, {root!r})
 from workloads import make_workload
 from oracle.attention import paged_decode
 from oracle.cache_ops import reshape_and_cache
 wl = make_workload({workload!r}, fill="zero", keep_logical=False)
-B = len(wl.dec_ctx)
-n = min(B, len(wl.slot_mapping)) if wl.slot_mapping is not None else 0
+B, H, Hk = len(wl.dec_ctx), wl.n_heads, wl.n_kv_heads
+G = H // Hk
+n_new = min(B, len(wl.slot_mapping)) if wl.slot_mapping is not None else 0
 budget, per_step = {seconds}, {per_step}
-kv_tok = wl.n_kv_heads * wl.head_dim * 2 * 2
+# The unit of work is one (sequence, KV head): its G query heads attend over
+# the sequence's blocks. Each unit runs through the unchanged oracle on a
+# compact copy of just that sequence's blocks of that KV head (built here,
+# outside the timed region), so a unit costs what its arithmetic costs.
+units = [(b, h) for b in range(B) for h in range(Hk)]
+def prepare(b, h):
+    nblk = (int(wl.dec_ctx[b]) + 15) // 16
+    ids = wl.dec_tables[b, :nblk]
+    kp = np.ascontiguousarray(wl.k_pool[ids, h:h + 1])
+    vp = np.ascontiguousarray(wl.v_pool[ids, h:h + 1])
+    table = np.arange(nblk, dtype=np.int32)[None, :]
+    slot = None
+    if b < n_new:
+        s = int(wl.slot_mapping[b]); blk, off = s // 16, s % 16
+        pos = int(np.nonzero(ids == blk)[0][0])
+        slot = np.array([pos * 16 + off], dtype=np.int64)
+    return kp, vp, table, slot
+kv_tok = 2 * wl.head_dim * 2   # K + V bytes of one token of one KV head
 done_tok = 0
-seqs = 0
-t0 = time.perf_counter()
-b = 0
+n_units = 0
+u = 0
+dt = 0.0
 while True:
-    sel = [(b + i) % B for i in range(per_step)]
-    b = (b + per_step) % B
-    if n:
-        sel_new = [i for i in sel if i < n]
-        kp, vp = reshape_and_cache(wl.new_k[sel_new], wl.new_v[sel_new], wl.k_pool, wl.v_pool,
-                                   wl.slot_mapping[sel_new])
-    else:
-        kp, vp = wl.k_pool, wl.v_pool
-    paged_decode(wl.q[sel], kp, vp, wl.dec_tables[sel], wl.dec_ctx[sel], wl.scale)
-    done_tok += int(wl.dec_ctx[sel].sum())
-    seqs += len(sel)
-    if {fixed_steps} and seqs >= {fixed_steps} * per_step:
+    sel = [units[(u + i) % len(units)] for i in range(per_step)]
+    u = (u + per_step) % len(units)
+    prep = [prepare(b, h) for b, h in sel]
+    t0 = time.perf_counter()
+    for (b, h), (kp, vp, table, slot) in zip(sel, prep):
+        if slot is not None:
+            kp, vp = reshape_and_cache(wl.new_k[b:b + 1, h:h + 1], wl.new_v[b:b + 1, h:h + 1], kp, vp, slot)
+        paged_decode(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1], wl.scale)
+        done_tok += int(wl.dec_ctx[b])
+    dt += time.perf_counter() - t0
+    n_units += len(sel)
+    if {fixed_steps} and n_units >= {fixed_steps} * per_step:
         break
-    if not {fixed_steps} and time.perf_counter() - t0 >= budget:
+    if not {fixed_steps} and dt >= budget:
         break
-dt = time.perf_counter() - t0
-print(json.dumps({{"seconds": dt, "tokens": done_tok, "seqs": seqs, "kv_bytes": done_tok * kv_tok}}))
+print(json.dumps({{"seconds": dt, "tokens": done_tok, "units": n_units, "kv_bytes": done_tok * kv_tok}}))
 """
 
 
@@ -529,9 +547,10 @@ def run_cpu_baseline(workload, seconds):
         return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "error": str(e)[-300:]}
     return {"value": round(res["kv_bytes"] / res["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
             "kind": "oracle",
-            "sample": f"{res['seqs']} sequences of the {workload} batch (cycled in order, "
-                      f"{res['tokens']} context tokens) through the fp64 numpy oracle in "
-                      f"{res['seconds']:.1f} s on 1 host thread (BLAS pinned to 1 thread)",
+            "sample": f"{res['units']} (sequence, KV head) units of the {workload} batch (cycled in "
+                      f"order; {res['tokens']} context tokens, each unit's cache write and decode) "
+                      f"through the fp64 numpy oracle in {res['seconds']:.1f} s on 1 host thread "
+                      f"(BLAS pinned to 1 thread)",
             "host_logical_cores": os.cpu_count()}
 
 
@@ -545,17 +564,18 @@ def run_reference(args):
         return
     # size the per-step sample so that warmup + steps stay within ~2 minutes
     calib = _oracle_child(args.workload, 2.0, per_step=1)
-    sec_per_seq = calib["seconds"] / max(calib["seqs"], 1)
+    sec_per_unit = calib["seconds"] / max(calib["units"], 1)
     budget = 120.0
     total_steps = args.steps + args.warmup
-    per_step = max(1, int(budget / total_steps / sec_per_seq))
-    per_step = min(per_step, 64)
+    per_step = max(1, int(budget / total_steps / sec_per_unit))
+    per_step = min(per_step, 512)
     if args.warmup:
         _oracle_child(args.workload, 0, per_step=per_step, fixed_steps=args.warmup)
     res = _oracle_child(args.workload, 0, per_step=per_step, fixed_steps=args.steps)
     value = res["kv_bytes"] / res["seconds"] / 1e9
-    sample = (f"each step: {per_step} sequence(s) of the {args.workload} batch, cycled in order, "
-              f"through the fp64 numpy oracle (reshape_and_cache + decode) on 1 host thread")
+    sample = (f"each step: {per_step} (sequence, KV head) unit(s) of the {args.workload} batch, "
+              f"cycled in order, through the fp64 numpy oracle (reshape_and_cache + decode) on 1 "
+              f"host thread")
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -570,7 +590,8 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic: the same seeded workload as the GPU arm",
-        "config": {"workload": args.workload, "sample_sequences_per_step": per_step},
+        "config": {"workload": args.workload, "sample_units_per_step": per_step,
+                   "unit": "one (sequence, KV head): its query heads over its context"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

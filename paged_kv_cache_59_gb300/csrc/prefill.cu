@@ -87,14 +87,17 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return r;
 }
 
+// Bounded wait (1 s) that also gives up once another role has aborted. A
+// waiting thread sleeps inside try_wait (up to 20 us per try, woken when the
+// phase completes), so idle roles take no issue slots from busy ones.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigned int* err,
                                          volatile int* abort_flag) {
     if (*abort_flag) return false;
     if (pa::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = pa::globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (pa::mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
+        if (pa::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if ((it & 15u) == 0) {
             if (*abort_flag) return false;
             if (pa::globaltimer_ns() - t0 > PA_WAIT_LIMIT_NS) {
                 pa::set_error(err, PA_DEVERR_TIMEOUT);
