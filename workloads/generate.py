@@ -267,7 +267,80 @@ def make_prefill_case(seed: int, chunk_ctx: Sequence[int], chunk_lens: Sequence[
 
 
 # --------------------------------------------------------------------------
-# The five named workloads. Seed = workload index (0..4).
+# fp8 (E4M3) KV cache
+# --------------------------------------------------------------------------
+
+E4M3_NAN = 0x7F
+_E4M3_FINITE = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+
+
+def _e4m3_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    """Cached K/V drawn directly as E4M3 codes: uniform over the 254 finite
+    bit patterns (both signs, zeros, subnormals, up to the largest finite
+    value). No rounding is involved: the codes are the input."""
+    return _E4M3_FINITE[rng.integers(0, len(_E4M3_FINITE), size=shape)]
+
+
+def make_decode_case_fp8(seed: int, context_lens: Sequence[int], n_heads: int, n_kv_heads: int,
+                         head_dim: int, num_blocks: Optional[int] = None, pool_factor: float = 1.25,
+                         n_new: int = 1, fill: str = "nan", scale: Optional[float] = None,
+                         name: str = "decode_fp8", rng: Optional[np.random.Generator] = None
+                         ) -> Workload:
+    """A decode batch over a randomly placed paged cache of E4M3 codes.
+
+    Draw order: context lengths -> placement -> q -> cached K codes -> cached
+    V codes (one sequence after another) -> this step's new K -> new V (bf16,
+    N(0,1); the cache write quantises them) -> per-KV-head scales for K and
+    for V, each 2^-6 * (1 + u), u ~ U[0, 1), as fp32.
+
+    Layouts: k_pool, v_pool uint8 [num_blocks][n_kv_heads][block_size][head_dim]
+    (fill: E4M3 NaN 0x7F for parity runs, 0 for timing runs); k_scale, v_scale
+    float32 [n_kv_heads]; q, new_k, new_v bf16 bits as in ``make_decode_case``.
+    """
+    bs = BLOCK_SIZE
+    rng = rng if rng is not None else np.random.default_rng(seed)
+    ctx = np.asarray(context_lens, dtype=np.int32)
+    B = len(ctx)
+    assert all(c >= n_new for c in ctx), "every context must hold its new tokens"
+    nb = [int(math.ceil(c / bs)) for c in ctx]
+    needed = sum(nb)
+    if num_blocks is None:
+        num_blocks = max(int(math.ceil(pool_factor * needed)), needed)
+    assert num_blocks >= needed
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    tables = _tables_from_placement(nb, perm[:needed])
+    H, Hk, D = n_heads, n_kv_heads, head_dim
+    q = _normal_bf16(rng, (B, H, D))
+    fillv = E4M3_NAN if fill == "nan" else 0
+    k_pool = np.full((num_blocks, Hk, bs, D), fillv, dtype=np.uint8)
+    v_pool = np.full((num_blocks, Hk, bs, D), fillv, dtype=np.uint8)
+    for pool in (k_pool, v_pool):
+        for b in range(B):
+            n_old = int(ctx[b]) - n_new
+            if n_old > 0:
+                _place(pool, tables[b], _e4m3_codes(rng, (n_old, Hk, D)), 0)
+    new_k = _normal_bf16(rng, (B * n_new, Hk, D))
+    new_v = _normal_bf16(rng, (B * n_new, Hk, D))
+    slots = np.empty((B * n_new,), dtype=np.int64)
+    for b in range(B):
+        c = int(ctx[b])
+        if n_new:
+            slots[b * n_new:(b + 1) * n_new] = _slots(tables[b], range(c - n_new, c), bs)
+    k_scale = (2.0 ** -6 * (1.0 + rng.random(Hk))).astype(np.float32)
+    v_scale = (2.0 ** -6 * (1.0 + rng.random(Hk))).astype(np.float32)
+    wl = Workload(name=name, seed=seed, n_heads=H, n_kv_heads=Hk, head_dim=D,
+                  num_blocks=num_blocks,
+                  scale=float(scale if scale is not None else 1.0 / math.sqrt(D)),
+                  k_pool=k_pool, v_pool=v_pool, dec_tables=tables, dec_ctx=ctx, q=q,
+                  new_k=new_k, new_v=new_v, slot_mapping=slots)
+    wl.meta.update(needed_blocks=needed, n_new=n_new, kv_dtype="fp8_e4m3",
+                   k_scale=k_scale, v_scale=v_scale)
+    return wl
+
+
+# --------------------------------------------------------------------------
+# The named workloads. Seed = workload index (0..4); the fp8 variant of the
+# 8B batch reuses the 8B batch's seed so its context lengths match.
 # --------------------------------------------------------------------------
 
 def _tiny_mha(fill="nan", keep_logical=True):
@@ -328,12 +401,22 @@ def _mixed(fill="nan", keep_logical=False):
                              rng=rng)
 
 
+def _gqa_8b_fp8(fill="nan", keep_logical=False):
+    """The 8B-shaped GQA batch (same context lengths as ``gqa_8b``) over an
+    E4M3 cache with per-KV-head scales."""
+    rng = np.random.default_rng(2)
+    ctx = rng.integers(128, 4096, size=64, endpoint=True)
+    return make_decode_case_fp8(2, ctx, 32, 8, 128, pool_factor=1.25, n_new=1, fill=fill,
+                                name="gqa8b_fp8_b64_ctx128-4096", rng=rng)
+
+
 WORKLOADS = {
     "tiny_mha": _tiny_mha,
     "mha_7b": _mha_7b,
     "gqa_8b": _gqa_8b,
     "gqa_70b_cow": _gqa_70b_cow,
     "mixed": _mixed,
+    "gqa_8b_fp8": _gqa_8b_fp8,
 }
 
 
