@@ -36,7 +36,8 @@ METRIC = "paged decode attention KV-read HBM GB/s (fraction of peak), tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 DEFAULT_WORKLOAD = "gqa_8b"
-WORKLOAD_LAYERS = {"tiny_mha": 1, "mha_7b": 32, "gqa_8b": 32, "gqa_70b_cow": 80, "mixed": 32}
+WORKLOAD_LAYERS = {"tiny_mha": 1, "mha_7b": 32, "gqa_8b": 32, "gqa_70b_cow": 80, "mixed": 32,
+                   "gqa_8b_fp8": 32}
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_decode_partition_gqa8b.md")
 
 
@@ -47,7 +48,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=["tiny_mha", "mha_7b", "gqa_8b", "gqa_70b_cow", "mixed"])
+                    choices=["tiny_mha", "mha_7b", "gqa_8b", "gqa_70b_cow", "mixed", "gqa_8b_fp8"])
     ap.add_argument("--partition-tokens", type=int, default=0,
                     help="decode context partition size (0 = library default)")
     ap.add_argument("--skip-baselines", action="store_true",
@@ -227,7 +228,9 @@ def run_ours(args):
     B = len(wl.dec_ctx)
     max_ctx = int(wl.dec_ctx.max())
     sum_ctx = int(wl.dec_ctx.sum())
-    kv_bytes = sum_ctx * Hk * D * 2 * 2
+    fp8 = wl.meta.get("kv_dtype") == "fp8_e4m3"
+    eb = 1 if fp8 else 2                       # bytes per cached element
+    kv_bytes = sum_ctx * Hk * D * 2 * eb
     alg_bytes = (kv_bytes + 2 * wl.q.nbytes + wl.dec_tables.nbytes + wl.dec_ctx.nbytes)
 
     def to_dev(a):
@@ -262,12 +265,28 @@ def run_ours(args):
     pt = args.partition_tokens
     ws = pk.decode_workspace(q, max_ctx, pt)
     stream = torch.cuda.current_stream()
+    if fp8:
+        ks, vs = to_dev(wl.meta["k_scale"]), to_dev(wl.meta["v_scale"])
+        alg_bytes += ks.numel() * 4 * 2
+
+    def write_cache():
+        if fp8:
+            pk.pa_reshape_and_cache_fp8(nk, nv, kp, vp, sl, ks, vs)
+        else:
+            pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
+
+    def decode():
+        if fp8:
+            pk.pa_decode_fp8(out, q, kp, vp, ks, vs, tabs, ctx, wl.scale, max_ctx, workspace=ws,
+                             partition_tokens=pt)
+        else:
+            pk.pa_decode(out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws, partition_tokens=pt)
     launches_per_step = ((1 if n_dec_new else 0) + (1 if has_pf else 0) + 1
                          + (1 if pk.pa_decode_workspace_bytes(B, H, D, max_ctx, pt) else 0))
 
     def step(ev_pair=None, pf_pair=None):
         if n_dec_new:
-            pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
+            write_cache()
         if has_pf:
             if pf_pair is not None:
                 pf_pair[0].record(stream)
@@ -276,7 +295,7 @@ def run_ours(args):
                 pf_pair[1].record(stream)
         if ev_pair is not None:
             ev_pair[0].record(stream)
-        pk.pa_decode(out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws, partition_tokens=pt)
+        decode()
         if ev_pair is not None:
             ev_pair[1].record(stream)
 
@@ -343,15 +362,20 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic: seeded N(0,1) q/K/V rounded to bf16, seeded context lengths, "
-                "random physical block placement",
+        "dtype": "fp8_e4m3" if fp8 else "bf16",
+        "data": ("synthetic: cached K/V as seeded E4M3 codes (uniform over finite codes) with "
+                 "per-KV-head fp32 scales, N(0,1) q and new tokens rounded to bf16, seeded context "
+                 "lengths, random physical block placement" if fp8 else
+                 "synthetic: seeded N(0,1) q/K/V rounded to bf16, seeded context lengths, "
+                 "random physical block placement"),
         "config": {
             "workload": wl.name,
             "n_seqs": B, "n_heads": H, "n_kv_heads": Hk, "head_dim": D, "block_size": 16,
             "sum_context_tokens": sum_ctx, "max_context": max_ctx, "num_blocks": wl.num_blocks,
             "kv_bytes_per_step": kv_bytes,
-            "step": "pa_reshape_and_cache (1 new token/seq) + pa_decode (partition kernel + split-K merge)",
+            "step": ("pa_reshape_and_cache_fp8 (1 new token/seq, encoded) + pa_decode_fp8 (partition "
+                     "kernel + split-K merge)" if fp8 else
+                     "pa_reshape_and_cache (1 new token/seq) + pa_decode (partition kernel + split-K merge)"),
             "l2": f"no flush: the KV stream ({kv_bytes / 1e6:.0f} MB/step) exceeds the 129 MB L2",
             "partition_tokens": pt or 512,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -397,7 +421,8 @@ def run_ours(args):
 
     if not args.skip_baselines:
         result["e2e"] = run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world,
-                                dist if world > 1 else None)
+                                dist if world > 1 else None,
+                                (ks, vs) if fp8 else None)
         if rank == 0:
             result["cpu_baseline"] = run_cpu_baseline(args.workload, args.cpu_seconds)
     if rank == 0:
@@ -407,7 +432,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dist):
+def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dist, fp8_scales=None):
     """Same metric through the public API with host buffers: each step copies
     its inputs (q, new K/V, slots, tables, context lengths) from pinned host
     memory, runs the hot path, and reads the output back."""
@@ -442,12 +467,19 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
             d.copy_(h, non_blocking=True)
         q, nk, nv, sl, tabs, ctx = d_in[:6]
         if len(slots):
-            pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
+            if fp8_scales is not None:
+                pk.pa_reshape_and_cache_fp8(nk, nv, kp, vp, sl, *fp8_scales)
+            else:
+                pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
         if has_pf:
             q_pf, pf_tabs, pf_ctx, qsl = d_in[6:]
             pk.pa_prefill_paged(d_out[1], q_pf, kp, vp, pf_tabs, pf_ctx, qsl, wl.scale, max_chunk)
-        pk.pa_decode(d_out[0], q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws,
-                     partition_tokens=args.partition_tokens)
+        if fp8_scales is not None:
+            pk.pa_decode_fp8(d_out[0], q, kp, vp, *fp8_scales, tabs, ctx, wl.scale, max_ctx, workspace=ws,
+                             partition_tokens=args.partition_tokens)
+        else:
+            pk.pa_decode(d_out[0], q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws,
+                         partition_tokens=args.partition_tokens)
         for h, d in zip(h_out, d_out):
             h.copy_(d, non_blocking=True)
         stream.synchronize()                       # the host reads this step's result
@@ -479,7 +511,9 @@ sys.path.insert(0, {root!r})
 from workloads import make_workload
 from oracle.attention import paged_decode
 from oracle.cache_ops import reshape_and_cache
+from oracle import fp8 as ofp8
 wl = make_workload({workload!r}, fill="zero", keep_logical=False)
+fp8 = wl.meta.get("kv_dtype") == "fp8_e4m3"
 B, H, Hk = len(wl.dec_ctx), wl.n_heads, wl.n_kv_heads
 G = H // Hk
 n_new = min(B, len(wl.slot_mapping)) if wl.slot_mapping is not None else 0
@@ -501,7 +535,7 @@ def prepare(b, h):
         pos = int(np.nonzero(ids == blk)[0][0])
         slot = np.array([pos * 16 + off], dtype=np.int64)
     return kp, vp, table, slot
-kv_tok = 2 * wl.head_dim * 2   # K + V bytes of one token of one KV head
+kv_tok = 2 * wl.head_dim * (1 if fp8 else 2)   # K + V bytes of one token of one KV head
 done_tok = 0
 n_units = 0
 u = 0
@@ -512,9 +546,18 @@ while True:
     prep = [prepare(b, h) for b, h in sel]
     t0 = time.perf_counter()
     for (b, h), (kp, vp, table, slot) in zip(sel, prep):
-        if slot is not None:
-            kp, vp = reshape_and_cache(wl.new_k[b:b + 1, h:h + 1], wl.new_v[b:b + 1, h:h + 1], kp, vp, slot)
-        paged_decode(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1], wl.scale)
+        if fp8:
+            ks, vs = wl.meta["k_scale"][h:h + 1], wl.meta["v_scale"][h:h + 1]
+            if slot is not None:
+                kp, vp = ofp8.reshape_and_cache_fp8(wl.new_k[b:b + 1, h:h + 1], wl.new_v[b:b + 1, h:h + 1],
+                                                    kp, vp, slot, ks, vs)
+            ofp8.paged_decode_fp8(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1],
+                                  wl.scale, ks, vs)
+        else:
+            if slot is not None:
+                kp, vp = reshape_and_cache(wl.new_k[b:b + 1, h:h + 1], wl.new_v[b:b + 1, h:h + 1], kp, vp,
+                                           slot)
+            paged_decode(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1], wl.scale)
         done_tok += int(wl.dec_ctx[b])
     dt += time.perf_counter() - t0
     n_units += len(sel)

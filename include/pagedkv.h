@@ -1,8 +1,8 @@
 /*
  * pagedkv.h - C ABI of libpagedkv.so: PagedAttention decode over a paged
- * bf16 KV cache on NVIDIA GB300 (sm_103a), the two kernels that keep the
- * cache valid, a chunked causal prefill over the same cache, and a host-side
- * block manager that builds the tables.
+ * bf16 (or fp8 E4M3) KV cache on NVIDIA GB300 (sm_103a), the kernels that
+ * keep the cache valid, a chunked causal prefill over the same cache, and a
+ * host-side block manager that builds the tables.
  *
  * Sources (page title, section):
  *  [PA]  "PagedAttention vs Traditional KV Cache: How vLLM Reinvented GPU
@@ -182,6 +182,51 @@ int pa_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_poo
 int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs,
                    int n_kv_heads, int head_dim, int block_size, int num_blocks,
                    pa_stream_t stream);
+
+/* ------------------------------------------------- fp8 (E4M3) KV cache */
+
+/*
+ * An fp8 cache stores every K and V element as one E4M3 code (1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, no infinities, 0x7F/0xFF NaN,
+ * largest magnitude 448) with one fp32 scale per KV head for K and one for V;
+ * an element stands for decode(code) * scale ([DR] "What insiders know": fp8
+ * KV with per-head scale factors; [KE] "KV Cache Quantization": one byte per
+ * element and a scale). The pool layout is the bf16 one with 1-byte elements:
+ *     uint8 [num_blocks][n_kv_heads][block_size][head_dim]
+ * so a block holds half the bytes.
+ *  k_scale, v_scale  fp32 [n_kv_heads], device memory, 4-byte aligned, > 0.
+ */
+
+/*
+ * Cache write for an fp8 cache: as pa_reshape_and_cache, but element x of
+ * k[t][h][:] (bf16) is stored as the E4M3 code of the fp32 quotient
+ * x / k_scale[h] (IEEE division, round to nearest even, finite values beyond
+ * +-448 saturate to +-448), and likewise for v with v_scale.
+ *  k, v          bf16 [n_tokens][n_kv_heads][head_dim], 16-byte aligned
+ *  k_pool,v_pool uint8 pools (8-byte aligned)
+ *  slot_mapping  int64 [n_tokens]; negative = skip; out of range sets
+ *                PA_DEVERR_SLOT and is skipped
+ */
+int pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool, void* v_pool,
+                             const int64_t* slot_mapping, const float* k_scale,
+                             const float* v_scale, int n_tokens, int n_kv_heads, int head_dim,
+                             int block_size, int num_blocks, pa_stream_t stream);
+
+/*
+ * Decode over an fp8 cache: pa_decode_ex with K and V read as E4M3 codes
+ * times their KV head's scale,
+ *     out[b][h] = sum_t softmax_t(scale * q[b][h] . Kd_b[t]) Vd_b[t],
+ *     Kd = decode(k code) * k_scale[kv head], Vd = decode(v code) * v_scale.
+ * q and out are bf16 as in pa_decode; the workspace is sized by
+ * pa_decode_workspace_bytes (the same formula); partition_tokens as in
+ * pa_decode_ex. Pools must be 16-byte aligned.
+ */
+int pa_decode_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                  const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                  const int32_t* context_lens, float scale, int n_heads, int n_kv_heads,
+                  int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
+                  int max_context_len, int num_blocks, int partition_tokens, void* workspace,
+                  size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------- chunked prefill */
 

@@ -20,8 +20,9 @@ from . import _capi
 from ._capi import PagedKVError, check, load  # noqa: F401
 
 __all__ = [
-    "pa_decode", "pa_decode_workspace_bytes", "decode_workspace", "pa_decode_noalloc", "pa_reshape_and_cache", "pa_copy_blocks",
-    "pa_prefill_paged", "pa_get_device_error", "BlockManager", "load", "PagedKVError",
+    "pa_decode", "pa_decode_workspace_bytes", "decode_workspace", "pa_decode_noalloc", "pa_reshape_and_cache",
+    "pa_copy_blocks", "pa_prefill_paged", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_get_device_error",
+    "BlockManager", "load", "PagedKVError",
 ]
 
 
@@ -131,6 +132,58 @@ def pa_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, stream=None) -> Non
         _ptr(v_pool, "v_pool", bf16=True), _ptr(slot_mapping, "slot_mapping", dtype=torch.int64),
         n_tokens, n_kv_heads, head_dim, block_size, num_blocks, _stream(stream))
     check("pa_reshape_and_cache", st)
+
+
+def _fp8_pool(t, what: str):
+    torch = _torch()
+    if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        raise TypeError(f"{what} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+    return _ptr(t, what)
+
+
+def pa_reshape_and_cache_fp8(k, v, k_pool, v_pool, slot_mapping, k_scale, v_scale, stream=None) -> None:
+    """Encodes k[t], v[t] (bf16 [n_tokens][n_kv_heads][head_dim]) as E4M3 codes
+    of x / scale[head] into the uint8 pools at slot_mapping[t]."""
+    torch = _torch()
+    n_tokens, n_kv_heads, head_dim = k.shape
+    num_blocks, hk2, block_size, hd2 = k_pool.shape
+    if (hk2, hd2) != (n_kv_heads, head_dim) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between k/v and the pools")
+    if slot_mapping.numel() != n_tokens or k_scale.numel() != n_kv_heads or v_scale.numel() != n_kv_heads:
+        raise ValueError("slot_mapping needs n_tokens entries, k_scale/v_scale n_kv_heads")
+    st = load().pa_reshape_and_cache_fp8(
+        _ptr(k, "k", bf16=True), _ptr(v, "v", bf16=True), _fp8_pool(k_pool, "k_pool"),
+        _fp8_pool(v_pool, "v_pool"), _ptr(slot_mapping, "slot_mapping", dtype=torch.int64),
+        _ptr(k_scale, "k_scale", dtype=torch.float32), _ptr(v_scale, "v_scale", dtype=torch.float32),
+        n_tokens, n_kv_heads, head_dim, block_size, num_blocks, _stream(stream))
+    check("pa_reshape_and_cache_fp8", st)
+
+
+def pa_decode_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale: float,
+                  max_context_len: int, workspace=None, partition_tokens: int = 0, stream=None) -> None:
+    """pa_decode over an E4M3 cache: K and V are decode(code) * scale of their
+    KV head. Pools uint8 [num_blocks][n_kv_heads][16][head_dim]."""
+    torch = _torch()
+    n_seqs, n_heads, head_dim = q.shape
+    num_blocks, n_kv_heads, block_size, hd2 = k_pool.shape
+    if hd2 != head_dim or tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if block_tables.dim() != 2 or block_tables.shape[0] != n_seqs or context_lens.numel() != n_seqs:
+        raise ValueError("block_tables must be [n_seqs][max_blocks], context_lens [n_seqs]")
+    if k_scale.numel() != n_kv_heads or v_scale.numel() != n_kv_heads:
+        raise ValueError("k_scale and v_scale need one entry per KV head")
+    ws_ptr, ws_bytes = C.c_void_p(None), 0
+    if workspace is not None:
+        ws_ptr = _ptr(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().pa_decode_fp8(
+        _ptr(out, "out", bf16=True), _ptr(q, "q", bf16=True), _fp8_pool(k_pool, "k_pool"),
+        _fp8_pool(v_pool, "v_pool"), _ptr(k_scale, "k_scale", dtype=torch.float32),
+        _ptr(v_scale, "v_scale", dtype=torch.float32), _ptr(block_tables, "block_tables", dtype=torch.int32),
+        _ptr(context_lens, "context_lens", dtype=torch.int32), float(scale), n_heads, n_kv_heads,
+        head_dim, block_size, n_seqs, block_tables.shape[1], int(max_context_len), num_blocks,
+        int(partition_tokens), ws_ptr, ws_bytes, _stream(stream))
+    check("pa_decode_fp8", st)
 
 
 def pa_copy_blocks(k_pool, v_pool, block_mapping, stream=None) -> None:

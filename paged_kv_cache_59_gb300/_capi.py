@@ -45,6 +45,9 @@ SIGNATURES = {
                                 i32, vp]),
     "pa_reshape_and_cache": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     "pa_copy_blocks": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp]),
+    "pa_reshape_and_cache_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
+    "pa_decode_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32,
+                            i32, i32, vp, C.c_size_t, vp]),
     "pa_prefill_paged": (i32, [vp, vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32,
                                i32, i32, vp]),
     "pa_get_device_error": (i32, [C.POINTER(C.c_int)]),

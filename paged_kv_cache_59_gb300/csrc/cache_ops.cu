@@ -1,6 +1,6 @@
-// Cache upkeep kernels: new-token scatter (reshape_and_cache) and the
-// copy-on-write block copy (copy_blocks). Both are pure bit copies moved in
-// 16-byte vectors, bound by HBM bandwidth.
+// Cache upkeep kernels: new-token scatter (reshape_and_cache, and its fp8
+// variant that encodes while it scatters) and the copy-on-write block copy
+// (copy_blocks). All are bound by HBM bandwidth.
 //
 // reshape_and_cache: each decode step appends the new token's K and V to the
 // cache ("KV Cache Explained Like You're an LLM Engineer", section "What KV
@@ -43,6 +43,62 @@ reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ 
     const long long dst = ((blk * n_kv_heads + h) * kBS + off) * chunks_per_head + c;
     k_pool[dst] = k[i];
     v_pool[dst] = v[i];
+}
+
+// fp8 (E4M3) cache write: one thread encodes one 8-element chunk of one
+// (token, KV head) row of K and the same chunk of V. Each bf16 element x
+// becomes the E4M3 code of the fp32 quotient x / scale[head] (IEEE division,
+// then round to nearest even with saturation at +-448), 8 bytes per chunk.
+__device__ __forceinline__ uint32_t e4m3x4_from_f32(float a, float b, float c, float d) {
+    // cvt.rn.satfinite.e4m3x2.f32 puts its first source in the upper byte
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b16 t;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\t"
+        "cvt.u32.u16 %0, t;\n\t}"
+        : "=r"(lo)
+        : "f"(a), "f"(b));
+    asm("{\n\t.reg .b16 t;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\t"
+        "cvt.u32.u16 %0, t;\n\t}"
+        : "=r"(hi)
+        : "f"(c), "f"(d));
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ uint2 encode_chunk(const uint4 w, float s) {
+    const float2 x0 = pa::bf16x2_to_float2(w.x), x1 = pa::bf16x2_to_float2(w.y);
+    const float2 x2 = pa::bf16x2_to_float2(w.z), x3 = pa::bf16x2_to_float2(w.w);
+    uint2 r;
+    r.x = e4m3x4_from_f32(__fdiv_rn(x0.x, s), __fdiv_rn(x0.y, s), __fdiv_rn(x1.x, s), __fdiv_rn(x1.y, s));
+    r.y = e4m3x4_from_f32(__fdiv_rn(x2.x, s), __fdiv_rn(x2.y, s), __fdiv_rn(x3.x, s), __fdiv_rn(x3.y, s));
+    return r;
+}
+
+__global__ void __launch_bounds__(256)
+reshape_and_cache_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                             uint2* __restrict__ k_pool, uint2* __restrict__ v_pool,
+                             const int64_t* __restrict__ slots, const float* __restrict__ k_scale,
+                             const float* __restrict__ v_scale, long long n_chunks, int n_kv_heads,
+                             int chunks_per_head, long long pool_slots, unsigned int* err) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    pa::launch_dependents();
+    pa::grid_dependency_wait();
+    if (i >= n_chunks) return;
+    const int per_token = n_kv_heads * chunks_per_head;
+    const long long t = i / per_token;
+    const int rem = (int)(i - t * per_token);
+    const int h = rem / chunks_per_head;
+    const int c = rem - h * chunks_per_head;
+    const int64_t slot = slots[t];
+    if (slot < 0) return;
+    if (slot >= pool_slots) {
+        if (rem == 0) pa::set_error(err, PA_DEVERR_SLOT);
+        return;
+    }
+    const long long blk = slot / kBS, off = slot % kBS;
+    const long long dst = ((blk * n_kv_heads + h) * kBS + off) * chunks_per_head + c;
+    k_pool[dst] = encode_chunk(k[i], k_scale[h]);
+    v_pool[dst] = encode_chunk(v[i], v_scale[h]);
 }
 
 // grid.x = pair, grid.y = slice of the block; each CTA copies its slice of K
@@ -92,6 +148,33 @@ extern "C" int pa_reshape_and_cache(const void* k, const void* v, void* k_pool, 
                          static_cast<const uint4*>(v), static_cast<uint4*>(k_pool),
                          static_cast<uint4*>(v_pool), slot_mapping, n_chunks, n_kv_heads, cph,
                          (long long)num_blocks * kBS, err);
+}
+
+extern "C" int pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool, void* v_pool,
+                                        const int64_t* slot_mapping, const float* k_scale,
+                                        const float* v_scale, int n_tokens, int n_kv_heads, int head_dim,
+                                        int block_size, int num_blocks, pa_stream_t stream) {
+    if (n_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (block_size != kBS) return PA_ERR_UNSUPPORTED;
+    if (head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return PA_OK;
+    if (!k || !v || !k_pool || !v_pool || !slot_mapping || !k_scale || !v_scale) return PA_ERR_INVALID_ARG;
+    if (!pa_aligned16(k) || !pa_aligned16(v) || (reinterpret_cast<uintptr_t>(k_pool) & 7u) ||
+        (reinterpret_cast<uintptr_t>(v_pool) & 7u) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+        (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+        return PA_ERR_INVALID_ARG;
+    unsigned int* err = pa_device_error_ptr();
+    if (!err) return PA_ERR_CUDA;
+    const int cph = head_dim / 8;
+    const long long n_chunks = (long long)n_tokens * n_kv_heads * cph;
+    const int threads = 256;
+    const long long blocks = (n_chunks + threads - 1) / threads;
+    if (blocks > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    return pa_launch_pdl(reshape_and_cache_fp8_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                         reinterpret_cast<cudaStream_t>(stream), static_cast<const uint4*>(k),
+                         static_cast<const uint4*>(v), static_cast<uint2*>(k_pool),
+                         static_cast<uint2*>(v_pool), slot_mapping, k_scale, v_scale, n_chunks, n_kv_heads,
+                         cph, (long long)num_blocks * kBS, err);
 }
 
 extern "C" int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs,

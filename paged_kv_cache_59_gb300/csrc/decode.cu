@@ -47,8 +47,10 @@ constexpr unsigned kFull = 0xffffffffu;
 struct DecodeParams {
     uint16_t* out;
     const uint16_t* q;
-    const uint16_t* k_pool;
-    const uint16_t* v_pool;
+    const unsigned char* k_pool;  // bf16 or E4M3 elements (see the kernel's EB)
+    const unsigned char* v_pool;
+    const float* k_scale;         // E4M3 cache: per-KV-head scales (else unused)
+    const float* v_scale;
     const int32_t* tables;
     const int32_t* ctx;
     float* ws_ml;  // [B][H][P][2]
@@ -87,7 +89,8 @@ struct TransposeReduce {
     }
 };
 
-template <int D, int G, int LPT>
+// EB = bytes per cached element: 2 (bf16) or 1 (E4M3 codes with per-head scales).
+template <int D, int G, int LPT, int EB>
 struct Shape {
     static constexpr int NCH = D / (8 * LPT);      // 16-byte chunks per lane per token row
     static constexpr int TPP = 32 / LPT;           // tokens per warp pass
@@ -95,7 +98,7 @@ struct Shape {
     static constexpr int NV = NPASS * G;           // partial dots per lane
     static constexpr int NKEEP = NV / LPT > 0 ? NV / LPT : 1;
     static constexpr int TILE_ELEMS = kBS * D;
-    static constexpr int TILE_BYTES = TILE_ELEMS * 2;
+    static constexpr int TILE_BYTES = TILE_ELEMS * EB;
     // lane-bit masks (within a warp) that do not select the head of the kept
     // values, and the subset on which kept values are duplicated
     static constexpr int HEAD_LO = LPT / G;        // masks >= HEAD_LO and < LPT select the head
@@ -117,9 +120,9 @@ struct Shape {
     static_assert(G <= LPT, "kept values of a lane must belong to one head");
 };
 
-template <int D, int G, int LPT, int NW, int S>
+template <int D, int G, int LPT, int EB, int NW, int S>
 struct Smem {
-    using SH = Shape<D, G, LPT>;
+    using SH = Shape<D, G, LPT, EB>;
     static constexpr size_t STAGES = (size_t)NW * S * 2 * SH::TILE_BYTES;
     static constexpr size_t BARS = (size_t)NW * S * 8;
     static constexpr size_t PBUF = (size_t)NW * G * kBS * 4;
@@ -129,11 +132,35 @@ struct Smem {
     static constexpr size_t TOTAL = STAGES + BARS + PBUF + ABUF;
 };
 
-template <int D, int G, int LPT, int NW, int S, int MINB>
+// Eight cached elements of a row chunk -> four float2 (element pairs 0-1,
+// 2-3, 4-5, 6-7). bf16 widens exactly by a shift; an E4M3 code widens exactly
+// to fp16 (every E4M3 value is an fp16 value) and then to fp32.
+template <int EB>
+struct Chunk8;
+template <>
+struct Chunk8<2> {
+    static __device__ __forceinline__ void load(const unsigned char* p, float2 (&f)[4]) {
+        const uint4 w = *reinterpret_cast<const uint4*>(p);
+        f[0] = pa::bf16x2_to_float2(w.x);
+        f[1] = pa::bf16x2_to_float2(w.y);
+        f[2] = pa::bf16x2_to_float2(w.z);
+        f[3] = pa::bf16x2_to_float2(w.w);
+    }
+};
+template <>
+struct Chunk8<1> {
+    static __device__ __forceinline__ void load(const unsigned char* p, float2 (&f)[4]) {
+        const uint2 w = *reinterpret_cast<const uint2*>(p);
+        pa::e4m3x4_to_float2x2(w.x, f[0], f[1]);
+        pa::e4m3x4_to_float2x2(w.y, f[2], f[3]);
+    }
+};
+
+template <int D, int G, int LPT, int EB, int NW, int S, int MINB>
 __global__ void __launch_bounds__(NW * 32, MINB)
 pa_decode_partition_kernel(const DecodeParams P) {
-    using SH = Shape<D, G, LPT>;
-    using SM = Smem<D, G, LPT, NW, S>;
+    using SH = Shape<D, G, LPT, EB>;
+    using SM = Smem<D, G, LPT, EB, NW, S>;
     constexpr int NCH = SH::NCH, TPP = SH::TPP, NPASS = SH::NPASS, NV = SH::NV;
     constexpr int NKEEP = SH::NKEEP;
     constexpr int NONHEAD = SH::nonhead_mask();
@@ -195,7 +222,7 @@ pa_decode_partition_kernel(const DecodeParams P) {
     if (lane < my_n) my_bid = P.tables[(size_t)b * P.max_blocks + blk_begin + warp + NW * lane];
 
     const uint64_t pol = pa::l2_evict_first_policy();
-    const size_t head_stride = (size_t)SH::TILE_ELEMS;
+    const size_t head_stride = (size_t)SH::TILE_BYTES;
     auto issue = [&](int i) {  // all lanes call (shuffle); lane 0 issues the copies
         const int bid = __shfl_sync(kFull, my_bid, i);
         if (lane == 0) {
@@ -215,6 +242,8 @@ pa_decode_partition_kernel(const DecodeParams P) {
     };
 
     // q for the G heads, this lane's dims, pre-scaled into the base-2 domain
+    // (an E4M3 cache folds the KV head's K scale in here: q.(code*s) = (q*s).code)
+    const float qscale = EB == 1 ? P.scale_log2 * P.k_scale[kvh] : P.scale_log2;
     float2 qf[G][NCH][4];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -226,7 +255,7 @@ pa_decode_partition_kernel(const DecodeParams P) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 float2 f = pa::bf16x2_to_float2(ws[k]);
-                qf[h][j][k] = make_float2(f.x * P.scale_log2, f.y * P.scale_log2);
+                qf[h][j][k] = make_float2(f.x * qscale, f.y * qscale);
             }
         }
     }
@@ -285,15 +314,14 @@ pa_decode_partition_kernel(const DecodeParams P) {
                 for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < NCH; ++j) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(sK + (t * D + (c + LPT * j) * 8) * 2);
-                    const float2 k0 = pa::bf16x2_to_float2(w.x), k1 = pa::bf16x2_to_float2(w.y);
-                    const float2 k2 = pa::bf16x2_to_float2(w.z), k3 = pa::bf16x2_to_float2(w.w);
+                    float2 kf[4];
+                    Chunk8<EB>::load(sK + (t * D + (c + LPT * j) * 8) * EB, kf);
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
-                        acc[h] = __ffma2_rn(qf[h][j][0], k0, acc[h]);
-                        acc[h] = __ffma2_rn(qf[h][j][1], k1, acc[h]);
-                        acc[h] = __ffma2_rn(qf[h][j][2], k2, acc[h]);
-                        acc[h] = __ffma2_rn(qf[h][j][3], k3, acc[h]);
+                        acc[h] = __ffma2_rn(qf[h][j][0], kf[0], acc[h]);
+                        acc[h] = __ffma2_rn(qf[h][j][1], kf[1], acc[h]);
+                        acc[h] = __ffma2_rn(qf[h][j][2], kf[2], acc[h]);
+                        acc[h] = __ffma2_rn(qf[h][j][3], kf[3], acc[h]);
                     }
                 }
 #pragma unroll
@@ -357,16 +385,15 @@ pa_decode_partition_kernel(const DecodeParams P) {
                 if (tok0 + t < ctx) {
 #pragma unroll
                     for (int j = 0; j < NCH; ++j) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(sV + (t * D + (c + LPT * j) * 8) * 2);
-                        const float2 v0 = pa::bf16x2_to_float2(w.x), v1 = pa::bf16x2_to_float2(w.y);
-                        const float2 v2 = pa::bf16x2_to_float2(w.z), v3 = pa::bf16x2_to_float2(w.w);
+                        float2 vf[4];
+                        Chunk8<EB>::load(sV + (t * D + (c + LPT * j) * 8) * EB, vf);
 #pragma unroll
                         for (int h = 0; h < G; ++h) {
                             const float2 pp = make_float2(pl[h][ip], pl[h][ip]);
-                            o[h][j][0] = __ffma2_rn(pp, v0, o[h][j][0]);
-                            o[h][j][1] = __ffma2_rn(pp, v1, o[h][j][1]);
-                            o[h][j][2] = __ffma2_rn(pp, v2, o[h][j][2]);
-                            o[h][j][3] = __ffma2_rn(pp, v3, o[h][j][3]);
+                            o[h][j][0] = __ffma2_rn(pp, vf[0], o[h][j][0]);
+                            o[h][j][1] = __ffma2_rn(pp, vf[1], o[h][j][1]);
+                            o[h][j][2] = __ffma2_rn(pp, vf[2], o[h][j][2]);
+                            o[h][j][3] = __ffma2_rn(pp, vf[3], o[h][j][3]);
                         }
                     }
                 }
@@ -420,6 +447,7 @@ pa_decode_partition_kernel(const DecodeParams P) {
     __syncthreads();
 
     const bool single = (nparts == 1);
+    const float vscale = EB == 1 ? P.v_scale[kvh] : 1.f;  // sum p (code*s) = s * sum p code
     for (int e = threadIdx.x; e < G * D / 2; e += NW * 32) {
         const int h = e / (D / 2), d = (e % (D / 2)) * 2;
         float M = -INFINITY;
@@ -434,6 +462,8 @@ pa_decode_partition_kernel(const DecodeParams P) {
             O0 += ov.x * f;
             O1 += ov.y * f;
         }
+        O0 *= vscale;
+        O1 *= vscale;
         const size_t row = (size_t)b * H + h0 + h;
         if (single) {
             const float inv = 1.f / L;
@@ -503,18 +533,20 @@ constexpr int kNW = 4;  // warps per CTA
 // runs two CTAs per SM. S stages of K+V tiles per warp fill the shared memory
 // of the resident CTAs (2 or 3 stages of 8 KiB at head_dim 128, 4 or 6 of
 // 4 KiB at head_dim 64).
-template <int D, int G>
+// An E4M3 cache (EB = 1) has half-size tiles and keeps the same bytes in
+// flight with twice the stages.
+template <int D, int G, int EB>
 struct Launch {
     static constexpr int LPT = (D == 128 && G >= 4) ? 16 : 8;
     static constexpr int MINB = G == 8 ? 2 : 3;
-    static constexpr int S = (D == 128 ? 2 : 4) * (MINB == 3 ? 1 : 3) / (MINB == 3 ? 1 : 2);
+    static constexpr int S = (D == 128 ? 2 : 4) * (MINB == 3 ? 1 : 3) / (MINB == 3 ? 1 : 2) * (2 / EB);
 };
 
-template <int D, int G>
+template <int D, int G, int EB>
 int launch_partition(const DecodeParams& P, int n_seqs, cudaStream_t stream) {
-    using LC = Launch<D, G>;
-    using SM = Smem<D, G, LC::LPT, kNW, LC::S>;
-    auto kern = pa_decode_partition_kernel<D, G, LC::LPT, kNW, LC::S, LC::MINB>;
+    using LC = Launch<D, G, EB>;
+    using SM = Smem<D, G, LC::LPT, EB, kNW, LC::S>;
+    auto kern = pa_decode_partition_kernel<D, G, LC::LPT, EB, kNW, LC::S, LC::MINB>;
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -528,13 +560,13 @@ int launch_partition(const DecodeParams& P, int n_seqs, cudaStream_t stream) {
     return pa_launch_pdl(kern, grid, dim3(kNW * 32), SM::TOTAL, stream, P);
 }
 
-template <int D>
+template <int D, int EB>
 int dispatch_group(int G, const DecodeParams& P, int n_seqs, cudaStream_t stream) {
     switch (G) {
-        case 1: return launch_partition<D, 1>(P, n_seqs, stream);
-        case 2: return launch_partition<D, 2>(P, n_seqs, stream);
-        case 4: return launch_partition<D, 4>(P, n_seqs, stream);
-        case 8: return launch_partition<D, 8>(P, n_seqs, stream);
+        case 1: return launch_partition<D, 1, EB>(P, n_seqs, stream);
+        case 2: return launch_partition<D, 2, EB>(P, n_seqs, stream);
+        case 4: return launch_partition<D, 4, EB>(P, n_seqs, stream);
+        case 8: return launch_partition<D, 8, EB>(P, n_seqs, stream);
         default: return PA_ERR_UNSUPPORTED;
     }
 }
@@ -564,12 +596,14 @@ extern "C" size_t pa_decode_workspace_bytes(int n_seqs, int n_heads, int head_di
     return workspace_bytes_for(n_seqs, n_heads, head_dim, max_parts);
 }
 
-extern "C" int pa_decode_ex(void* out, const void* q, const void* k_pool, const void* v_pool,
-                            const int32_t* block_tables, const int32_t* context_lens, float scale,
-                            int n_heads, int n_kv_heads, int head_dim, int block_size, int n_seqs,
-                            int max_blocks_per_seq, int max_context_len, int num_blocks,
-                            int partition_tokens, void* workspace, size_t workspace_bytes,
-                            pa_stream_t stream) {
+namespace {
+
+// Shared body of the bf16 (eb = 2) and E4M3 (eb = 1) decode entry points.
+int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void* v_pool,
+                const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                const int32_t* context_lens, float scale, int n_heads, int n_kv_heads, int head_dim,
+                int block_size, int n_seqs, int max_blocks_per_seq, int max_context_len, int num_blocks,
+                int partition_tokens, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
     if (n_seqs < 0 || max_context_len < 0 || num_blocks < 0 || max_blocks_per_seq < 0 ||
         n_heads <= 0 || n_kv_heads <= 0)
         return PA_ERR_INVALID_ARG;
@@ -587,6 +621,9 @@ extern "C" int pa_decode_ex(void* out, const void* q, const void* k_pool, const 
     if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
     if (!pa_aligned16(out) || !pa_aligned16(q) || !pa_aligned16(k_pool) || !pa_aligned16(v_pool))
         return PA_ERR_INVALID_ARG;
+    if (eb == 1 && (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
+                    (reinterpret_cast<uintptr_t>(v_scale) & 3u)))
+        return PA_ERR_INVALID_ARG;
     if (out == q) return PA_ERR_INVALID_ARG;
     const int max_parts = max_context_len > 0 ? (max_context_len + pt - 1) / pt : 1;
     const size_t need = workspace_bytes_for(n_seqs, n_heads, head_dim, max_parts);
@@ -598,8 +635,10 @@ extern "C" int pa_decode_ex(void* out, const void* q, const void* k_pool, const 
     DecodeParams P;
     P.out = static_cast<uint16_t*>(out);
     P.q = static_cast<const uint16_t*>(q);
-    P.k_pool = static_cast<const uint16_t*>(k_pool);
-    P.v_pool = static_cast<const uint16_t*>(v_pool);
+    P.k_pool = static_cast<const unsigned char*>(k_pool);
+    P.v_pool = static_cast<const unsigned char*>(v_pool);
+    P.k_scale = k_scale;
+    P.v_scale = v_scale;
     P.tables = block_tables;
     P.ctx = context_lens;
     const size_t rows = (size_t)n_seqs * n_heads * max_parts;
@@ -617,12 +656,40 @@ extern "C" int pa_decode_ex(void* out, const void* q, const void* k_pool, const 
     P.err = err;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int st = head_dim == 128 ? dispatch_group<128>(G, P, n_seqs, s) : dispatch_group<64>(G, P, n_seqs, s);
+    int st;
+    if (eb == 1)
+        st = head_dim == 128 ? dispatch_group<128, 1>(G, P, n_seqs, s) : dispatch_group<64, 1>(G, P, n_seqs, s);
+    else
+        st = head_dim == 128 ? dispatch_group<128, 2>(G, P, n_seqs, s) : dispatch_group<64, 2>(G, P, n_seqs, s);
     if (st != PA_OK || max_parts <= 1) return st;
     const int n_rows = n_seqs * n_heads;
     dim3 grid((n_rows + 3) / 4);
     if (head_dim == 128) return pa_launch_pdl(pa_decode_merge_kernel<128>, grid, dim3(128), 0, s, P, n_rows);
     return pa_launch_pdl(pa_decode_merge_kernel<64>, grid, dim3(128), 0, s, P, n_rows);
+}
+
+}  // namespace
+
+extern "C" int pa_decode_ex(void* out, const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, const int32_t* context_lens, float scale,
+                            int n_heads, int n_kv_heads, int head_dim, int block_size, int n_seqs,
+                            int max_blocks_per_seq, int max_context_len, int num_blocks,
+                            int partition_tokens, void* workspace, size_t workspace_bytes,
+                            pa_stream_t stream) {
+    return decode_impl(2, out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens, scale,
+                       n_heads, n_kv_heads, head_dim, block_size, n_seqs, max_blocks_per_seq,
+                       max_context_len, num_blocks, partition_tokens, workspace, workspace_bytes, stream);
+}
+
+extern "C" int pa_decode_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                             const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                             const int32_t* context_lens, float scale, int n_heads, int n_kv_heads,
+                             int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
+                             int max_context_len, int num_blocks, int partition_tokens, void* workspace,
+                             size_t workspace_bytes, pa_stream_t stream) {
+    return decode_impl(1, out, q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale,
+                       n_heads, n_kv_heads, head_dim, block_size, n_seqs, max_blocks_per_seq,
+                       max_context_len, num_blocks, partition_tokens, workspace, workspace_bytes, stream);
 }
 
 extern "C" int pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,

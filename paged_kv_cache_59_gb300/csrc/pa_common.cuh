@@ -154,6 +154,34 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float a, float b) {
     return r;
 }
 
+// Four E4M3 codes (bytes 0..3 of w, byte 0 first) -> (v0, v1), (v2, v3).
+// E4M3 values are a subset of fp16 values, so the hardware conversion to
+// f16x2 and the widening to fp32 are both exact.
+__device__ __forceinline__ void e4m3x4_to_float2x2(uint32_t w, float2& a, float2& b) {
+    uint32_t h0, h1;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(w));
+    float f0, f1, f2, f3;
+    asm("{\n\t.reg .f16 x, y;\n\t"
+        "mov.b32 {x, y}, %2;\n\t"
+        "cvt.f32.f16 %0, x;\n\t"
+        "cvt.f32.f16 %1, y;\n\t}"
+        : "=f"(f0), "=f"(f1)
+        : "r"(h0));
+    asm("{\n\t.reg .f16 x, y;\n\t"
+        "mov.b32 {x, y}, %2;\n\t"
+        "cvt.f32.f16 %0, x;\n\t"
+        "cvt.f32.f16 %1, y;\n\t}"
+        : "=f"(f2), "=f"(f3)
+        : "r"(h1));
+    a = make_float2(f0, f1);
+    b = make_float2(f2, f3);
+}
+
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream serialization attribute may start while the previous kernel in the
 // stream is still running; grid_dependency_wait() blocks until that kernel

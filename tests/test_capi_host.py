@@ -86,6 +86,28 @@ def test_cache_ops_argument_errors(capi):
     assert capi.pa_copy_blocks(p, p, C.c_void_p(12), 3, 2, 64, 16, 16, None) == -1
 
 
+def test_fp8_argument_errors_need_no_device(capi):
+    p = C.c_void_p(4096)
+    # cache write: block size 8, head_dim 60, missing scale, misaligned k, empty
+    assert capi.pa_reshape_and_cache_fp8(p, p, p, p, p, p, p, 4, 2, 64, 8, 16, None) == -2
+    assert capi.pa_reshape_and_cache_fp8(p, p, p, p, p, p, p, 4, 2, 60, 16, 16, None) == -2
+    assert capi.pa_reshape_and_cache_fp8(p, p, p, p, p, None, p, 4, 2, 64, 16, 16, None) == -1
+    assert capi.pa_reshape_and_cache_fp8(C.c_void_p(4104), p, p, p, p, p, p, 4, 2, 64, 16, 16, None) == -1
+    assert capi.pa_reshape_and_cache_fp8(p, p, p, p, p, p, p, 0, 2, 64, 16, 16, None) == 0
+    # decode: missing or misaligned scales, unsupported head_dim, group 3, empty batch
+    tail = [C.c_float(0.1), 8, 2, 128, 16, 4, 64, 1024, 256, 0, None, 0, None]
+    assert capi.pa_decode_fp8(p, C.c_void_p(8192), p, p, None, p, p, p, *tail) == -1
+    assert capi.pa_decode_fp8(p, C.c_void_p(8192), p, p, p, C.c_void_p(4098), p, p, *tail) == -1
+    bad_d = list(tail); bad_d[3] = 96
+    assert capi.pa_decode_fp8(p, C.c_void_p(8192), p, p, p, p, p, p, *bad_d) == -2
+    bad_g = list(tail); bad_g[1], bad_g[2] = 6, 2
+    assert capi.pa_decode_fp8(p, C.c_void_p(8192), p, p, p, p, p, p, *bad_g) == -2
+    empty = list(tail); empty[5] = 0
+    assert capi.pa_decode_fp8(p, C.c_void_p(8192), p, p, p, p, p, p, *empty) == 0
+    # a batch that needs split-K scratch and gets none
+    assert capi.pa_decode_fp8(p, C.c_void_p(8192), p, p, p, p, p, p, *tail) == -3
+
+
 # ----------------------------------------------------------- block manager --
 
 def test_block_manager_matches_model_on_random_operations(capi):
