@@ -119,6 +119,37 @@ def paged_decode_rows(q, k_pool, v_pool, block_tables, context_lens, scale, rows
     return res
 
 
+def paged_decode_window(q, k_pool, v_pool, block_tables, context_lens, scale, window) -> np.ndarray:
+    """Sliding-window decode: the query at position i = context_lens[b] - 1
+    attends to positions max(0, i - window) .. i ("KV Cache Explained Like
+    You're an LLM Engineer", section "Sliding Window Attention": token i
+    attends to tokens [i - W, i], so the cache it needs is O(W)). Blocks that
+    lie wholly before the window are never read (their table entries may be
+    -1). q [B][H][D]; returns fp64 [B][H][D]; a context <= 0 gives zeros.
+    """
+    q = np.asarray(q)
+    B, H, D = q.shape
+    Hk = np.asarray(k_pool).shape[1]
+    bs = np.asarray(k_pool).shape[2]
+    g = H // Hk
+    out = np.zeros((B, H, D), dtype=np.float64)
+    for b in range(B):
+        n = int(context_lens[b])
+        if n <= 0:
+            continue
+        lo = max(0, n - 1 - int(window))
+        rows_k, rows_v = [], []
+        for t in range(lo, n):
+            blk = int(block_tables[b][t // bs])
+            rows_k.append(np.asarray(k_pool)[blk, :, t % bs, :])
+            rows_v.append(np.asarray(v_pool)[blk, :, t % bs, :])
+        kc = _as_f64(np.stack(rows_k))
+        vc = _as_f64(np.stack(rows_v))
+        for h in range(H):
+            out[b, h] = attend(q[b, h], kc[:, h // g, :], vc[:, h // g, :], scale)
+    return out
+
+
 def paged_prefill(q, k_pool, v_pool, block_tables, context_lens, q_start_loc, scale,
                   rows=None) -> np.ndarray:
     """Causal attention of a chunk of new queries over the paged cache.

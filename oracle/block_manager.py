@@ -27,6 +27,13 @@ Readings taken where the pages are silent or disagree:
 * An append of n tokens is all-or-nothing: if the free list cannot supply
   every block it needs, nothing changes and OutOfBlocks is raised.
 * Allocation order (LIFO pop) is not part of any result the tests compare.
+* Sliding window ("KV Cache Explained Like You're an LLM Engineer", section
+  "Sliding Window Attention": attention reaches back W tokens, so the cache
+  it needs stays O(W)): ``release_before(seq, first)`` drops every block that
+  lies wholly before position ``first`` - its table entry becomes the hole -1
+  and its refcount drops (the block returns to the free list at zero).
+  Positions keep their logical block index, so later appends are unaffected;
+  fork, free and the invariants skip holes.
 """
 from __future__ import annotations
 
@@ -117,6 +124,8 @@ class BlockManagerModel:
     def make_private(self, seq_id: int, logical_block: int) -> List[Tuple[int, int]]:
         tab = self.tables[seq_id]
         b = tab[logical_block]
+        if b < 0:
+            raise BlockManagerError("block was released")
         if self.ref[b] <= 1:
             return []
         fresh = self._alloc()
@@ -132,14 +141,32 @@ class BlockManagerModel:
         self.tables[child] = list(self.tables[parent])
         self.lens[child] = self.lens[parent]
         for b in self.tables[child]:
-            self.ref[b] += 1
+            if b >= 0:
+                self.ref[b] += 1
 
     def free_seq(self, seq_id: int) -> None:
         if seq_id not in self.tables:
             raise BlockManagerError("unknown sequence")
         for b in self.tables.pop(seq_id):
-            self._put(b)
+            if b >= 0:
+                self._put(b)
         del self.lens[seq_id]
+
+    def release_before(self, seq_id: int, first_pos: int) -> List[int]:
+        """Drops the blocks wholly before logical position first_pos; returns
+        the dropped table entries (block ids), in logical order."""
+        if seq_id not in self.tables:
+            raise BlockManagerError("unknown sequence")
+        tab = self.tables[seq_id]
+        bs = self.block_size
+        first_pos = min(max(int(first_pos), 0), self.lens[seq_id])
+        dropped = []
+        for j in range(min(first_pos // bs, len(tab))):
+            if tab[j] >= 0:
+                dropped.append(tab[j])
+                self._put(tab[j])
+                tab[j] = -1
+        return dropped
 
     # -- queries -----------------------------------------------------------
     def block_table(self, seq_id: int) -> List[int]:
@@ -158,7 +185,7 @@ class BlockManagerModel:
         """Sum of refcounts == sum of table lengths; a block is free iff its
         refcount is 0; every table covers exactly ceil(len / bs) blocks."""
         total_refs = sum(self.ref)
-        total_entries = sum(len(t) for t in self.tables.values())
+        total_entries = sum(sum(1 for b in t if b >= 0) for t in self.tables.values())
         assert total_refs == total_entries, (total_refs, total_entries)
         free = set(self.free)
         assert len(free) == len(self.free), "duplicate free entry"

@@ -17,6 +17,7 @@ from .generate import (  # noqa: F401
     make_decode_case,
     make_prefill_case,
     make_decode_case_fp8,
+    make_decode_case_window,
     E4M3_NAN,
     f32_to_bf16_bits,
 )

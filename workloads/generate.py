@@ -267,6 +267,64 @@ def make_prefill_case(seed: int, chunk_ctx: Sequence[int], chunk_lens: Sequence[
 
 
 # --------------------------------------------------------------------------
+# Sliding window: only blocks that reach into the window are held
+# --------------------------------------------------------------------------
+
+def make_decode_case_window(seed: int, context_lens: Sequence[int], n_heads: int, n_kv_heads: int,
+                            head_dim: int, window: int, pool_factor: float = 1.25, n_new: int = 1,
+                            fill: str = "nan", scale: Optional[float] = None, name: str = "decode_window",
+                            rng: Optional[np.random.Generator] = None) -> Workload:
+    """A decode batch whose sequences hold only the blocks that reach into the
+    window of the query at position ctx - 1 (positions ctx-1-window .. ctx-1):
+    table entries of blocks wholly before it are -1 (released). The first
+    held block is drawn whole, so every held slot has a value.
+
+    Draw order: context lengths -> placement -> q -> K -> V (held positions
+    only, one sequence after another; this step's new token last).
+    """
+    bs = BLOCK_SIZE
+    rng = rng if rng is not None else np.random.default_rng(seed)
+    ctx = np.asarray(context_lens, dtype=np.int32)
+    B = len(ctx)
+    assert all(c >= n_new for c in ctx)
+    first_blk = [max(0, int(c) - 1 - window) // bs for c in ctx]
+    nb = [int(math.ceil(c / bs)) for c in ctx]
+    held = [n - f for n, f in zip(nb, first_blk)]
+    needed = sum(held)
+    num_blocks = max(int(math.ceil(pool_factor * needed)), needed)
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    tables = np.full((B, max(nb)), -1, dtype=np.int32)
+    cur = 0
+    for b in range(B):
+        tables[b, first_blk[b]:nb[b]] = perm[cur:cur + held[b]]
+        cur += held[b]
+    H, Hk, D = n_heads, n_kv_heads, head_dim
+    q = _normal_bf16(rng, (B, H, D))
+    fillv = BF16_NAN if fill == "nan" else 0
+    k_pool = np.full((num_blocks, Hk, bs, D), fillv, dtype=np.uint16)
+    v_pool = np.full((num_blocks, Hk, bs, D), fillv, dtype=np.uint16)
+    new_k = np.empty((B * n_new, Hk, D), dtype=np.uint16)
+    new_v = np.empty((B * n_new, Hk, D), dtype=np.uint16)
+    for pool, new in ((k_pool, new_k), (v_pool, new_v)):
+        for b in range(B):
+            c, p0 = int(ctx[b]), first_blk[b] * bs
+            rows = _normal_bf16(rng, (c - p0, Hk, D))
+            if c - n_new > p0:
+                _place(pool, tables[b], rows[:c - n_new - p0], p0)
+            new[b * n_new:(b + 1) * n_new] = rows[c - n_new - p0:]
+    slots = np.empty((B * n_new,), dtype=np.int64)
+    for b in range(B):
+        c = int(ctx[b])
+        slots[b * n_new:(b + 1) * n_new] = _slots(tables[b], range(c - n_new, c), bs)
+    wl = Workload(name=name, seed=seed, n_heads=H, n_kv_heads=Hk, head_dim=D, num_blocks=num_blocks,
+                  scale=float(scale if scale is not None else 1.0 / math.sqrt(D)),
+                  k_pool=k_pool, v_pool=v_pool, dec_tables=tables, dec_ctx=ctx, q=q,
+                  new_k=new_k, new_v=new_v, slot_mapping=slots)
+    wl.meta.update(needed_blocks=needed, n_new=n_new, window=int(window))
+    return wl
+
+
+# --------------------------------------------------------------------------
 # fp8 (E4M3) KV cache
 # --------------------------------------------------------------------------
 
@@ -410,6 +468,16 @@ def _gqa_8b_fp8(fill="nan", keep_logical=False):
                                 name="gqa8b_fp8_b64_ctx128-4096", rng=rng)
 
 
+def _swa_mistral(fill="nan", keep_logical=False):
+    """Mistral-7B-shaped sliding-window decode: 32 sequences, context
+    U{4096..32768}, window 4096, 32 q / 8 kv heads, d 128; only the blocks
+    that reach into each window are held."""
+    rng = np.random.default_rng(5)
+    ctx = rng.integers(4096, 32768, size=32, endpoint=True)
+    return make_decode_case_window(5, ctx, 32, 8, 128, 4096, fill=fill,
+                                   name="swa_mistral_b32_ctx4k-32k_w4096", rng=rng)
+
+
 WORKLOADS = {
     "tiny_mha": _tiny_mha,
     "mha_7b": _mha_7b,
@@ -417,6 +485,7 @@ WORKLOADS = {
     "gqa_70b_cow": _gqa_70b_cow,
     "mixed": _mixed,
     "gqa_8b_fp8": _gqa_8b_fp8,
+    "swa_mistral": _swa_mistral,
 }
 
 
