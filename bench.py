@@ -37,7 +37,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 DEFAULT_WORKLOAD = "gqa_8b"
 WORKLOAD_LAYERS = {"tiny_mha": 1, "mha_7b": 32, "gqa_8b": 32, "gqa_70b_cow": 80, "mixed": 32,
-                   "gqa_8b_fp8": 32}
+                   "gqa_8b_fp8": 32, "swa_mistral": 32}
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_decode_partition_gqa8b.md")
 
 
@@ -48,7 +48,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=["tiny_mha", "mha_7b", "gqa_8b", "gqa_70b_cow", "mixed", "gqa_8b_fp8"])
+                    choices=["tiny_mha", "mha_7b", "gqa_8b", "gqa_70b_cow", "mixed", "gqa_8b_fp8",
+                             "swa_mistral"])
     ap.add_argument("--partition-tokens", type=int, default=0,
                     help="decode context partition size (0 = library default)")
     ap.add_argument("--skip-baselines", action="store_true",
@@ -227,7 +228,11 @@ def run_ours(args):
     H, Hk, D = wl.n_heads, wl.n_kv_heads, wl.head_dim
     B = len(wl.dec_ctx)
     max_ctx = int(wl.dec_ctx.max())
-    sum_ctx = int(wl.dec_ctx.sum())
+    window = wl.meta.get("window")
+    if window is not None:   # tokens each query attends to: ctx-1-W .. ctx-1
+        sum_ctx = int(sum(min(int(c), window + 1) for c in wl.dec_ctx))
+    else:
+        sum_ctx = int(wl.dec_ctx.sum())
     fp8 = wl.meta.get("kv_dtype") == "fp8_e4m3"
     eb = 1 if fp8 else 2                       # bytes per cached element
     kv_bytes = sum_ctx * Hk * D * 2 * eb
@@ -279,6 +284,9 @@ def run_ours(args):
         if fp8:
             pk.pa_decode_fp8(out, q, kp, vp, ks, vs, tabs, ctx, wl.scale, max_ctx, workspace=ws,
                              partition_tokens=pt)
+        elif window is not None:
+            pk.pa_decode_window(out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, window, workspace=ws,
+                                partition_tokens=pt)
         else:
             pk.pa_decode(out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws, partition_tokens=pt)
     launches_per_step = ((1 if n_dec_new else 0) + (1 if has_pf else 0) + 1
@@ -375,6 +383,8 @@ def run_ours(args):
             "kv_bytes_per_step": kv_bytes,
             "step": ("pa_reshape_and_cache_fp8 (1 new token/seq, encoded) + pa_decode_fp8 (partition "
                      "kernel + split-K merge)" if fp8 else
+                     f"pa_reshape_and_cache (1 new token/seq) + pa_decode_window (window {window})"
+                     if window is not None else
                      "pa_reshape_and_cache (1 new token/seq) + pa_decode (partition kernel + split-K merge)"),
             "l2": f"no flush: the KV stream ({kv_bytes / 1e6:.0f} MB/step) exceeds the 129 MB L2",
             "partition_tokens": pt or 512,
@@ -477,6 +487,9 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
         if fp8_scales is not None:
             pk.pa_decode_fp8(d_out[0], q, kp, vp, *fp8_scales, tabs, ctx, wl.scale, max_ctx, workspace=ws,
                              partition_tokens=args.partition_tokens)
+        elif wl.meta.get("window") is not None:
+            pk.pa_decode_window(d_out[0], q, kp, vp, tabs, ctx, wl.scale, max_ctx, wl.meta["window"],
+                                workspace=ws, partition_tokens=args.partition_tokens)
         else:
             pk.pa_decode(d_out[0], q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws,
                          partition_tokens=args.partition_tokens)
@@ -509,7 +522,7 @@ import json, sys, time
 import numpy as np
 sys.path.insert(0, {root!r})
 from workloads import make_workload
-from oracle.attention import paged_decode
+from oracle.attention import paged_decode, paged_decode_window
 from oracle.cache_ops import reshape_and_cache
 from oracle import fp8 as ofp8
 wl = make_workload({workload!r}, fill="zero", keep_logical=False)
@@ -523,17 +536,19 @@ budget, per_step = {seconds}, {per_step}
 # compact copy of just that sequence's blocks of that KV head (built here,
 # outside the timed region), so a unit costs what its arithmetic costs.
 units = [(b, h) for b in range(B) for h in range(Hk)]
+W = wl.meta.get("window")
 def prepare(b, h):
     nblk = (int(wl.dec_ctx[b]) + 15) // 16
-    ids = wl.dec_tables[b, :nblk]
+    blk0 = max(0, int(wl.dec_ctx[b]) - 1 - W) // 16 if W is not None else 0
+    ids = wl.dec_tables[b, blk0:nblk]                  # blocks the unit reads (held blocks only)
     kp = np.ascontiguousarray(wl.k_pool[ids, h:h + 1])
     vp = np.ascontiguousarray(wl.v_pool[ids, h:h + 1])
-    table = np.arange(nblk, dtype=np.int32)[None, :]
+    table = np.concatenate([np.full(blk0, -1, np.int32), np.arange(nblk - blk0, dtype=np.int32)])[None, :]
     slot = None
     if b < n_new:
         s = int(wl.slot_mapping[b]); blk, off = s // 16, s % 16
-        pos = int(np.nonzero(ids == blk)[0][0])
-        slot = np.array([pos * 16 + off], dtype=np.int64)
+        idx = int(np.nonzero(ids == blk)[0][0])        # the block's place in the compact pool
+        slot = np.array([idx * 16 + off], dtype=np.int64)
     return kp, vp, table, slot
 kv_tok = 2 * wl.head_dim * (1 if fp8 else 2)   # K + V bytes of one token of one KV head
 done_tok = 0
@@ -557,8 +572,12 @@ while True:
             if slot is not None:
                 kp, vp = reshape_and_cache(wl.new_k[b:b + 1, h:h + 1], wl.new_v[b:b + 1, h:h + 1], kp, vp,
                                            slot)
-            paged_decode(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1], wl.scale)
-        done_tok += int(wl.dec_ctx[b])
+            if W is not None:
+                paged_decode_window(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1],
+                                    wl.scale, W)
+            else:
+                paged_decode(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1], wl.scale)
+        done_tok += int(wl.dec_ctx[b]) if W is None else min(int(wl.dec_ctx[b]), W + 1)
     dt += time.perf_counter() - t0
     n_units += len(sel)
     if {fixed_steps} and n_units >= {fixed_steps} * per_step:

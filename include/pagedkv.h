@@ -183,6 +183,26 @@ int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int
                    int n_kv_heads, int head_dim, int block_size, int num_blocks,
                    pa_stream_t stream);
 
+/* ------------------------------------------------------ sliding window */
+
+/*
+ * Sliding-window decode ([KE] "Sliding Window Attention": token i attends to
+ * tokens [i - W, i], so the cache it needs is O(W)): as pa_decode_ex, but the
+ * query at position i = context_lens[b] - 1 attends only to positions
+ * max(0, i - window) .. i (window >= 0, else PA_ERR_INVALID_ARG).
+ *     out[b][h] = sum_{i-W <= t <= i} softmax_t(scale * q[b][h] . K_b[t]) V_b[t]
+ * Table entries of blocks that lie wholly before the window are never read
+ * (they may be -1, see pa_bm_release_before); the block that holds position
+ * i - W must be present. Workspace as for pa_decode_ex (sized by
+ * max_context_len, an upper bound for any window).
+ */
+int pa_decode_window(void* out, const void* q, const void* k_pool, const void* v_pool,
+                     const int32_t* block_tables, const int32_t* context_lens, float scale,
+                     int n_heads, int n_kv_heads, int head_dim, int block_size, int n_seqs,
+                     int max_blocks_per_seq, int max_context_len, int num_blocks, int window,
+                     int partition_tokens, void* workspace, size_t workspace_bytes,
+                     pa_stream_t stream);
+
 /* ------------------------------------------------- fp8 (E4M3) KV cache */
 
 /*
@@ -311,6 +331,17 @@ int pa_bm_fork(pa_bm* bm, int64_t parent, int64_t child);
 
 /* Drops seq_id; each of its blocks is decref'd and freed at refcount 0. */
 int pa_bm_free_seq(pa_bm* bm, int64_t seq_id);
+
+/*
+ * Window release ([KE] "Sliding Window Attention"): drops every block of the
+ * sequence that lies wholly before logical position first_pos (clamped to
+ * [0, len]); its table entry becomes -1 (a hole, kept so positions keep
+ * their logical block) and its refcount drops (free list at zero). Holes are
+ * skipped by fork and free and reported as -1 by pa_bm_block_table and
+ * pa_bm_build_batch; pa_bm_make_private on a hole returns
+ * PA_ERR_INVALID_ARG. *n_released_out = entries dropped by this call.
+ */
+int pa_bm_release_before(pa_bm* bm, int64_t seq_id, int64_t first_pos, int* n_released_out);
 
 /* Copies seq_id's table into out[0..cap); *n_out = its length. PA_ERR_CAPACITY
  * (with *n_out set) if cap is too small. */

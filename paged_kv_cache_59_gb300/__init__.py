@@ -21,7 +21,8 @@ from ._capi import PagedKVError, check, load  # noqa: F401
 
 __all__ = [
     "pa_decode", "pa_decode_workspace_bytes", "decode_workspace", "pa_decode_noalloc", "pa_reshape_and_cache",
-    "pa_copy_blocks", "pa_prefill_paged", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_get_device_error",
+    "pa_copy_blocks", "pa_prefill_paged", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_window",
+    "pa_get_device_error",
     "BlockManager", "load", "PagedKVError",
 ]
 
@@ -139,6 +140,31 @@ def _fp8_pool(t, what: str):
     if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
         raise TypeError(f"{what} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
     return _ptr(t, what)
+
+
+def pa_decode_window(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,
+                     max_context_len: int, window: int, workspace=None, partition_tokens: int = 0,
+                     stream=None) -> None:
+    """Sliding-window decode: the query at position ctx-1 attends to positions
+    ctx-1-window .. ctx-1; blocks wholly before that are never read."""
+    torch = _torch()
+    n_seqs, n_heads, head_dim = q.shape
+    num_blocks, n_kv_heads, block_size, hd2 = k_pool.shape
+    if hd2 != head_dim or tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if block_tables.dim() != 2 or block_tables.shape[0] != n_seqs or context_lens.numel() != n_seqs:
+        raise ValueError("block_tables must be [n_seqs][max_blocks], context_lens [n_seqs]")
+    ws_ptr, ws_bytes = C.c_void_p(None), 0
+    if workspace is not None:
+        ws_ptr = _ptr(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().pa_decode_window(
+        _ptr(out, "out", bf16=True), _ptr(q, "q", bf16=True), _ptr(k_pool, "k_pool", bf16=True),
+        _ptr(v_pool, "v_pool", bf16=True), _ptr(block_tables, "block_tables", dtype=torch.int32),
+        _ptr(context_lens, "context_lens", dtype=torch.int32), float(scale), n_heads, n_kv_heads,
+        head_dim, block_size, n_seqs, block_tables.shape[1], int(max_context_len), num_blocks, int(window),
+        int(partition_tokens), ws_ptr, ws_bytes, _stream(stream))
+    check("pa_decode_window", st)
 
 
 def pa_reshape_and_cache_fp8(k, v, k_pool, v_pool, slot_mapping, k_scale, v_scale, stream=None) -> None:
@@ -266,6 +292,13 @@ class BlockManager:
 
     def free_seq(self, seq_id: int) -> None:
         check("pa_bm_free_seq", self._lib.pa_bm_free_seq(self._h, seq_id))
+
+    def release_before(self, seq_id: int, first_pos: int) -> int:
+        """Drops the blocks wholly before logical position first_pos (sliding
+        window); their table entries become -1. Returns how many were dropped."""
+        n = C.c_int(0)
+        check("pa_bm_release_before", self._lib.pa_bm_release_before(self._h, seq_id, first_pos, C.byref(n)))
+        return n.value
 
     def block_table(self, seq_id: int) -> List[int]:
         n = C.c_int(0)

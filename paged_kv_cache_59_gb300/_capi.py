@@ -45,6 +45,8 @@ SIGNATURES = {
                                 i32, vp]),
     "pa_reshape_and_cache": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     "pa_copy_blocks": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp]),
+    "pa_decode_window": (i32, [vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32, i32,
+                               i32, i32, vp, C.c_size_t, vp]),
     "pa_reshape_and_cache_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     "pa_decode_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32,
                             i32, i32, vp, C.c_size_t, vp]),
@@ -60,6 +62,7 @@ SIGNATURES = {
     "pa_bm_make_private": (i32, [vp, i64, i32, p_i64, C.POINTER(C.c_int)]),
     "pa_bm_fork": (i32, [vp, i64, i64]),
     "pa_bm_free_seq": (i32, [vp, i64]),
+    "pa_bm_release_before": (i32, [vp, i64, i64, C.POINTER(C.c_int)]),
     "pa_bm_block_table": (i32, [vp, i64, p_i32, i32, C.POINTER(C.c_int)]),
     "pa_bm_seq_len": (i64, [vp, i64]),
     "pa_bm_num_free": (i32, [vp]),

@@ -12,6 +12,10 @@
 //    private block.
 //  - "Modern AI Infrastructure and Agentic System Design", 9.1, copy-on-write
 //    figure: a write into a shared block copies it into a fresh one first.
+//  - "KV Cache Explained Like You're an LLM Engineer", section "Sliding Window
+//    Attention": with a window the cache a sequence needs stays O(W); blocks
+//    wholly before the window are released (table entry -1, a hole) and
+//    return to the free list when no table references them.
 #include <cstdint>
 #include <new>
 #include <unordered_map>
@@ -113,6 +117,7 @@ int pa_bm_make_private(pa_bm* bm, int64_t seq_id, int logical_block, int64_t* pa
     if (logical_block < 0 || logical_block >= (int)s.table.size()) return PA_ERR_INVALID_ARG;
     *n_out = 0;
     int32_t b = s.table[logical_block];
+    if (b < 0) return PA_ERR_INVALID_ARG;  // released by the window
     if (bm->ref[b] <= 1) return PA_OK;
     if (bm->free_list.empty()) return PA_ERR_OOM;
     int32_t fresh = bm->alloc();
@@ -129,7 +134,8 @@ int pa_bm_fork(pa_bm* bm, int64_t parent, int64_t child) {
     auto it = bm->seqs.find(parent);
     if (it == bm->seqs.end() || bm->seqs.count(child)) return PA_ERR_REFCOUNT;
     pa_bm::Seq c = it->second;  // copy before emplace may rehash
-    for (int32_t b : c.table) bm->ref[b] += 1;
+    for (int32_t b : c.table)
+        if (b >= 0) bm->ref[b] += 1;
     bm->seqs.emplace(child, std::move(c));
     return PA_OK;
 }
@@ -139,10 +145,31 @@ int pa_bm_free_seq(pa_bm* bm, int64_t seq_id) {
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PA_ERR_REFCOUNT;
     for (int32_t b : it->second.table) {
-        if (bm->ref[b] <= 0) return PA_ERR_REFCOUNT;  // cannot happen if state is consistent
+        if (b >= 0 && bm->ref[b] <= 0) return PA_ERR_REFCOUNT;  // cannot happen if state is consistent
     }
-    for (int32_t b : it->second.table) bm->put(b);
+    for (int32_t b : it->second.table)
+        if (b >= 0) bm->put(b);
     bm->seqs.erase(it);
+    return PA_OK;
+}
+
+int pa_bm_release_before(pa_bm* bm, int64_t seq_id, int64_t first_pos, int* n_released_out) {
+    if (!bm || !n_released_out) return PA_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PA_ERR_REFCOUNT;
+    pa_bm::Seq& s = it->second;
+    if (first_pos < 0) first_pos = 0;
+    if (first_pos > s.len) first_pos = s.len;
+    const int64_t whole = first_pos / bm->block_size;  // blocks wholly before first_pos
+    int n = 0;
+    for (int64_t j = 0; j < whole && j < (int64_t)s.table.size(); ++j) {
+        if (s.table[j] >= 0) {
+            bm->put(s.table[j]);
+            s.table[j] = -1;
+            ++n;
+        }
+    }
+    *n_released_out = n;
     return PA_OK;
 }
 

@@ -62,8 +62,14 @@ struct DecodeParams {
     int num_blocks;
     int part_blocks;
     int max_parts;
+    int window;  // >= 0: the query at position ctx-1 sees positions ctx-1-window .. ctx-1
     unsigned int* err;
 };
+
+// First block and partition count of a sequence's (windowed) context.
+__device__ __forceinline__ int first_position(const DecodeParams& P, int ctx) {
+    return P.window >= 0 ? max(0, ctx - 1 - P.window) : 0;
+}
 
 // Transposing butterfly: N values per lane are summed across the lanes that
 // differ in bits M, M/2, ..., 1; each level keeps half of the values.
@@ -190,15 +196,20 @@ pa_decode_partition_kernel(const DecodeParams P) {
         return;
     }
     int nblk = (ctx + kBS - 1) / kBS;
-    int nparts = (nblk + P.part_blocks - 1) / P.part_blocks;
+    // sliding window: blocks wholly before the window are never read (their
+    // table entries may be released); positions before it are masked
+    const int first_pos = first_position(P, ctx);
+    int blk_first = first_pos / kBS;
+    int nparts = (nblk - blk_first + P.part_blocks - 1) / P.part_blocks;
     if (nblk > P.max_blocks || nparts > P.max_parts) {  // caller broke the bounds it passed
         if (p == 0 && threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_CONTEXT);
         nblk = min(nblk, P.max_blocks);
-        nparts = min((nblk + P.part_blocks - 1) / P.part_blocks, P.max_parts);
-        nblk = min(nblk, nparts * P.part_blocks);
+        blk_first = min(blk_first, nblk);
+        nparts = min((nblk - blk_first + P.part_blocks - 1) / P.part_blocks, P.max_parts);
+        nblk = min(nblk, blk_first + nparts * P.part_blocks);
     }
     if (p >= nparts) return;
-    const int blk_begin = p * P.part_blocks;
+    const int blk_begin = blk_first + p * P.part_blocks;
     const int nb_local = min(blk_begin + P.part_blocks, nblk) - blk_begin;
     const int my_n = nb_local > warp ? (nb_local - warp + NW - 1) / NW : 0;  // <= 32
 
@@ -334,7 +345,7 @@ pa_decode_partition_kernel(const DecodeParams P) {
 #pragma unroll
             for (int k = 0; k < NKEEP; ++k) {
                 const int t = (ip0 + k) * TPP + tg;
-                sc[k] = (tok0 + t < ctx) ? sc[k] : -INFINITY;
+                sc[k] = (tok0 + t < ctx && tok0 + t >= first_pos) ? sc[k] : -INFINITY;
                 tmax = fmaxf(tmax, sc[k]);
             }
 #pragma unroll
@@ -382,7 +393,7 @@ pa_decode_partition_kernel(const DecodeParams P) {
 #pragma unroll
             for (int ip = 0; ip < NPASS; ++ip) {
                 const int t = ip * TPP + tg;
-                if (tok0 + t < ctx) {
+                if (tok0 + t < ctx && tok0 + t >= first_pos) {
 #pragma unroll
                     for (int j = 0; j < NCH; ++j) {
                         float2 vf[4];
@@ -494,7 +505,8 @@ pa_decode_merge_kernel(const DecodeParams P, int n_rows) {
     const int ctx = P.ctx[b];
     if (ctx <= 0) return;
     const int nblk = min((ctx + kBS - 1) / kBS, P.max_blocks);
-    const int nparts = min((nblk + P.part_blocks - 1) / P.part_blocks, P.max_parts);
+    const int blk_first = min(first_position(P, ctx) / kBS, nblk);
+    const int nparts = min((nblk - blk_first + P.part_blocks - 1) / P.part_blocks, P.max_parts);
     if (nparts <= 1) return;  // the partition kernel wrote this row
     const size_t slot0 = (size_t)row * P.max_parts;
     float M = -INFINITY;
@@ -603,7 +615,8 @@ int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void
                 const float* k_scale, const float* v_scale, const int32_t* block_tables,
                 const int32_t* context_lens, float scale, int n_heads, int n_kv_heads, int head_dim,
                 int block_size, int n_seqs, int max_blocks_per_seq, int max_context_len, int num_blocks,
-                int partition_tokens, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+                int window, int partition_tokens, void* workspace, size_t workspace_bytes,
+                pa_stream_t stream) {
     if (n_seqs < 0 || max_context_len < 0 || num_blocks < 0 || max_blocks_per_seq < 0 ||
         n_heads <= 0 || n_kv_heads <= 0)
         return PA_ERR_INVALID_ARG;
@@ -653,6 +666,7 @@ int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void
     P.num_blocks = num_blocks;
     P.part_blocks = pt / kBS;
     P.max_parts = max_parts;
+    P.window = window;
     P.err = err;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -678,7 +692,21 @@ extern "C" int pa_decode_ex(void* out, const void* q, const void* k_pool, const 
                             pa_stream_t stream) {
     return decode_impl(2, out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens, scale,
                        n_heads, n_kv_heads, head_dim, block_size, n_seqs, max_blocks_per_seq,
-                       max_context_len, num_blocks, partition_tokens, workspace, workspace_bytes, stream);
+                       max_context_len, num_blocks, -1, partition_tokens, workspace, workspace_bytes,
+                       stream);
+}
+
+extern "C" int pa_decode_window(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                const int32_t* block_tables, const int32_t* context_lens, float scale,
+                                int n_heads, int n_kv_heads, int head_dim, int block_size, int n_seqs,
+                                int max_blocks_per_seq, int max_context_len, int num_blocks, int window,
+                                int partition_tokens, void* workspace, size_t workspace_bytes,
+                                pa_stream_t stream) {
+    if (window < 0) return PA_ERR_INVALID_ARG;
+    return decode_impl(2, out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens, scale,
+                       n_heads, n_kv_heads, head_dim, block_size, n_seqs, max_blocks_per_seq,
+                       max_context_len, num_blocks, window, partition_tokens, workspace, workspace_bytes,
+                       stream);
 }
 
 extern "C" int pa_decode_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -689,7 +717,8 @@ extern "C" int pa_decode_fp8(void* out, const void* q, const void* k_pool, const
                              size_t workspace_bytes, pa_stream_t stream) {
     return decode_impl(1, out, q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale,
                        n_heads, n_kv_heads, head_dim, block_size, n_seqs, max_blocks_per_seq,
-                       max_context_len, num_blocks, partition_tokens, workspace, workspace_bytes, stream);
+                       max_context_len, num_blocks, -1, partition_tokens, workspace, workspace_bytes,
+                       stream);
 }
 
 extern "C" int pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,

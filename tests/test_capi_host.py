@@ -8,7 +8,7 @@ import re
 
 import pytest
 
-from oracle.block_manager import BlockManagerModel, OutOfBlocks
+from oracle.block_manager import BlockManagerError, BlockManagerModel, OutOfBlocks
 from tests.conftest import ROOT
 
 
@@ -144,8 +144,16 @@ def test_block_manager_matches_model_on_random_operations(capi):
                     except OutOfBlocks:
                         with pytest.raises(PagedKVError):
                             bm.make_private(s, lb)
+                    except BlockManagerError:          # a block released by the window
+                        with pytest.raises(PagedKVError) as e:
+                            bm.make_private(s, lb)
+                        assert e.value.status == -1
                     else:
                         assert bm.make_private(s, lb) == want
+            elif op < 0.9:
+                s = rng.choice(live)
+                first = rng.randint(0, model.seq_len(s) + 5)
+                assert bm.release_before(s, first) == len(model.release_before(s, first))
             else:
                 s = rng.choice(live)
                 model.free_seq(s); bm.free_seq(s); live.remove(s)
