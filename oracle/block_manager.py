@@ -34,10 +34,33 @@ Readings taken where the pages are silent or disagree:
   and its refcount drops (the block returns to the free list at zero).
   Positions keep their logical block index, so later appends are unaffected;
   fork, free and the invariants skip holes.
+* Prefix caching ("Modular LLM Inference Engine from Scratch", section
+  "Prefix caching - skip recomputing the same prompt": a hash-based LRU cache
+  whose lookup returns the longest cached prefix made of whole blocks and
+  refreshes it; "Inference serving: the KV-cache machine" and "KV Cache
+  Explained Like You're an LLM Engineer", section "Prefix Caching": a shared
+  prompt's KV is computed once and shared). Reading taken:
+  - a cache entry is one full block, keyed by the exact token prefix that
+    ends with it (all tokens from position 0 through the block's last), so a
+    block is shared only when everything before it matches too;
+  - ``cache_full_blocks(seq, tokens)`` registers the sequence's full blocks
+    (those whose 16 tokens are all in the sequence); each new entry holds one
+    reference to its block and goes to the most-recently-used end; entries
+    already present are left where they are;
+  - ``add_seq_cached(seq, tokens)`` starts a sequence on the longest run of
+    leading blocks whose prefixes are all cached (the longest cached prefix
+    of whole blocks), increfs them, sets its length to that many tokens and
+    moves those entries to the most-recently-used end, first block first;
+  - when an allocation finds the free list empty, entries are evicted from
+    the least-recently-used end, skipping entries whose block a table still
+    references, until a block is free; an append or a copy succeeds iff the
+    free list plus the evictable entries cover it (all-or-nothing);
+  - refcount = table references + cache entries.
 """
 from __future__ import annotations
 
-from typing import Dict, List, Tuple
+from collections import OrderedDict
+from typing import Dict, List, Sequence, Tuple
 
 
 class OutOfBlocks(Exception):
@@ -57,11 +80,28 @@ class BlockManagerModel:
         self.ref: List[int] = [0] * num_blocks
         self.tables: Dict[int, List[int]] = {}
         self.lens: Dict[int, int] = {}
+        # prefix cache: exact token prefix (tuple) -> block id, oldest first
+        self.cache: "OrderedDict[tuple, int]" = OrderedDict()
 
     # -- allocation primitives ---------------------------------------------
+    def _evictable(self) -> int:
+        return sum(1 for b in self.cache.values() if self.ref[b] == 1)
+
+    def available(self) -> int:
+        """Blocks an allocation can obtain: free ones plus evictable cache entries."""
+        return len(self.free) + self._evictable()
+
+    def _evict_one(self) -> None:
+        for key, b in self.cache.items():          # least recently used first
+            if self.ref[b] == 1:
+                del self.cache[key]
+                self._put(b)
+                return
+        raise OutOfBlocks()
+
     def _alloc(self) -> int:
         if not self.free:
-            raise OutOfBlocks()
+            self._evict_one()
         b = self.free.pop()
         assert self.ref[b] == 0
         self.ref[b] = 1
@@ -100,7 +140,7 @@ class BlockManagerModel:
             raise BlockManagerError("unknown sequence")
         if n < 0:
             raise BlockManagerError("negative count")
-        if self._blocks_needed(seq_id, n) > len(self.free):
+        if self._blocks_needed(seq_id, n) > self.available():
             raise OutOfBlocks()
         bs = self.block_size
         tab = self.tables[seq_id]
@@ -128,6 +168,8 @@ class BlockManagerModel:
             raise BlockManagerError("block was released")
         if self.ref[b] <= 1:
             return []
+        if self.available() < 1:
+            raise OutOfBlocks()
         fresh = self._alloc()
         self._put(b)
         tab[logical_block] = fresh
@@ -168,6 +210,56 @@ class BlockManagerModel:
                 tab[j] = -1
         return dropped
 
+    # -- prefix cache --------------------------------------------------------
+    def cache_full_blocks(self, seq_id: int, tokens: Sequence[int]) -> int:
+        """Registers the sequence's full blocks under their token prefixes;
+        returns how many entries were added. ``tokens`` are the sequence's
+        token ids from position 0 (at least as many as its full blocks)."""
+        if seq_id not in self.tables:
+            raise BlockManagerError("unknown sequence")
+        bs = self.block_size
+        tab = self.tables[seq_id]
+        n_full = min(self.lens[seq_id], len(tokens)) // bs
+        added = 0
+        for j in range(n_full):
+            if tab[j] < 0:
+                continue                                 # released by a window
+            key = tuple(int(t) for t in tokens[:(j + 1) * bs])
+            if key in self.cache:
+                continue
+            self.cache[key] = tab[j]
+            self.ref[tab[j]] += 1
+            added += 1
+        return added
+
+    def lookup(self, tokens: Sequence[int]) -> List[int]:
+        """Blocks of the longest cached prefix of whole blocks (no LRU update)."""
+        bs = self.block_size
+        blocks = []
+        for j in range(len(tokens) // bs):
+            b = self.cache.get(tuple(int(t) for t in tokens[:(j + 1) * bs]))
+            if b is None:
+                break
+            blocks.append(b)
+        return blocks
+
+    def add_seq_cached(self, seq_id: int, tokens: Sequence[int]) -> int:
+        """Starts a sequence on the longest cached prefix of ``tokens``;
+        returns the number of tokens it already holds."""
+        if seq_id in self.tables:
+            raise BlockManagerError("sequence exists")
+        bs = self.block_size
+        blocks = self.lookup(tokens)
+        for j, b in enumerate(blocks):
+            self.cache.move_to_end(tuple(int(t) for t in tokens[:(j + 1) * bs]))
+            self.ref[b] += 1
+        self.tables[seq_id] = list(blocks)
+        self.lens[seq_id] = len(blocks) * bs
+        return len(blocks) * bs
+
+    def num_cached(self) -> int:
+        return len(self.cache)
+
     # -- queries -----------------------------------------------------------
     def block_table(self, seq_id: int) -> List[int]:
         return list(self.tables[seq_id])
@@ -185,7 +277,8 @@ class BlockManagerModel:
         """Sum of refcounts == sum of table lengths; a block is free iff its
         refcount is 0; every table covers exactly ceil(len / bs) blocks."""
         total_refs = sum(self.ref)
-        total_entries = sum(sum(1 for b in t if b >= 0) for t in self.tables.values())
+        total_entries = (sum(sum(1 for b in t if b >= 0) for t in self.tables.values())
+                         + len(self.cache))
         assert total_refs == total_entries, (total_refs, total_entries)
         free = set(self.free)
         assert len(free) == len(self.free), "duplicate free entry"
