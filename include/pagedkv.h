@@ -343,6 +343,34 @@ int pa_bm_free_seq(pa_bm* bm, int64_t seq_id);
  */
 int pa_bm_release_before(pa_bm* bm, int64_t seq_id, int64_t first_pos, int* n_released_out);
 
+/*
+ * Prefix caching ("Modular LLM Inference Engine from Scratch", section
+ * "Prefix caching - skip recomputing the same prompt": a hash-based LRU cache
+ * whose lookup finds the longest cached prefix of whole blocks; [DR], [KE]
+ * "Prefix Caching": a shared prompt's KV is computed once). An entry is one
+ * full block, identified by all tokens from position 0 through its last
+ * (a 128-bit chained hash of them); each entry holds one reference to its
+ * block. When an allocation (append, copy-on-write, make_private) finds the
+ * free list empty it evicts entries from the least-recently-used end,
+ * skipping blocks a table still holds; appends stay all-or-nothing over
+ * free + evictable blocks.
+ *
+ * pa_bm_cache_blocks: registers the sequence's full blocks (the first
+ * min(n_tokens, len) / block_size, tokens = the sequence's token ids from
+ * position 0); new entries go to the most-recently-used end, entries that
+ * exist are left in place; *n_added_out = entries added.
+ * pa_bm_add_seq_cached: creates seq_id on the longest run of leading blocks
+ * whose prefixes of tokens[0..n_tokens) are cached (incref'd, refreshed in
+ * block order); *n_cached_out = tokens it already holds (a multiple of the
+ * block size) - append the rest with pa_bm_append_tokens.
+ * pa_bm_num_cached: number of entries.
+ */
+int pa_bm_cache_blocks(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int64_t n_tokens,
+                       int* n_added_out);
+int pa_bm_add_seq_cached(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int64_t n_tokens,
+                         int64_t* n_cached_out);
+int pa_bm_num_cached(const pa_bm* bm);
+
 /* Copies seq_id's table into out[0..cap); *n_out = its length. PA_ERR_CAPACITY
  * (with *n_out set) if cap is too small. */
 int pa_bm_block_table(const pa_bm* bm, int64_t seq_id, int32_t* out, int cap, int* n_out);

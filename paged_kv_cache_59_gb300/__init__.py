@@ -293,6 +293,26 @@ class BlockManager:
     def free_seq(self, seq_id: int) -> None:
         check("pa_bm_free_seq", self._lib.pa_bm_free_seq(self._h, seq_id))
 
+    def cache_blocks(self, seq_id: int, tokens: Sequence[int]) -> int:
+        """Registers the sequence's full blocks in the prefix cache; returns
+        how many entries were added."""
+        arr = (C.c_int32 * max(len(tokens), 1))(*tokens)
+        n = C.c_int(0)
+        check("pa_bm_cache_blocks", self._lib.pa_bm_cache_blocks(self._h, seq_id, arr, len(tokens), C.byref(n)))
+        return n.value
+
+    def add_seq_cached(self, seq_id: int, tokens: Sequence[int]) -> int:
+        """Starts a sequence on the longest cached prefix of tokens; returns
+        the number of tokens it already holds."""
+        arr = (C.c_int32 * max(len(tokens), 1))(*tokens)
+        n = C.c_int64(0)
+        check("pa_bm_add_seq_cached", self._lib.pa_bm_add_seq_cached(self._h, seq_id, arr, len(tokens),
+                                                                      C.byref(n)))
+        return n.value
+
+    def num_cached(self) -> int:
+        return self._lib.pa_bm_num_cached(self._h)
+
     def release_before(self, seq_id: int, first_pos: int) -> int:
         """Drops the blocks wholly before logical position first_pos (sliding
         window); their table entries become -1. Returns how many were dropped."""

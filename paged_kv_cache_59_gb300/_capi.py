@@ -63,6 +63,9 @@ SIGNATURES = {
     "pa_bm_fork": (i32, [vp, i64, i64]),
     "pa_bm_free_seq": (i32, [vp, i64]),
     "pa_bm_release_before": (i32, [vp, i64, i64, C.POINTER(C.c_int)]),
+    "pa_bm_cache_blocks": (i32, [vp, i64, p_i32, i64, C.POINTER(C.c_int)]),
+    "pa_bm_add_seq_cached": (i32, [vp, i64, p_i32, i64, p_i64]),
+    "pa_bm_num_cached": (i32, [vp]),
     "pa_bm_block_table": (i32, [vp, i64, p_i32, i32, C.POINTER(C.c_int)]),
     "pa_bm_seq_len": (i64, [vp, i64]),
     "pa_bm_num_free": (i32, [vp]),

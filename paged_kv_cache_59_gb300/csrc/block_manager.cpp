@@ -16,31 +16,103 @@
 //    Attention": with a window the cache a sequence needs stays O(W); blocks
 //    wholly before the window are released (table entry -1, a hole) and
 //    return to the free list when no table references them.
+//  - "Modular LLM Inference Engine from Scratch", section "Prefix caching -
+//    skip recomputing the same prompt": a hash-based LRU cache of prompt
+//    prefixes; lookup returns the longest cached prefix of whole blocks and
+//    refreshes it. An entry is one full block, identified by all the tokens
+//    from position 0 through its last one; the cache holds one reference per
+//    entry; an allocation that finds the free list empty evicts entries from
+//    the least-recently-used end, skipping blocks a table still holds.
+//
+// A prefix is identified by a 128-bit hash chained over its tokens (two
+// independent 64-bit chains, each token absorbed with the splitmix64
+// finalizer of Steele, Lea and Flood); distinct prefixes collide with
+// probability about 2^-128 per pair.
 #include <cstdint>
+#include <list>
 #include <new>
 #include <unordered_map>
 #include <vector>
 
 #include "../../include/pagedkv.h"
 
+namespace {
+
+uint64_t mix64(uint64_t z) {  // splitmix64 finalizer
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    return z ^ (z >> 31);
+}
+
+struct PrefixKey {
+    uint64_t a, b;
+    bool operator==(const PrefixKey& o) const { return a == o.a && b == o.b; }
+};
+struct PrefixKeyHash {
+    size_t operator()(const PrefixKey& k) const { return (size_t)(k.a ^ (k.b * 0x9e3779b97f4a7c15ull)); }
+};
+
+// Extends the hash of a prefix by the tokens [t, t + n).
+PrefixKey extend(PrefixKey h, const int32_t* t, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) {
+        const uint64_t v = (uint64_t)(uint32_t)t[i];
+        h.a = mix64(h.a ^ (v + 0x632be59bd9b4e019ull));
+        h.b = mix64(h.b + v * 0xd6e8feb86659fd93ull + 0x8cb92ba72f3d8dd7ull);
+    }
+    return h;
+}
+constexpr PrefixKey kEmptyPrefix = {0x243f6a8885a308d3ull, 0x13198a2e03707344ull};
+
+}  // namespace
+
 struct pa_bm {
     int block_size = 16;
     std::vector<int32_t> free_list;  // LIFO: back() is the next allocation
-    std::vector<int32_t> ref;
+    std::vector<int32_t> ref;        // table references + cache entries
+    std::vector<uint8_t> cached;     // block has a cache entry
+    int64_t evictable = 0;           // cache entries whose block only the cache holds
     struct Seq {
         std::vector<int32_t> table;
         int64_t len = 0;
     };
     std::unordered_map<int64_t, Seq> seqs;
+    struct Entry {
+        PrefixKey key;
+        int32_t block;
+    };
+    std::list<Entry> lru;  // front = least recently used
+    std::unordered_map<PrefixKey, std::list<Entry>::iterator, PrefixKeyHash> index;
 
-    int32_t alloc() {
+    void inc(int32_t b) {
+        if (cached[b] && ref[b] == 1) --evictable;
+        ++ref[b];
+    }
+    void put(int32_t b) {
+        --ref[b];
+        if (cached[b] && ref[b] == 1) ++evictable;
+        if (ref[b] == 0) free_list.push_back(b);
+    }
+    int64_t available() const { return (int64_t)free_list.size() + evictable; }
+    // Drops the least recently used entry whose block only the cache holds.
+    bool evict_one() {
+        for (auto it = lru.begin(); it != lru.end(); ++it) {
+            const int32_t b = it->block;
+            if (ref[b] != 1) continue;
+            index.erase(it->key);
+            lru.erase(it);
+            cached[b] = 0;
+            --evictable;
+            put(b);  // 1 -> 0: back to the free list
+            return true;
+        }
+        return false;
+    }
+    int32_t alloc() {  // callers check available() first
+        if (free_list.empty()) evict_one();
         int32_t b = free_list.back();
         free_list.pop_back();
         ref[b] = 1;
         return b;
-    }
-    void put(int32_t b) {
-        if (--ref[b] == 0) free_list.push_back(b);
     }
 };
 
@@ -53,6 +125,7 @@ pa_bm* pa_bm_create(int num_blocks, int block_size) {
     try {
         bm->block_size = block_size;
         bm->ref.assign(num_blocks, 0);
+        bm->cached.assign(num_blocks, 0);
         bm->free_list.resize(num_blocks);
         for (int i = 0; i < num_blocks; ++i) bm->free_list[i] = i;
     } catch (...) {
@@ -85,7 +158,7 @@ int pa_bm_append_tokens(pa_bm* bm, int64_t seq_id, int n, int64_t* slots_out,
     int64_t have = (int64_t)s.table.size() * bs - s.len;
     int64_t extra = n - have;
     int64_t need = (tail_cow ? 1 : 0) + (extra > 0 ? (extra + bs - 1) / bs : 0);
-    if (need > (int64_t)bm->free_list.size()) return PA_ERR_OOM;
+    if (need > bm->available()) return PA_ERR_OOM;
     if (tail_cow && (cow_cap < 1 || !cow_pairs_out || !n_cow_out)) return PA_ERR_CAPACITY;
     for (int i = 0; i < n; ++i) {
         int64_t L = s.len;
@@ -119,7 +192,7 @@ int pa_bm_make_private(pa_bm* bm, int64_t seq_id, int logical_block, int64_t* pa
     int32_t b = s.table[logical_block];
     if (b < 0) return PA_ERR_INVALID_ARG;  // released by the window
     if (bm->ref[b] <= 1) return PA_OK;
-    if (bm->free_list.empty()) return PA_ERR_OOM;
+    if (bm->available() < 1) return PA_ERR_OOM;
     int32_t fresh = bm->alloc();
     bm->put(b);
     s.table[logical_block] = fresh;
@@ -135,7 +208,7 @@ int pa_bm_fork(pa_bm* bm, int64_t parent, int64_t child) {
     if (it == bm->seqs.end() || bm->seqs.count(child)) return PA_ERR_REFCOUNT;
     pa_bm::Seq c = it->second;  // copy before emplace may rehash
     for (int32_t b : c.table)
-        if (b >= 0) bm->ref[b] += 1;
+        if (b >= 0) bm->inc(b);
     bm->seqs.emplace(child, std::move(c));
     return PA_OK;
 }
@@ -171,6 +244,62 @@ int pa_bm_release_before(pa_bm* bm, int64_t seq_id, int64_t first_pos, int* n_re
     }
     *n_released_out = n;
     return PA_OK;
+}
+
+int pa_bm_cache_blocks(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int64_t n_tokens,
+                       int* n_added_out) {
+    if (!bm || !n_added_out || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PA_ERR_REFCOUNT;
+    const pa_bm::Seq& s = it->second;
+    const int64_t bs = bm->block_size;
+    const int64_t n_full = (n_tokens < s.len ? n_tokens : s.len) / bs;
+    int added = 0;
+    PrefixKey h = kEmptyPrefix;
+    try {
+        for (int64_t j = 0; j < n_full; ++j) {
+            h = extend(h, tokens + j * bs, bs);
+            const int32_t b = s.table[j];
+            if (b < 0 || bm->index.count(h)) continue;  // released, or already cached
+            bm->lru.push_back({h, b});
+            bm->index.emplace(h, std::prev(bm->lru.end()));
+            bm->inc(b);  // held by the table too, so it is not evictable
+            bm->cached[b] = 1;
+            ++added;
+        }
+    } catch (...) {
+        *n_added_out = added;
+        return PA_ERR_OOM;
+    }
+    *n_added_out = added;
+    return PA_OK;
+}
+
+int pa_bm_add_seq_cached(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int64_t n_tokens,
+                         int64_t* n_cached_out) {
+    if (!bm || !n_cached_out || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID_ARG;
+    if (bm->seqs.count(seq_id)) return PA_ERR_REFCOUNT;
+    const int64_t bs = bm->block_size;
+    pa_bm::Seq s;
+    PrefixKey h = kEmptyPrefix;
+    for (int64_t j = 0; j < n_tokens / bs; ++j) {
+        h = extend(h, tokens + j * bs, bs);
+        auto f = bm->index.find(h);
+        if (f == bm->index.end()) break;
+        bm->lru.splice(bm->lru.end(), bm->lru, f->second);  // most recently used
+        const int32_t b = f->second->block;
+        bm->inc(b);
+        s.table.push_back(b);
+    }
+    s.len = (int64_t)s.table.size() * bs;
+    *n_cached_out = s.len;
+    bm->seqs.emplace(seq_id, std::move(s));
+    return PA_OK;
+}
+
+int pa_bm_num_cached(const pa_bm* bm) {
+    if (!bm) return PA_ERR_INVALID_ARG;
+    return (int)bm->lru.size();
 }
 
 int pa_bm_block_table(const pa_bm* bm, int64_t seq_id, int32_t* out, int cap, int* n_out) {

@@ -190,6 +190,80 @@ def test_block_manager_errors_and_batch_tables(capi):
         bm.refcount(8)
 
 
+def test_prefix_cache_matches_model_on_random_operations(capi):
+    """The C++ manager's prefix cache against the model: admissions that reuse
+    cached prefixes, appends, cache registrations, forks, window releases,
+    copies and frees, with eviction under a small pool; tables, refcounts,
+    free and cached counts compared after every operation."""
+    from paged_kv_cache_59_gb300 import BlockManager, PagedKVError
+    rng = random.Random(23)
+    for trial in range(12):
+        nb = rng.randint(6, 60)
+        model, bm = BlockManagerModel(nb, 16), BlockManager(nb, 16)
+        prompts = [[rng.randrange(30) for _ in range(rng.randrange(1, 120))] for _ in range(6)]
+        toks, nxt = {}, 0
+        for _ in range(300):
+            op = rng.random()
+            if op < 0.35:
+                t = list(rng.choice(prompts)) + [rng.randrange(30) for _ in range(rng.randrange(0, 25))]
+                got = model.add_seq_cached(nxt, t)
+                assert bm.add_seq_cached(nxt, t) == got
+                toks[nxt] = t
+                try:
+                    want = model.append_tokens(nxt, len(t) - got)
+                except OutOfBlocks:
+                    with pytest.raises(PagedKVError) as e:
+                        bm.append_tokens(nxt, len(t) - got)
+                    assert e.value.status == -6
+                    model.free_seq(nxt); bm.free_seq(nxt); del toks[nxt]
+                else:
+                    assert bm.append_tokens(nxt, len(t) - got) == want
+                    assert bm.cache_blocks(nxt, t) == model.cache_full_blocks(nxt, t)
+                nxt += 1
+            elif op < 0.5 and toks:
+                s_ = rng.choice(list(toks))
+                extra = [rng.randrange(30) for _ in range(rng.randrange(1, 30))]
+                try:
+                    want = model.append_tokens(s_, len(extra))
+                except OutOfBlocks:
+                    with pytest.raises(PagedKVError):
+                        bm.append_tokens(s_, len(extra))
+                else:
+                    assert bm.append_tokens(s_, len(extra)) == want
+                    toks[s_] = toks[s_] + extra
+                    assert bm.cache_blocks(s_, toks[s_]) == model.cache_full_blocks(s_, toks[s_])
+            elif op < 0.58 and toks:
+                s_ = rng.choice(list(toks))
+                model.fork(s_, nxt); bm.fork(s_, nxt)
+                toks[nxt] = list(toks[s_]); nxt += 1
+            elif op < 0.66 and toks:
+                s_ = rng.choice(list(toks))
+                first = rng.randint(0, model.seq_len(s_))
+                assert bm.release_before(s_, first) == len(model.release_before(s_, first))
+            elif op < 0.74 and toks:
+                s_ = rng.choice(list(toks))
+                if model.block_table(s_):
+                    lb = rng.randrange(len(model.block_table(s_)))
+                    try:
+                        want = model.make_private(s_, lb)
+                    except (OutOfBlocks, BlockManagerError):
+                        with pytest.raises(PagedKVError):
+                            bm.make_private(s_, lb)
+                    else:
+                        assert bm.make_private(s_, lb) == want
+            elif toks:
+                s_ = rng.choice(list(toks))
+                model.free_seq(s_); bm.free_seq(s_); del toks[s_]
+            model.check_invariants()
+            assert bm.num_free() == model.num_free()
+            assert bm.num_cached() == model.num_cached()
+            for s_ in toks:
+                assert bm.block_table(s_) == model.block_table(s_)
+                assert bm.seq_len(s_) == model.seq_len(s_)
+            for b in range(nb):
+                assert bm.refcount(b) == model.refcount(b)
+
+
 def test_prefill_argument_errors_need_no_device(capi):
     p = C.c_void_p(4096)
     args = [p, p, p, p, p, p, p, C.c_float(0.1)]
