@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["tiny_mha", "mha_7b", "gqa_8b", "gqa_70b_cow", "mixed", "gqa_8b_fp8",
-                             "swa_mistral"])
+                             "swa_mistral", "swap_8b"])
     ap.add_argument("--partition-tokens", type=int, default=0,
                     help="decode context partition size (0 = library default)")
     ap.add_argument("--skip-baselines", action="store_true",
@@ -662,10 +662,112 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+SWAP_METRIC = "KV block swap between HBM and page-locked host memory, GB/s (out + in)"
+
+
+def run_swap(args):
+    """Preemption by swapping on the 8B-GQA block shape: each step swaps 4,096
+    blocks (16 sequences x 4,096 tokens; 32 KiB of K and 32 KiB of V each) out
+    to page-locked host memory and back into other blocks. The roofline
+    denominator is a contiguous cudaMemcpyAsync of the same bytes each way,
+    measured in the same run."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_59_gb300 as pk
+    from paged_kv_cache_59_gb300 import build as pk_build
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    pk_build.build()
+    pk.load()
+    dev = torch.device("cuda", local)
+    Hk, D, BS = 8, 128, 16
+    n_move, n_pool = 4096, 8192
+    rng = np.random.default_rng(8)
+    kp = torch.zeros((n_pool, Hk, BS, D), dtype=torch.int16, device=dev)
+    vp = torch.zeros_like(kp)
+    ids_out = torch.from_numpy(rng.permutation(n_pool)[:n_move].astype(np.int32)).to(dev)
+    ids_in = torch.from_numpy(rng.permutation(n_pool)[:n_move].astype(np.int32)).to(dev)
+    hk = torch.empty((n_move, Hk, BS, D), dtype=torch.int16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    block_bytes = Hk * BS * D * 2 * 2          # K + V
+    bytes_each_way = n_move * block_bytes
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs: evs[0].record(stream)
+        pk.pa_swap_out_blocks(kp, vp, ids_out, hk, hv)
+        if evs: evs[1].record(stream)
+        pk.pa_swap_in_blocks(hk, hv, kp, vp, ids_in)
+        if evs: evs[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert pk.pa_get_device_error() == 0
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    sampler = ClockSampler(vis[local] if local < len(vis) else str(local))
+    sampler.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    sampler.mark("begin")
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("end")
+    clocks = sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    out_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    in_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    # the link's contiguous copy rate, same bytes, both directions
+    dk = torch.empty((n_move, Hk, BS, D), dtype=torch.int16, device=dev)
+    dv = torch.empty_like(dk)
+    def memcpy_ms(to_host):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            (hk.copy_(dk, non_blocking=True), hv.copy_(dv, non_blocking=True)) if to_host else \
+                (dk.copy_(hk, non_blocking=True), dv.copy_(hv, non_blocking=True))
+        a.record(stream)
+        for _ in range(10):
+            (hk.copy_(dk, non_blocking=True), hv.copy_(dv, non_blocking=True)) if to_host else \
+                (dk.copy_(hk, non_blocking=True), dv.copy_(hv, non_blocking=True))
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 10
+    m_out, m_in = memcpy_ms(True), memcpy_ms(False)
+    gbs = lambda ms: bytes_each_way / (ms / 1e3) / 1e9
+    value = 2 * bytes_each_way / (total_ms / args.steps / 1e3) / 1e9
+    peak = 2 * bytes_each_way / ((m_out + m_in) / 1e3) / 1e9
+    result = {
+        "metric": SWAP_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: 4,096 of 8,192 pool blocks (random ids) out to host memory and back into "
+                "4,096 other random blocks",
+        "config": {"workload": "swap_8b_4096blocks", "n_kv_heads": Hk, "head_dim": D, "block_size": BS,
+                   "bytes_each_way_per_step": bytes_each_way, "blocks_per_step": n_move,
+                   "step": "pa_swap_out_blocks + pa_swap_in_blocks (one kernel each)"},
+        "swap_out_gbs": round(gbs(out_ms), 1), "swap_in_gbs": round(gbs(in_ms), 1),
+        "roofline": {"bound": "host link", "kernel": "swap_blocks_kernel (out and in)",
+                     "achieved": round(value, 1), "peak": round(peak, 1),
+                     "peak_source": "contiguous cudaMemcpyAsync of the same bytes, pinned host <-> HBM, "
+                                    "measured in this run (out %.1f, in %.1f GB/s)" % (gbs(m_out), gbs(m_in)),
+                     "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None},
+        "gpu_launches": 2 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(result), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "swap_8b":
+        run_swap(args)
     else:
         run_ours(args)
 

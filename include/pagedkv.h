@@ -183,6 +183,36 @@ int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int
                    int n_kv_heads, int head_dim, int block_size, int num_blocks,
                    pa_stream_t stream);
 
+/* ----------------------------------------------------- swap (preemption) */
+
+/*
+ * Whole-block copies between the pools and host memory for preemption by
+ * swapping ([MA] 9.1 "Batching and the scheduler": swapping costs a transfer
+ * and no compute; [DR] "Paged KV: virtual memory for tokens": swap out the
+ * private blocks, reload them anywhere). One launch moves n_blocks blocks,
+ * K and V, every KV head and slot of each, in bits.
+ *  block_ids     int32 [n_blocks] pool block ids, DEVICE memory (e.g. the
+ *                ids pa_bm_swap_out / pa_bm_swap_in returned, copied over);
+ *                an id outside [0, num_blocks) sets PA_DEVERR_BLOCK_ID and
+ *                that block is skipped
+ *  host_k,host_v HOST memory, page-locked (cudaHostAlloc, or registered with
+ *                cudaHostRegister) so that the device reaches it directly;
+ *                16-byte aligned; block i of the transfer occupies bytes
+ *                [i * B, (i + 1) * B), B = n_kv_heads * 16 * head_dim *
+ *                elem_bytes (the pool's block layout)
+ *  elem_bytes    2 for a bf16 pool, 1 for an fp8 pool
+ * pa_swap_out_blocks: host[i] := pool block block_ids[i].
+ * pa_swap_in_blocks:  pool block block_ids[i] := host[i].
+ * Asynchronous on stream: the host copy is complete once the stream is; a
+ * swap-in must be ordered before any kernel that reads those blocks.
+ */
+int pa_swap_out_blocks(const void* k_pool, const void* v_pool, const int32_t* block_ids, int n_blocks,
+                       void* host_k, void* host_v, int n_kv_heads, int head_dim, int block_size,
+                       int elem_bytes, int num_blocks, pa_stream_t stream);
+int pa_swap_in_blocks(const void* host_k, const void* host_v, void* k_pool, void* v_pool,
+                      const int32_t* block_ids, int n_blocks, int n_kv_heads, int head_dim,
+                      int block_size, int elem_bytes, int num_blocks, pa_stream_t stream);
+
 /* ------------------------------------------------------ sliding window */
 
 /*
@@ -342,6 +372,24 @@ int pa_bm_free_seq(pa_bm* bm, int64_t seq_id);
  * PA_ERR_INVALID_ARG. *n_released_out = entries dropped by this call.
  */
 int pa_bm_release_before(pa_bm* bm, int64_t seq_id, int64_t first_pos, int* n_released_out);
+
+/*
+ * Preemption by swapping ([MA] 9.1 "Batching and the scheduler": a preempted
+ * sequence is recomputed or swapped to host memory; [DR] "Paged KV: virtual
+ * memory for tokens": swap out the private blocks, reload them anywhere).
+ * pa_bm_swap_out releases the sequence's private tail - the longest run of
+ * trailing blocks only its table holds - writes those block ids to
+ * blocks_out (logical order; copy their contents out with pa_swap_out_blocks
+ * before anything reuses them) and marks the sequence swapped: it keeps its
+ * length and shared head, and append, copy, fork, release, cache
+ * registration and pa_bm_build_batch on it return PA_ERR_INVALID_ARG until
+ * pa_bm_swap_in allocates that many fresh blocks (all-or-nothing: PA_ERR_OOM
+ * changes nothing), appends them and writes them to blocks_out (copy the
+ * contents back with pa_swap_in_blocks). *n_out = the tail's block count;
+ * PA_ERR_CAPACITY (nothing changed) when cap is smaller.
+ */
+int pa_bm_swap_out(pa_bm* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n_out);
+int pa_bm_swap_in(pa_bm* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n_out);
 
 /*
  * Prefix caching ("Modular LLM Inference Engine from Scratch", section

@@ -56,6 +56,20 @@ Readings taken where the pages are silent or disagree:
     references, until a block is free; an append or a copy succeeds iff the
     free list plus the evictable entries cover it (all-or-nothing);
   - refcount = table references + cache entries.
+* Preemption by swapping ("Modern AI Infrastructure and Agentic System
+  Design", 9.1, part "Batching and the scheduler": a preempted sequence is
+  recomputed later or swapped to host memory; "Inference serving: the
+  KV-cache machine", section "Paged KV: virtual memory for tokens": a block
+  table makes state movable - swap out the private blocks, reload them later
+  anywhere; its Lab B simulator preempts and swaps under this policy).
+  Reading taken: ``swap_out(seq)`` releases the sequence's private tail, the
+  longest run of trailing blocks that only its table holds (refcount 1), and
+  returns them in logical order (the caller copies their contents to host
+  memory before anything reuses them); the table keeps the shared head and
+  the sequence keeps its length. ``swap_in(seq)`` allocates that many fresh
+  blocks (all-or-nothing), appends them to the table and returns them (the
+  caller copies the contents back in). A swapped sequence cannot append,
+  fork, copy or release until it is swapped in.
 """
 from __future__ import annotations
 
@@ -82,6 +96,7 @@ class BlockManagerModel:
         self.lens: Dict[int, int] = {}
         # prefix cache: exact token prefix (tuple) -> block id, oldest first
         self.cache: "OrderedDict[tuple, int]" = OrderedDict()
+        self.swapped: Dict[int, int] = {}   # seq -> blocks held in host memory
 
     # -- allocation primitives ---------------------------------------------
     def _evictable(self) -> int:
@@ -134,10 +149,15 @@ class BlockManagerModel:
             need += (extra + bs - 1) // bs
         return need
 
-    def append_tokens(self, seq_id: int, n: int) -> Tuple[List[int], List[Tuple[int, int]]]:
-        """Append n tokens; returns (slots, cow_pairs)."""
+    def _resident(self, seq_id: int) -> None:
         if seq_id not in self.tables:
             raise BlockManagerError("unknown sequence")
+        if seq_id in self.swapped:
+            raise BlockManagerError("sequence is swapped out")
+
+    def append_tokens(self, seq_id: int, n: int) -> Tuple[List[int], List[Tuple[int, int]]]:
+        """Append n tokens; returns (slots, cow_pairs)."""
+        self._resident(seq_id)
         if n < 0:
             raise BlockManagerError("negative count")
         if self._blocks_needed(seq_id, n) > self.available():
@@ -162,6 +182,7 @@ class BlockManagerModel:
         return slots, cow
 
     def make_private(self, seq_id: int, logical_block: int) -> List[Tuple[int, int]]:
+        self._resident(seq_id)
         tab = self.tables[seq_id]
         b = tab[logical_block]
         if b < 0:
@@ -178,6 +199,8 @@ class BlockManagerModel:
     def fork(self, parent: int, child: int) -> None:
         if parent not in self.tables:
             raise BlockManagerError("unknown parent")
+        if parent in self.swapped:
+            raise BlockManagerError("parent is swapped out")
         if child in self.tables:
             raise BlockManagerError("child exists")
         self.tables[child] = list(self.tables[parent])
@@ -193,12 +216,39 @@ class BlockManagerModel:
             if b >= 0:
                 self._put(b)
         del self.lens[seq_id]
+        self.swapped.pop(seq_id, None)
+
+    def swap_out(self, seq_id: int) -> List[int]:
+        """Releases the private tail of the table; returns its blocks."""
+        self._resident(seq_id)
+        tab = self.tables[seq_id]
+        k = len(tab)
+        while k > 0 and tab[k - 1] >= 0 and self.ref[tab[k - 1]] == 1:
+            k -= 1
+        out = tab[k:]
+        for b in out:
+            self._put(b)
+        del tab[k:]
+        self.swapped[seq_id] = len(out)
+        return out
+
+    def swap_in(self, seq_id: int) -> List[int]:
+        """Re-allocates the swapped-out tail (all-or-nothing); returns the
+        new blocks in logical order."""
+        if seq_id not in self.swapped:
+            raise BlockManagerError("sequence is not swapped out")
+        n = self.swapped[seq_id]
+        if n > self.available():
+            raise OutOfBlocks()
+        new = [self._alloc() for _ in range(n)]
+        self.tables[seq_id].extend(new)
+        del self.swapped[seq_id]
+        return new
 
     def release_before(self, seq_id: int, first_pos: int) -> List[int]:
         """Drops the blocks wholly before logical position first_pos; returns
         the dropped table entries (block ids), in logical order."""
-        if seq_id not in self.tables:
-            raise BlockManagerError("unknown sequence")
+        self._resident(seq_id)
         tab = self.tables[seq_id]
         bs = self.block_size
         first_pos = min(max(int(first_pos), 0), self.lens[seq_id])
@@ -215,8 +265,7 @@ class BlockManagerModel:
         """Registers the sequence's full blocks under their token prefixes;
         returns how many entries were added. ``tokens`` are the sequence's
         token ids from position 0 (at least as many as its full blocks)."""
-        if seq_id not in self.tables:
-            raise BlockManagerError("unknown sequence")
+        self._resident(seq_id)
         bs = self.block_size
         tab = self.tables[seq_id]
         n_full = min(self.lens[seq_id], len(tokens)) // bs
@@ -286,4 +335,4 @@ class BlockManagerModel:
             assert (r == 0) == (b in free), (b, r)
         bs = self.block_size
         for s, t in self.tables.items():
-            assert len(t) == (self.lens[s] + bs - 1) // bs
+            assert len(t) + self.swapped.get(s, 0) == (self.lens[s] + bs - 1) // bs

@@ -15,8 +15,15 @@
   diverging block gets copied). The copy moves every KV head and every slot
   of the block, for K and for V.
 
-Both are bit copies; the oracle works on the raw bf16 bit patterns and
-returns new arrays (the inputs are not modified).
+* swap_out / swap_in: preemption by swapping moves a sequence's private
+  blocks to host memory and later back into any free blocks ("Modern AI
+  Infrastructure and Agentic System Design", 9.1, part "Batching and the
+  scheduler"; "Inference serving: the KV-cache machine", section "Paged KV:
+  virtual memory for tokens"). The host copy holds the blocks in the order
+  given, each with the pool's block layout.
+
+All are bit copies; the oracle works on the raw bit patterns and returns new
+arrays (the inputs are not modified).
 """
 from __future__ import annotations
 
@@ -56,4 +63,21 @@ def copy_blocks(k_pool, v_pool, block_mapping):
     for src, dst in np.asarray(block_mapping).reshape(-1, 2):
         kp[int(dst)] = kp[int(src)]
         vp[int(dst)] = vp[int(src)]
+    return kp, vp
+
+
+def swap_out(k_pool, v_pool, block_ids):
+    """Host copies [n][n_kv_heads][bs][D] of pool blocks block_ids, in order."""
+    ids = [int(b) for b in np.asarray(block_ids)]
+    return (np.array([np.asarray(k_pool)[b] for b in ids]).reshape((len(ids),) + np.asarray(k_pool).shape[1:]),
+            np.array([np.asarray(v_pool)[b] for b in ids]).reshape((len(ids),) + np.asarray(v_pool).shape[1:]))
+
+
+def swap_in(host_k, host_v, k_pool, v_pool, block_ids):
+    """Pool block block_ids[i] := host block i (new arrays returned)."""
+    kp = np.array(k_pool, copy=True)
+    vp = np.array(v_pool, copy=True)
+    for i, b in enumerate(np.asarray(block_ids)):
+        kp[int(b)] = host_k[i]
+        vp[int(b)] = host_v[i]
     return kp, vp

@@ -22,7 +22,7 @@ from ._capi import PagedKVError, check, load  # noqa: F401
 __all__ = [
     "pa_decode", "pa_decode_workspace_bytes", "decode_workspace", "pa_decode_noalloc", "pa_reshape_and_cache",
     "pa_copy_blocks", "pa_prefill_paged", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_window",
-    "pa_get_device_error",
+    "pa_swap_out_blocks", "pa_swap_in_blocks", "pa_get_device_error",
     "BlockManager", "load", "PagedKVError",
 ]
 
@@ -167,6 +167,49 @@ def pa_decode_window(out, q, k_pool, v_pool, block_tables, context_lens, scale: 
     check("pa_decode_window", st)
 
 
+def _host_pinned(t, what: str):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch.Tensor")
+    if t.device.type != "cpu" or not t.is_pinned():
+        raise ValueError(f"{what} must be page-locked host memory (pin_memory=True)")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _swap_args(k_pool, host_k, host_v, block_ids):
+    torch = _torch()
+    num_blocks, n_kv_heads, block_size, head_dim = k_pool.shape
+    eb = k_pool.element_size()
+    n = block_ids.numel()
+    need = n * n_kv_heads * block_size * head_dim * eb
+    for h, name in ((host_k, "host_k"), (host_v, "host_v")):
+        if h.numel() * h.element_size() < need:
+            raise ValueError(f"{name} holds fewer than {need} bytes")
+    return (n, n_kv_heads, head_dim, block_size, eb, num_blocks,
+            _ptr(block_ids, "block_ids", dtype=torch.int32) if n else C.c_void_p(None))
+
+
+def pa_swap_out_blocks(k_pool, v_pool, block_ids, host_k, host_v, stream=None) -> None:
+    """host_k[i], host_v[i] := pool block block_ids[i] (K and V, all heads);
+    host buffers page-locked, block_ids int32 on the device."""
+    n, hk, d, bs, eb, nb, ids = _swap_args(k_pool, host_k, host_v, block_ids)
+    st = load().pa_swap_out_blocks(_ptr(k_pool, "k_pool"), _ptr(v_pool, "v_pool"), ids, n,
+                                   _host_pinned(host_k, "host_k"), _host_pinned(host_v, "host_v"), hk, d, bs,
+                                   eb, nb, _stream(stream))
+    check("pa_swap_out_blocks", st)
+
+
+def pa_swap_in_blocks(host_k, host_v, k_pool, v_pool, block_ids, stream=None) -> None:
+    """pool block block_ids[i] := host_k[i], host_v[i]."""
+    n, hk, d, bs, eb, nb, ids = _swap_args(k_pool, host_k, host_v, block_ids)
+    st = load().pa_swap_in_blocks(_host_pinned(host_k, "host_k"), _host_pinned(host_v, "host_v"),
+                                  _ptr(k_pool, "k_pool"), _ptr(v_pool, "v_pool"), ids, n, hk, d, bs, eb, nb,
+                                  _stream(stream))
+    check("pa_swap_in_blocks", st)
+
+
 def pa_reshape_and_cache_fp8(k, v, k_pool, v_pool, slot_mapping, k_scale, v_scale, stream=None) -> None:
     """Encodes k[t], v[t] (bf16 [n_tokens][n_kv_heads][head_dim]) as E4M3 codes
     of x / scale[head] into the uint8 pools at slot_mapping[t]."""
@@ -292,6 +335,27 @@ class BlockManager:
 
     def free_seq(self, seq_id: int) -> None:
         check("pa_bm_free_seq", self._lib.pa_bm_free_seq(self._h, seq_id))
+
+    def _swap(self, fn: str, seq_id: int) -> List[int]:
+        n = C.c_int(0)
+        st = getattr(self._lib, fn)(self._h, seq_id, None, 0, C.byref(n))
+        if st == _capi.PA_OK:
+            return []
+        if st != _capi.PA_ERR_CAPACITY:
+            check(fn, st)
+        buf = (C.c_int32 * n.value)()
+        check(fn, getattr(self._lib, fn)(self._h, seq_id, buf, n.value, C.byref(n)))
+        return list(buf)[:n.value]
+
+    def swap_out(self, seq_id: int) -> List[int]:
+        """Releases the sequence's private tail; returns its block ids (copy
+        their contents to host memory before anything reuses them)."""
+        return self._swap("pa_bm_swap_out", seq_id)
+
+    def swap_in(self, seq_id: int) -> List[int]:
+        """Re-allocates a swapped sequence's tail; returns the new block ids
+        (copy the contents back into them)."""
+        return self._swap("pa_bm_swap_in", seq_id)
 
     def cache_blocks(self, seq_id: int, tokens: Sequence[int]) -> int:
         """Registers the sequence's full blocks in the prefix cache; returns

@@ -47,6 +47,8 @@ SIGNATURES = {
     "pa_copy_blocks": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     "pa_decode_window": (i32, [vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32, i32,
                                i32, i32, vp, C.c_size_t, vp]),
+    "pa_swap_out_blocks": (i32, [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp]),
+    "pa_swap_in_blocks": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
     "pa_reshape_and_cache_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     "pa_decode_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32,
                             i32, i32, vp, C.c_size_t, vp]),
@@ -63,6 +65,8 @@ SIGNATURES = {
     "pa_bm_fork": (i32, [vp, i64, i64]),
     "pa_bm_free_seq": (i32, [vp, i64]),
     "pa_bm_release_before": (i32, [vp, i64, i64, C.POINTER(C.c_int)]),
+    "pa_bm_swap_out": (i32, [vp, i64, p_i32, i32, C.POINTER(C.c_int)]),
+    "pa_bm_swap_in": (i32, [vp, i64, p_i32, i32, C.POINTER(C.c_int)]),
     "pa_bm_cache_blocks": (i32, [vp, i64, p_i32, i64, C.POINTER(C.c_int)]),
     "pa_bm_add_seq_cached": (i32, [vp, i64, p_i32, i64, p_i64]),
     "pa_bm_num_cached": (i32, [vp]),

@@ -16,6 +16,12 @@
 //    Attention": with a window the cache a sequence needs stays O(W); blocks
 //    wholly before the window are released (table entry -1, a hole) and
 //    return to the free list when no table references them.
+//  - "Modern AI Infrastructure and Agentic System Design", 9.1, part
+//    "Batching and the scheduler", and "Inference serving: the KV-cache
+//    machine", section "Paged KV: virtual memory for tokens" (and its Lab B
+//    simulator): a preempted sequence's private blocks are swapped to host
+//    memory and reloaded later into any free blocks. The private tail is the
+//    longest run of trailing blocks only this table holds.
 //  - "Modular LLM Inference Engine from Scratch", section "Prefix caching -
 //    skip recomputing the same prompt": a hash-based LRU cache of prompt
 //    prefixes; lookup returns the longest cached prefix of whole blocks and
@@ -74,6 +80,7 @@ struct pa_bm {
     struct Seq {
         std::vector<int32_t> table;
         int64_t len = 0;
+        int64_t swapped = -1;  // >= 0: that many trailing blocks are in host memory
     };
     std::unordered_map<int64_t, Seq> seqs;
     struct Entry {
@@ -150,6 +157,7 @@ int pa_bm_append_tokens(pa_bm* bm, int64_t seq_id, int n, int64_t* slots_out,
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PA_ERR_REFCOUNT;
     pa_bm::Seq& s = it->second;
+    if (s.swapped >= 0) return PA_ERR_INVALID_ARG;  // swapped out
     const int64_t bs = bm->block_size;
     if (n_cow_out) *n_cow_out = 0;
     // blocks this append needs: a copy of a shared, partially filled tail
@@ -187,6 +195,7 @@ int pa_bm_make_private(pa_bm* bm, int64_t seq_id, int logical_block, int64_t* pa
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PA_ERR_REFCOUNT;
     pa_bm::Seq& s = it->second;
+    if (s.swapped >= 0) return PA_ERR_INVALID_ARG;
     if (logical_block < 0 || logical_block >= (int)s.table.size()) return PA_ERR_INVALID_ARG;
     *n_out = 0;
     int32_t b = s.table[logical_block];
@@ -206,6 +215,7 @@ int pa_bm_fork(pa_bm* bm, int64_t parent, int64_t child) {
     if (!bm) return PA_ERR_INVALID_ARG;
     auto it = bm->seqs.find(parent);
     if (it == bm->seqs.end() || bm->seqs.count(child)) return PA_ERR_REFCOUNT;
+    if (it->second.swapped >= 0) return PA_ERR_INVALID_ARG;
     pa_bm::Seq c = it->second;  // copy before emplace may rehash
     for (int32_t b : c.table)
         if (b >= 0) bm->inc(b);
@@ -231,6 +241,7 @@ int pa_bm_release_before(pa_bm* bm, int64_t seq_id, int64_t first_pos, int* n_re
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PA_ERR_REFCOUNT;
     pa_bm::Seq& s = it->second;
+    if (s.swapped >= 0) return PA_ERR_INVALID_ARG;
     if (first_pos < 0) first_pos = 0;
     if (first_pos > s.len) first_pos = s.len;
     const int64_t whole = first_pos / bm->block_size;  // blocks wholly before first_pos
@@ -246,12 +257,52 @@ int pa_bm_release_before(pa_bm* bm, int64_t seq_id, int64_t first_pos, int* n_re
     return PA_OK;
 }
 
+int pa_bm_swap_out(pa_bm* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n_out) {
+    if (!bm || !n_out || cap < 0 || (cap > 0 && !blocks_out)) return PA_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PA_ERR_REFCOUNT;
+    pa_bm::Seq& s = it->second;
+    if (s.swapped >= 0) return PA_ERR_INVALID_ARG;
+    size_t k = s.table.size();
+    while (k > 0 && s.table[k - 1] >= 0 && bm->ref[s.table[k - 1]] == 1) --k;
+    const int n = (int)(s.table.size() - k);
+    *n_out = n;
+    if (n > cap) return PA_ERR_CAPACITY;  // nothing changed
+    for (int i = 0; i < n; ++i) {
+        blocks_out[i] = s.table[k + i];
+        bm->put(s.table[k + i]);
+    }
+    s.table.resize(k);
+    s.swapped = n;
+    return PA_OK;
+}
+
+int pa_bm_swap_in(pa_bm* bm, int64_t seq_id, int32_t* blocks_out, int cap, int* n_out) {
+    if (!bm || !n_out || cap < 0 || (cap > 0 && !blocks_out)) return PA_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PA_ERR_REFCOUNT;
+    pa_bm::Seq& s = it->second;
+    if (s.swapped < 0) return PA_ERR_INVALID_ARG;  // not swapped out
+    const int n = (int)s.swapped;
+    *n_out = n;
+    if (n > cap) return PA_ERR_CAPACITY;
+    if (n > bm->available()) return PA_ERR_OOM;
+    for (int i = 0; i < n; ++i) {
+        const int32_t b = bm->alloc();
+        s.table.push_back(b);
+        blocks_out[i] = b;
+    }
+    s.swapped = -1;
+    return PA_OK;
+}
+
 int pa_bm_cache_blocks(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int64_t n_tokens,
                        int* n_added_out) {
     if (!bm || !n_added_out || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID_ARG;
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PA_ERR_REFCOUNT;
     const pa_bm::Seq& s = it->second;
+    if (s.swapped >= 0) return PA_ERR_INVALID_ARG;
     const int64_t bs = bm->block_size;
     const int64_t n_full = (n_tokens < s.len ? n_tokens : s.len) / bs;
     int added = 0;
@@ -339,6 +390,7 @@ int pa_bm_build_batch(const pa_bm* bm, const int64_t* seq_ids, int n, int max_bl
     for (int i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seq_ids[i]);
         if (it == bm->seqs.end()) return PA_ERR_REFCOUNT;
+        if (it->second.swapped >= 0) return PA_ERR_INVALID_ARG;
         if ((int)it->second.table.size() > max_blocks) return PA_ERR_CAPACITY;
     }
     for (int i = 0; i < n; ++i) {

@@ -1,6 +1,10 @@
 // Cache upkeep kernels: new-token scatter (reshape_and_cache, and its fp8
-// variant that encodes while it scatters) and the copy-on-write block copy
-// (copy_blocks). All are bound by HBM bandwidth.
+// variant that encodes while it scatters), the copy-on-write block copy
+// (copy_blocks), and the swap of whole blocks to and from page-locked host
+// memory for preemption ("Modern AI Infrastructure and Agentic System Design",
+// 9.1 "Batching and the scheduler"; "Inference serving: the KV-cache machine",
+// section "Paged KV: virtual memory for tokens"). The first three are bound
+// by HBM bandwidth, the swap by the host link.
 //
 // reshape_and_cache: each decode step appends the new token's K and V to the
 // cache ("KV Cache Explained Like You're an LLM Engineer", section "What KV
@@ -123,7 +127,77 @@ copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
     }
 }
 
+// Swap of whole blocks between the pool and page-locked host memory.
+// grid.x = block index i, grid.y = slice; each CTA moves its slice of block
+// ids[i]'s K and V (all KV heads, all 16 slots) in 16-byte vectors. out == true:
+// pool -> host (host_k[i] is block i of the host copy); else host -> pool.
+__global__ void __launch_bounds__(256)
+swap_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, uint4* __restrict__ host_k,
+                   uint4* __restrict__ host_v, const int32_t* __restrict__ ids, long long chunks_per_block,
+                   int num_blocks, bool out, unsigned int* err) {
+    pa::grid_dependency_wait();
+    const int i = blockIdx.x;
+    const int32_t b = ids[i];
+    if (b < 0 || b >= num_blocks) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) pa::set_error(err, PA_DEVERR_BLOCK_ID);
+        return;
+    }
+    const long long p0 = (long long)b * chunks_per_block, h0 = (long long)i * chunks_per_block;
+    for (long long c = (long long)blockIdx.y * blockDim.x + threadIdx.x; c < chunks_per_block;
+         c += (long long)gridDim.y * blockDim.x) {
+        if (out) {
+            host_k[h0 + c] = k_pool[p0 + c];
+            host_v[h0 + c] = v_pool[p0 + c];
+        } else {
+            k_pool[p0 + c] = host_k[h0 + c];
+            v_pool[p0 + c] = host_v[h0 + c];
+        }
+    }
+}
+
 }  // namespace
+
+namespace {
+int swap_blocks(void* k_pool, void* v_pool, void* host_k, void* host_v, const int32_t* block_ids, int n_blocks,
+                int n_kv_heads, int head_dim, int block_size, int elem_bytes, int num_blocks, bool out,
+                pa_stream_t stream) {
+    if (n_blocks < 0 || n_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (block_size != kBS) return PA_ERR_UNSUPPORTED;
+    if (elem_bytes != 1 && elem_bytes != 2) return PA_ERR_UNSUPPORTED;
+    const long long block_bytes = (long long)n_kv_heads * kBS * head_dim * elem_bytes;
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (n_blocks == 0) return PA_OK;
+    if (!k_pool || !v_pool || !host_k || !host_v || !block_ids) return PA_ERR_INVALID_ARG;
+    if (!pa_aligned16(k_pool) || !pa_aligned16(v_pool) || !pa_aligned16(host_k) || !pa_aligned16(host_v) ||
+        (reinterpret_cast<uintptr_t>(block_ids) & 3u))
+        return PA_ERR_INVALID_ARG;
+    if (n_blocks > 0x7fffffff) return PA_ERR_UNSUPPORTED;
+    unsigned int* err = pa_device_error_ptr();
+    if (!err) return PA_ERR_CUDA;
+    const long long chunks = block_bytes / 16;
+    const int threads = 256;
+    int slices = (int)((chunks + threads - 1) / threads);
+    if (slices > 64) slices = 64;
+    return pa_launch_pdl(swap_blocks_kernel, dim3((unsigned)n_blocks, slices), dim3(threads), 0,
+                         reinterpret_cast<cudaStream_t>(stream), static_cast<uint4*>(k_pool),
+                         static_cast<uint4*>(v_pool), static_cast<uint4*>(host_k), static_cast<uint4*>(host_v),
+                         block_ids, chunks, num_blocks, out, err);
+}
+}  // namespace
+
+extern "C" int pa_swap_out_blocks(const void* k_pool, const void* v_pool, const int32_t* block_ids, int n_blocks,
+                                  void* host_k, void* host_v, int n_kv_heads, int head_dim, int block_size,
+                                  int elem_bytes, int num_blocks, pa_stream_t stream) {
+    return swap_blocks(const_cast<void*>(k_pool), const_cast<void*>(v_pool), host_k, host_v, block_ids, n_blocks,
+                       n_kv_heads, head_dim, block_size, elem_bytes, num_blocks, true, stream);
+}
+
+extern "C" int pa_swap_in_blocks(const void* host_k, const void* host_v, void* k_pool, void* v_pool,
+                                 const int32_t* block_ids, int n_blocks, int n_kv_heads, int head_dim,
+                                 int block_size, int elem_bytes, int num_blocks, pa_stream_t stream) {
+    return swap_blocks(k_pool, v_pool, const_cast<void*>(host_k), const_cast<void*>(host_v), block_ids, n_blocks,
+                       n_kv_heads, head_dim, block_size, elem_bytes, num_blocks, false, stream);
+}
 
 extern "C" int pa_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
                                     const int64_t* slot_mapping, int n_tokens, int n_kv_heads,

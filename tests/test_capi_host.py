@@ -222,6 +222,11 @@ def test_prefix_cache_matches_model_on_random_operations(capi):
                 nxt += 1
             elif op < 0.5 and toks:
                 s_ = rng.choice(list(toks))
+                if s_ in model.swapped:
+                    with pytest.raises(PagedKVError) as e:
+                        bm.append_tokens(s_, 1)
+                    assert e.value.status == -1
+                    continue
                 extra = [rng.randrange(30) for _ in range(rng.randrange(1, 30))]
                 try:
                     want = model.append_tokens(s_, len(extra))
@@ -234,14 +239,20 @@ def test_prefix_cache_matches_model_on_random_operations(capi):
                     assert bm.cache_blocks(s_, toks[s_]) == model.cache_full_blocks(s_, toks[s_])
             elif op < 0.58 and toks:
                 s_ = rng.choice(list(toks))
+                if s_ in model.swapped:
+                    continue
                 model.fork(s_, nxt); bm.fork(s_, nxt)
                 toks[nxt] = list(toks[s_]); nxt += 1
             elif op < 0.66 and toks:
                 s_ = rng.choice(list(toks))
+                if s_ in model.swapped:
+                    continue
                 first = rng.randint(0, model.seq_len(s_))
                 assert bm.release_before(s_, first) == len(model.release_before(s_, first))
             elif op < 0.74 and toks:
                 s_ = rng.choice(list(toks))
+                if s_ in model.swapped:
+                    continue
                 if model.block_table(s_):
                     lb = rng.randrange(len(model.block_table(s_)))
                     try:
@@ -251,6 +262,19 @@ def test_prefix_cache_matches_model_on_random_operations(capi):
                             bm.make_private(s_, lb)
                     else:
                         assert bm.make_private(s_, lb) == want
+            elif op < 0.84 and toks:
+                s_ = rng.choice(list(toks))
+                if s_ in model.swapped:
+                    try:
+                        want = model.swap_in(s_)
+                    except OutOfBlocks:
+                        with pytest.raises(PagedKVError) as e:
+                            bm.swap_in(s_)
+                        assert e.value.status == -6
+                    else:
+                        assert len(bm.swap_in(s_)) == len(want)
+                else:
+                    assert len(bm.swap_out(s_)) == len(model.swap_out(s_))
             elif toks:
                 s_ = rng.choice(list(toks))
                 model.free_seq(s_); bm.free_seq(s_); del toks[s_]

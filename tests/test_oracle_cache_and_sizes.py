@@ -164,3 +164,26 @@ def test_cow_copy_leaves_sibling_attention_unchanged():
     after = paged_decode(wl.q, kp2, vp2, tabs, wl.dec_ctx, wl.scale)
     assert np.array_equal(after[0], before[0])     # sibling unchanged
     assert not np.array_equal(after[1], before[1])  # the diverged sequence changed
+
+
+def test_swap_round_trip_moves_blocks_to_new_places():
+    from oracle.cache_ops import swap_in, swap_out
+    from workloads import make_decode_case
+    wl = make_decode_case(91, [40, 70], 8, 2, 64, num_blocks=40, n_new=0)
+    ids = list(wl.dec_tables[1, :5])
+    hk, hv = swap_out(wl.k_pool, wl.v_pool, ids)
+    for i, b in enumerate(ids):
+        assert np.array_equal(hk[i], wl.k_pool[b]) and np.array_equal(hv[i], wl.v_pool[b])
+    free = [b for b in range(wl.num_blocks) if b not in set(wl.dec_tables.ravel())][:5]
+    kp, vp = swap_in(hk, hv, wl.k_pool, wl.v_pool, free)
+    for i, b in enumerate(free):
+        assert np.array_equal(kp[b], wl.k_pool[ids[i]]) and np.array_equal(vp[b], wl.v_pool[ids[i]])
+    untouched = [b for b in range(wl.num_blocks) if b not in set(free)]
+    assert np.array_equal(kp[untouched], wl.k_pool[untouched])
+    # decode over the moved blocks equals decode over the originals (paging is addressing only)
+    from oracle.attention import paged_decode
+    t2 = wl.dec_tables.copy()
+    t2[1, :5] = free
+    a = paged_decode(wl.q, wl.k_pool, wl.v_pool, wl.dec_tables, wl.dec_ctx, wl.scale)
+    b = paged_decode(wl.q, kp, vp, t2, wl.dec_ctx, wl.scale)
+    assert np.array_equal(a, b)
