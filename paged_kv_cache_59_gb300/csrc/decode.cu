@@ -638,7 +638,12 @@ int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void
                     (reinterpret_cast<uintptr_t>(v_scale) & 3u)))
         return PA_ERR_INVALID_ARG;
     if (out == q) return PA_ERR_INVALID_ARG;
-    const int max_parts = max_context_len > 0 ? (max_context_len + pt - 1) / pt : 1;
+    int max_parts = max_context_len > 0 ? (max_context_len + pt - 1) / pt : 1;
+    if (window >= 0) {  // W + 1 positions touch at most ceil((W + 16) / 16) blocks
+        const int wblocks = (window + 2 * kBS - 1) / kBS;
+        const int wparts = (wblocks + pt / kBS - 1) / (pt / kBS);
+        if (wparts < max_parts) max_parts = wparts;
+    }
     const size_t need = workspace_bytes_for(n_seqs, n_heads, head_dim, max_parts);
     if (need > 0 && (!workspace || workspace_bytes < need || !pa_aligned16(workspace)))
         return PA_ERR_WORKSPACE;
