@@ -111,15 +111,17 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+def profiled_traffic(workload: str = None):
+    """DRAM bytes per launch of the partition kernel from the committed ncu
+    summary (the default workload's line, or the line tagged with the
+    workload), if it was taken on the current kernel source (else None)."""
     if not os.path.exists(PROFILE_SUMMARY):
         return None
+    tag = "bench_traffic:" if workload in (None, DEFAULT_WORKLOAD) else f"bench_traffic[{workload}]:"
     vals = {}
     with open(PROFILE_SUMMARY) as f:
         for line in f:
-            if line.startswith("bench_traffic:"):
+            if line.startswith(tag):
                 for kv in line.split(":", 1)[1].split():
                     k, _, v = kv.partition("=")
                     vals[k] = v
@@ -357,7 +359,7 @@ def run_ours(args):
     dec_avg = sum(dec_ms) / len(dec_ms)
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / (dec_avg / 1e3) / 1e9
-    traffic = profiled_traffic() if args.workload == DEFAULT_WORKLOAD and pt == 0 else None
+    traffic = profiled_traffic(args.workload) if pt == 0 else None
 
     result = {
         "metric": METRIC,
