@@ -269,6 +269,8 @@ def run_ours(args):
         q_pf, pf_tabs, pf_ctx, qsl = to_dev(wl.q_pf), to_dev(wl.pf_tables), to_dev(wl.pf_ctx), to_dev(wl.q_start_loc)
         out_pf = torch.empty_like(q_pf)
         max_chunk = int(np.max(np.diff(wl.q_start_loc)))
+        # key ranges split into pieces so the grid fills whole waves of SMs
+        ws_pf = pk.prefill_workspace(q_pf, len(wl.pf_ctx), Hk, max_chunk, 0)
     pt = args.partition_tokens
     ws = pk.decode_workspace(q, max_ctx, pt)
     stream = torch.cuda.current_stream()
@@ -292,7 +294,8 @@ def run_ours(args):
         else:
             pk.pa_decode(out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws, partition_tokens=pt)
     launches_per_step = ((1 if n_dec_new else 0) + (1 if has_pf else 0) + 1
-                         + (1 if pk.pa_decode_workspace_bytes(B, H, D, max_ctx, pt) else 0))
+                         + (1 if pk.pa_decode_workspace_bytes(B, H, D, max_ctx, pt) else 0)
+                         + (1 if has_pf and ws_pf is not None else 0))
 
     def step(ev_pair=None, pf_pair=None):
         if n_dec_new:
@@ -300,7 +303,8 @@ def run_ours(args):
         if has_pf:
             if pf_pair is not None:
                 pf_pair[0].record(stream)
-            pk.pa_prefill_paged(out_pf, q_pf, kp, vp, pf_tabs, pf_ctx, qsl, wl.scale, max_chunk)
+            pk.pa_prefill_paged_ex(out_pf, q_pf, kp, vp, pf_tabs, pf_ctx, qsl, wl.scale, max_chunk,
+                                   splits=0, workspace=ws_pf)
             if pf_pair is not None:
                 pf_pair[1].record(stream)
         if ev_pair is not None:
@@ -422,8 +426,10 @@ def run_ours(args):
         result["config"]["step"] = ("pa_reshape_and_cache (decode tokens + chunk tokens) + "
                                     "pa_prefill_paged (tcgen05) + pa_decode")
         result["config"]["prefill_flop_per_step"] = pf_flops
+        result["config"]["prefill_splits"] = ("auto: %d bytes of partials" % ws_pf.numel()
+                                              if ws_pf is not None else 1)
         result["prefill_roofline"] = {
-            "bound": "tensor", "kernel": "pa_prefill_tc_kernel",
+            "bound": "tensor", "kernel": "pa_prefill_tc_kernel (+ pa_prefill_merge_kernel when split)",
             "achieved": round(pf_flops / (pf_avg / 1e3) / 1e12, 1), "peak": tpk,
             "peak_source": tpk_kind, "unit": "TFLOP/s",
             "frac": round(pf_flops / (pf_avg / 1e3) / 1e12 / tpk, 4),
@@ -480,6 +486,7 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
     max_ctx = int(wl.dec_ctx.max())
     max_chunk = int(np.max(np.diff(wl.q_start_loc))) if has_pf else 0
     ws = pk.decode_workspace(d_in[0], max_ctx, args.partition_tokens)
+    ws_pf = pk.prefill_workspace(d_in[6], len(wl.pf_ctx), wl.n_kv_heads, max_chunk, 0) if has_pf else None
     h2d = int(h_buf.numel())
     d2h = int(h_out.numel())
 
@@ -493,7 +500,8 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
                 pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
         if has_pf:
             q_pf, pf_tabs, pf_ctx, qsl = d_in[6:]
-            pk.pa_prefill_paged(d_out[1], q_pf, kp, vp, pf_tabs, pf_ctx, qsl, wl.scale, max_chunk)
+            pk.pa_prefill_paged_ex(d_out[1], q_pf, kp, vp, pf_tabs, pf_ctx, qsl, wl.scale, max_chunk,
+                                   splits=0, workspace=ws_pf)
         if fp8_scales is not None:
             pk.pa_decode_fp8(d_out[0], q, kp, vp, *fp8_scales, tabs, ctx, wl.scale, max_ctx, workspace=ws,
                              partition_tokens=args.partition_tokens)

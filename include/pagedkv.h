@@ -303,6 +303,30 @@ int pa_prefill_paged(void* out, const void* q, const void* k_pool, const void* v
                      int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
                      int max_chunk_len, int num_blocks, pa_stream_t stream);
 
+/*
+ * pa_prefill_paged with the key range of each query-tile pair optionally
+ * split into pieces, so that the grid fills whole waves of the GPU's SMs
+ * (one prefill CTA runs per SM). Each piece keeps its un-normalised output,
+ * reference maximum and sum in the workspace; a merge kernel combines the
+ * pieces (O = sum_p O_p 2^(m_p - M), l = sum_p l_p 2^(m_p - M), out = O / l).
+ *  splits     pieces per pair: 0 = chosen from the grid size and the
+ *             device's SM count, 1 = no split (no workspace needed), 2..64
+ *  workspace  DEVICE memory, 16-byte aligned, of at least
+ *             pa_prefill_workspace_bytes(n_seqs, n_heads, n_kv_heads,
+ *             max_chunk_len, splits) bytes (query it with the same
+ *             arguments and the same current device); PA_ERR_WORKSPACE if
+ *             missing or too small. Contents need no initialisation.
+ * Returns 0 from pa_prefill_workspace_bytes for arguments
+ * pa_prefill_paged_ex would reject, and for splits = 1.
+ */
+size_t pa_prefill_workspace_bytes(int n_seqs, int n_heads, int n_kv_heads, int max_chunk_len, int splits);
+int pa_prefill_paged_ex(void* out, const void* q, const void* k_pool, const void* v_pool,
+                        const int32_t* block_tables, const int32_t* context_lens,
+                        const int32_t* q_start_loc, float scale, int n_heads, int n_kv_heads,
+                        int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
+                        int max_chunk_len, int num_blocks, int splits, void* workspace,
+                        size_t workspace_bytes, pa_stream_t stream);
+
 /* ----------------------------------------------------------- diagnostics */
 
 /* Reads the current device's error word into *flags_out (a PA_DEVERR_* mask)

@@ -21,7 +21,8 @@ from ._capi import PagedKVError, check, load  # noqa: F401
 
 __all__ = [
     "pa_decode", "pa_decode_workspace_bytes", "decode_workspace", "pa_decode_noalloc", "pa_reshape_and_cache",
-    "pa_copy_blocks", "pa_prefill_paged", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_window",
+    "pa_copy_blocks", "pa_prefill_paged", "pa_prefill_paged_ex", "pa_prefill_workspace_bytes",
+    "prefill_workspace", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_window",
     "pa_swap_out_blocks", "pa_swap_in_blocks", "pa_get_device_error",
     "BlockManager", "load", "PagedKVError",
 ]
@@ -284,6 +285,42 @@ def pa_prefill_paged(out, q, k_pool, v_pool, block_tables, context_lens, q_start
         head_dim, block_size, n_seqs, block_tables.shape[1], int(max_chunk_len), num_blocks,
         _stream(stream))
     check("pa_prefill_paged", st)
+
+
+def pa_prefill_workspace_bytes(n_seqs: int, n_heads: int, n_kv_heads: int, max_chunk_len: int,
+                               splits: int = 0) -> int:
+    return int(load().pa_prefill_workspace_bytes(n_seqs, n_heads, n_kv_heads, max_chunk_len, splits))
+
+
+def prefill_workspace(q, n_seqs: int, n_kv_heads: int, max_chunk_len: int, splits: int = 0):
+    """A workspace tensor for pa_prefill_paged_ex (None when no split is needed)."""
+    torch = _torch()
+    nbytes = pa_prefill_workspace_bytes(n_seqs, q.shape[1], n_kv_heads, max_chunk_len, splits)
+    return torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
+
+
+def pa_prefill_paged_ex(out, q, k_pool, v_pool, block_tables, context_lens, q_start_loc, scale: float,
+                        max_chunk_len: int, splits: int = 0, workspace=None, stream=None) -> None:
+    """pa_prefill_paged with each query-tile pair's key range split into pieces
+    (splits = 0: chosen from the grid and the SM count) merged afterwards."""
+    torch = _torch()
+    n_rows, n_heads, head_dim = q.shape
+    num_blocks, n_kv_heads, block_size, hd2 = k_pool.shape
+    n_seqs = context_lens.numel()
+    if hd2 != head_dim or tuple(out.shape) != tuple(q.shape) or q_start_loc.numel() != n_seqs + 1:
+        raise ValueError("shape mismatch in pa_prefill_paged_ex arguments")
+    ws_ptr, ws_bytes = C.c_void_p(None), 0
+    if workspace is not None:
+        ws_ptr = _ptr(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().pa_prefill_paged_ex(
+        _ptr(out, "out", bf16=True), _ptr(q, "q", bf16=True), _ptr(k_pool, "k_pool", bf16=True),
+        _ptr(v_pool, "v_pool", bf16=True), _ptr(block_tables, "block_tables", dtype=torch.int32),
+        _ptr(context_lens, "context_lens", dtype=torch.int32),
+        _ptr(q_start_loc, "q_start_loc", dtype=torch.int32), float(scale), n_heads, n_kv_heads,
+        head_dim, block_size, n_seqs, block_tables.shape[1], int(max_chunk_len), num_blocks, int(splits),
+        ws_ptr, ws_bytes, _stream(stream))
+    check("pa_prefill_paged_ex", st)
 
 
 def pa_get_device_error() -> int:

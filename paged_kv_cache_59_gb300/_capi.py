@@ -54,6 +54,9 @@ SIGNATURES = {
                             i32, i32, vp, C.c_size_t, vp]),
     "pa_prefill_paged": (i32, [vp, vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32,
                                i32, i32, vp]),
+    "pa_prefill_workspace_bytes": (C.c_size_t, [i32, i32, i32, i32, i32]),
+    "pa_prefill_paged_ex": (i32, [vp, vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32,
+                                  i32, i32, i32, vp, C.c_size_t, vp]),
     "pa_get_device_error": (i32, [C.POINTER(C.c_int)]),
     "pa_selftest_wait_timeout": (i32, [i32, vp]),
     "pa_status_string": (C.c_char_p, [i32]),

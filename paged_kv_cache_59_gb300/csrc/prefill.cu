@@ -77,8 +77,20 @@ struct PrefillParams {
     int max_blocks;
     int num_blocks;
     int oob_row;  // a TMA row coordinate past the end of the pool (zero fill)
+    int splits;   // pieces per query-tile pair (1: no split)
+    float* part;  // splits > 1: per-piece partials [item][piece][tile][row][kPartStride]
     unsigned int* err;
 };
+
+// A piece's partial for one row: the un-normalised O (128 floats), the
+// reference maximum m (base-2 units) and the sum l of 2^(s*scale - m).
+constexpr int kPartStride = 132;  // floats, 16-byte aligned rows
+
+// Key tiles [kt0, kt1) of piece sp out of `splits` over a pair's n_kt tiles.
+__host__ __device__ inline void piece_range(int n_kt, int sp, int splits, int& kt0, int& kt1) {
+    kt0 = (int)((long long)sp * n_kt / splits);
+    kt1 = (int)((long long)(sp + 1) * n_kt / splits);
+}
 
 // max of three floats in one instruction (sm_100 family)
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -126,7 +138,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
 
-    const int qp = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int qp = blockIdx.x / P.splits, sp = blockIdx.x % P.splits, kvh = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = P.n_heads, Hk = P.n_kv_heads, h0 = kvh * G;
     if (pa::smem_u32(sm) & 1023u) {  // never expected; refuse rather than mis-swizzle
@@ -147,7 +159,12 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     // both tiles walk the key tiles up to the last row of the pair (tile A's
     // extra tiles beyond its own rows are fully masked)
     const int p_last = first_pos + min(i0 + 2 * QT, L) - 1;
-    const int n_kt = p_last / kKT + 1;
+    const int n_kt_all = p_last / kKT + 1;
+    // this CTA's piece of the key tiles (all of them when not split)
+    int kt0, kt1;
+    piece_range(n_kt_all, sp, P.splits, kt0, kt1);
+    const int n_kt = kt1 - kt0;  // tiles this CTA walks; local tile j is key tile kt0 + j
+    if (n_kt <= 0) return;       // CTA-uniform; the merge skips empty pieces
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kKS; ++i) {
@@ -226,8 +243,12 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             }
             __syncwarp();
         };
-        auto issue_k = [&](int j) { issue_tile(idk, &tmK, sm + kK0 + (j % kKS) * 32768, &k_full[j % kKS], j); };
-        auto issue_v = [&](int j) { issue_tile(idv, &tmV, sm + kV0 + (j % kVS) * 32768, &v_full[j % kVS], j); };
+        auto issue_k = [&](int j) {
+            issue_tile(idk, &tmK, sm + kK0 + (j % kKS) * 32768, &k_full[j % kKS], kt0 + j);
+        };
+        auto issue_v = [&](int j) {
+            issue_tile(idv, &tmV, sm + kV0 + (j % kVS) * 32768, &v_full[j % kVS], kt0 + j);
+        };
         int nk = 0, nv = 0;  // loads issued
         bool ok = true;
         for (; nk < kKS && nk < n_kt; ++nk) issue_k(nk);
@@ -333,7 +354,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             if (ok) ok = wait_bar(&s_full[x], (uint32_t)(j & 1), P.err, abort_flag);
             ok = __all_sync(kFull, ok);
             tc::fence_after_sync();
-            const int kb = j * kKT;
+            const int kb = (kt0 + j) * kKT;
             // V rows of the sequence's last, partial block hold whatever the pool
             // has there: zero them so that p = 0 never meets a NaN (tile A's
             // warpgroup, once V_j has landed and before PV_A(j), the first PV
@@ -440,7 +461,26 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         tc::tmem_wait_st();  // no store may be pending when the columns are released
         if (ok) ok = wait_bar(&pv_done[x], (uint32_t)((n_kt - 1) & 1), P.err, abort_flag);
         ok = __all_sync(kFull, ok);
-        if (ok) {
+        if (ok && P.splits > 1) {
+            // a piece: keep O, m and l for the merge
+            tc::fence_after_sync();
+            const size_t item = ((size_t)s * Hk + kvh) * (gridDim.x / P.splits) + qp;
+            float* dst = P.part + (((item * P.splits + sp) * 2 + x) * 128 + r) * kPartStride;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t raw[32];
+                tc::tmem_ld32(tO + c * 32, raw);
+                tc::tmem_wait_ld();
+                if (i < L) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4)
+                        *reinterpret_cast<float4*>(dst + c * 32 + k) =
+                            make_float4(__uint_as_float(raw[k]), __uint_as_float(raw[k + 1]),
+                                        __uint_as_float(raw[k + 2]), __uint_as_float(raw[k + 3]));
+                }
+            }
+            if (i < L) *reinterpret_cast<float2*>(dst + 128) = make_float2(m_used, l);
+        } else if (ok) {
             tc::fence_after_sync();
             const float inv = 1.f / l;
             uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
@@ -468,9 +508,62 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     if (warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
 }
 
+// Merges the pieces of a split query-tile pair: one warp per (chunk row, query
+// head). O = sum_p O_p 2^(m_p - M), l = sum_p l_p 2^(m_p - M), out = O / l.
+template <int G>
+__global__ void __launch_bounds__(128)
+pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int n_qp) {
+    constexpr int QT = kRows / G;
+    pa::grid_dependency_wait();  // every piece's partial is written
+    const long long w = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int H = P.n_heads, Hk = P.n_kv_heads;
+    if (w >= (long long)n_rows_total * H) return;
+    const int t = (int)(w / H), h = (int)(w % H);
+    // the sequence whose chunk holds row t: the last s with qsl[s] <= t
+    int lo = 0, hi = n_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.qsl[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int s = lo;
+    const int q0 = P.qsl[s], L = P.qsl[s + 1] - q0, ctx = P.ctx[s];
+    const int i = t - q0;
+    if (i < 0 || i >= L || ctx < L) return;
+    const int qp = i / (2 * QT), x = (i % (2 * QT)) / QT, r = (i % QT) * G + h % G, kvh = h / G;
+    const int i0 = qp * 2 * QT;
+    const int p_last = ctx - L + min(i0 + 2 * QT, L) - 1;
+    const int n_kt_all = p_last / kKT + 1;
+    const size_t item = ((size_t)s * Hk + kvh) * n_qp + qp;
+    float M = -INFINITY;
+    for (int sp = 0; sp < P.splits; ++sp) {
+        int a, b;
+        piece_range(n_kt_all, sp, P.splits, a, b);
+        if (b > a) M = fmaxf(M, P.part[(((item * P.splits + sp) * 2 + x) * 128 + r) * kPartStride + 128]);
+    }
+    float l = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < P.splits; ++sp) {
+        int a, b;
+        piece_range(n_kt_all, sp, P.splits, a, b);
+        if (b <= a) continue;
+        const float* src = P.part + (((item * P.splits + sp) * 2 + x) * 128 + r) * kPartStride;
+        const float m = src[128];
+        const float f = m == -INFINITY ? 0.f : pa::fast_exp2(m - M);
+        l += src[129] * f;
+        const float4 v = *reinterpret_cast<const float4*>(src + lane * 4);
+        o.x += v.x * f; o.y += v.y * f; o.z += v.z * f; o.w += v.w * f;
+    }
+    const float inv = 1.f / l;
+    uint2 pk;
+    pk.x = pa::float2_to_bf16x2(o.x * inv, o.y * inv);
+    pk.y = pa::float2_to_bf16x2(o.z * inv, o.w * inv);
+    *reinterpret_cast<uint2*>(P.out + ((size_t)t * H + h) * kD + lane * 4) = pk;
+}
+
 template <int G>
 int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtensorMap& tv, int n_seqs,
-                   int max_chunk_len, cudaStream_t stream) {
+                   int max_chunk_len, int n_rows, cudaStream_t stream) {
     auto kern = pa_prefill_tc_kernel<G>;
     static bool attr_done[64] = {false};
     int dev = 0;
@@ -482,20 +575,59 @@ int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtenso
         attr_done[dev] = true;
     }
     constexpr int QT = kRows / G;
-    dim3 grid((max_chunk_len + 2 * QT - 1) / (2 * QT), Pp.n_kv_heads, n_seqs);
+    const int n_qp = (max_chunk_len + 2 * QT - 1) / (2 * QT);
+    dim3 grid(n_qp * Pp.splits, Pp.n_kv_heads, n_seqs);
     kern<<<grid, 320, kSmemBytes, stream>>>(Pp, tk, tv);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (Pp.splits <= 1) return PA_OK;
+    // rows of all chunks: the merge finds each row's sequence in q_start_loc
+    const long long warps = (long long)n_rows * Pp.n_heads;
+    return pa_launch_pdl(pa_prefill_merge_kernel<G>, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, stream, Pp,
+                         n_seqs, n_rows, n_qp);
 }
 
 }  // namespace
 
-extern "C" int pa_prefill_paged(void* out, const void* q, const void* k_pool, const void* v_pool,
-                                const int32_t* block_tables, const int32_t* context_lens,
-                                const int32_t* q_start_loc, float scale, int n_heads, int n_kv_heads,
-                                int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
-                                int max_chunk_len, int num_blocks, pa_stream_t stream) {
+namespace {
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cached[dev] && cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cached[dev] = 0;
+    return cached[dev];
+}
+
+int pairs_per_seq(int G, int max_chunk_len) {
+    const int QT = kRows / G;
+    return (max_chunk_len + 2 * QT - 1) / (2 * QT);
+}
+
+// Pieces per query-tile pair for splits = 0: one CTA runs per SM, so a grid
+// of fewer pairs than SMs leaves SMs idle; splitting each pair's key range
+// into S pieces (S = SMs / pairs, at most 8) puts them to work. A grid of a
+// wave or more is not split: measured on the mixed batch (256 pairs on 152
+// SMs), 2..8 pieces per pair ran 1-6% slower than none, as CTAs that share
+// the GPU with fewer others run faster and make up the partial last wave.
+int auto_splits(long long n_items) {
+    const int sms = sm_count();
+    if (sms <= 0 || n_items <= 0 || n_items * 2 > sms) return 1;
+    const long long S = sms / n_items;
+    return (int)(S > 8 ? 8 : S);
+}
+
+size_t part_bytes(long long n_items, int splits) {
+    return splits > 1 ? (size_t)n_items * splits * 2 * 128 * kPartStride * sizeof(float) : 0;
+}
+
+int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                 const int32_t* context_lens, const int32_t* q_start_loc, float scale, int n_heads,
+                 int n_kv_heads, int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
+                 int max_chunk_len, int num_blocks, int splits, void* workspace, size_t workspace_bytes,
+                 pa_stream_t stream) {
     if (n_seqs < 0 || max_chunk_len < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || n_heads <= 0 ||
-        n_kv_heads <= 0)
+        n_kv_heads <= 0 || splits < 0 || splits > 64)
         return PA_ERR_INVALID_ARG;
     if (head_dim != kD || block_size != kBS) return PA_ERR_UNSUPPORTED;
     if (n_heads % n_kv_heads != 0) return PA_ERR_INVALID_ARG;
@@ -510,6 +642,12 @@ extern "C" int pa_prefill_paged(void* out, const void* q, const void* k_pool, co
     if (out == q) return PA_ERR_INVALID_ARG;
     const long long rows = (long long)num_blocks * n_kv_heads * kBS;
     if (rows + kBS > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+    const int n_qp = pairs_per_seq(G, max_chunk_len);
+    const long long n_items = (long long)n_qp * n_kv_heads * n_seqs;
+    if (splits == 0) splits = auto_splits(n_items);
+    if ((long long)n_qp * splits > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    const size_t need = part_bytes(n_items, splits);
+    if (need > 0 && (!workspace || workspace_bytes < need || !pa_aligned16(workspace))) return PA_ERR_WORKSPACE;
     unsigned int* err = pa_device_error_ptr();
     if (!err) return PA_ERR_CUDA;
     CUtensorMap tk, tv;
@@ -528,12 +666,51 @@ extern "C" int pa_prefill_paged(void* out, const void* q, const void* k_pool, co
     Pp.max_blocks = max_blocks_per_seq;
     Pp.num_blocks = num_blocks;
     Pp.oob_row = (int)rows;
+    Pp.splits = splits;
+    Pp.part = need ? static_cast<float*>(workspace) : nullptr;
     Pp.err = err;
+    // chunk rows bound for the merge grid (rows past the last chunk exit)
+    const long long n_rows = (long long)n_seqs * max_chunk_len;
+    if (n_rows > 0x7fffffffLL || n_rows * n_heads > 0x7fffffffLL * 4LL) return PA_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (G) {
-        case 1: return launch_prefill<1>(Pp, tk, tv, n_seqs, max_chunk_len, st);
-        case 2: return launch_prefill<2>(Pp, tk, tv, n_seqs, max_chunk_len, st);
-        case 4: return launch_prefill<4>(Pp, tk, tv, n_seqs, max_chunk_len, st);
-        default: return launch_prefill<8>(Pp, tk, tv, n_seqs, max_chunk_len, st);
+        case 1: return launch_prefill<1>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
+        case 2: return launch_prefill<2>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
+        case 4: return launch_prefill<4>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
+        default: return launch_prefill<8>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
     }
+}
+
+}  // namespace
+
+extern "C" size_t pa_prefill_workspace_bytes(int n_seqs, int n_heads, int n_kv_heads, int max_chunk_len,
+                                             int splits) {
+    if (n_seqs <= 0 || n_heads <= 0 || n_kv_heads <= 0 || max_chunk_len <= 0 || splits < 0 || splits > 64 ||
+        n_heads % n_kv_heads != 0)
+        return 0;
+    const int G = n_heads / n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return 0;
+    const long long n_items = (long long)pairs_per_seq(G, max_chunk_len) * n_kv_heads * n_seqs;
+    return part_bytes(n_items, splits == 0 ? auto_splits(n_items) : splits);
+}
+
+extern "C" int pa_prefill_paged_ex(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                   const int32_t* block_tables, const int32_t* context_lens,
+                                   const int32_t* q_start_loc, float scale, int n_heads, int n_kv_heads,
+                                   int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
+                                   int max_chunk_len, int num_blocks, int splits, void* workspace,
+                                   size_t workspace_bytes, pa_stream_t stream) {
+    return prefill_impl(out, q, k_pool, v_pool, block_tables, context_lens, q_start_loc, scale, n_heads,
+                        n_kv_heads, head_dim, block_size, n_seqs, max_blocks_per_seq, max_chunk_len, num_blocks,
+                        splits, workspace, workspace_bytes, stream);
+}
+
+extern "C" int pa_prefill_paged(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                const int32_t* q_start_loc, float scale, int n_heads, int n_kv_heads,
+                                int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
+                                int max_chunk_len, int num_blocks, pa_stream_t stream) {
+    return prefill_impl(out, q, k_pool, v_pool, block_tables, context_lens, q_start_loc, scale, n_heads,
+                        n_kv_heads, head_dim, block_size, n_seqs, max_blocks_per_seq, max_chunk_len, num_blocks,
+                        1, nullptr, 0, stream);
 }

@@ -288,6 +288,21 @@ def test_prefix_cache_matches_model_on_random_operations(capi):
                 assert bm.refcount(b) == model.refcount(b)
 
 
+def test_prefill_workspace_formula_and_errors(capi):
+    # pieces of partials: pairs per sequence x kv heads x sequences x splits x 2 tiles x 128 rows x 132 floats
+    pairs = (512 + 63) // 64                     # G = 4: 32 tokens per tile, 64 per pair
+    assert capi.pa_prefill_workspace_bytes(4, 32, 8, 512, 3) == pairs * 8 * 4 * 3 * 2 * 128 * 132 * 4
+    assert capi.pa_prefill_workspace_bytes(4, 32, 8, 512, 1) == 0
+    assert capi.pa_prefill_workspace_bytes(4, 32, 6, 512, 2) == 0   # group 32/6: not supported
+    assert capi.pa_prefill_workspace_bytes(0, 32, 8, 512, 2) == 0
+    assert capi.pa_prefill_workspace_bytes(4, 32, 8, 512, 65) == 0
+    p = C.c_void_p(4096)
+    args = [C.c_void_p(8192), p, p, p, p, p, p, C.c_float(0.1), 32, 8, 128, 16, 2, 4, 512, 16]
+    assert capi.pa_prefill_paged_ex(*args, 3, None, 0, None) == -3      # split needs a workspace
+    assert capi.pa_prefill_paged_ex(*args, -1, None, 0, None) == -1
+    assert capi.pa_prefill_paged_ex(*args, 65, None, 0, None) == -1
+
+
 def test_prefill_argument_errors_need_no_device(capi):
     p = C.c_void_p(4096)
     args = [p, p, p, p, p, p, p, C.c_float(0.1)]

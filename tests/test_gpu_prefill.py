@@ -25,15 +25,21 @@ def pk(capi):
     return m
 
 
-def _run(pk, wl):
+def _run(pk, wl, splits=None):
+    """splits None: pa_prefill_paged (no split); else pa_prefill_paged_ex with that count."""
     torch = torch_cuda()
     kp, vp = dev(wl.k_pool), dev(wl.v_pool)
     pk.pa_reshape_and_cache(dev(wl.new_k), dev(wl.new_v), kp, vp, dev(wl.slot_mapping))
     q = dev(wl.q_pf)
     out = torch.full_like(q, 0x7FC0)
     max_chunk = int(np.max(np.diff(wl.q_start_loc)))
-    pk.pa_prefill_paged(out, q, kp, vp, dev(wl.pf_tables), dev(wl.pf_ctx), dev(wl.q_start_loc), wl.scale,
-                        max_chunk)
+    args = (out, q, kp, vp, dev(wl.pf_tables), dev(wl.pf_ctx), dev(wl.q_start_loc), wl.scale, max_chunk)
+    if splits is None:
+        pk.pa_prefill_paged(*args)
+    else:
+        ws = pk.prefill_workspace(q, len(wl.pf_ctx), wl.n_kv_heads, max_chunk, splits)
+        ws_poison = ws.fill_(0xFF) if ws is not None else None  # no piece may read what it did not write
+        pk.pa_prefill_paged_ex(*args, splits=splits, workspace=ws_poison)
     torch.cuda.synchronize()
     return host_bits(out)
 
@@ -78,4 +84,36 @@ def test_prefill_mixed_workload_sampled_rows(pk):
     ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale, rows=rows)
     for r, h in rows:
         assert_attention_close(got[r, h], ref[r, h], f"mixed prefill row {(r, h)}")
+    check_device_error(0)
+
+
+@pytest.mark.parametrize("splits", [0, 2, 3, 5, 8])
+@pytest.mark.parametrize("case", [
+    dict(ctx=[300, 129], lens=[37, 129], H=32, Hk=8),     # G=4, offsets, partial blocks (few key tiles)
+    dict(ctx=[700], lens=[33], H=64, Hk=8),               # G=8, 6 key tiles
+    dict(ctx=[1500, 40], lens=[300, 40], H=16, Hk=8),     # G=2, pieces of a long range and empty pieces
+])
+def test_prefill_split_pieces_match_oracle(pk, case, splits):
+    """Key ranges split into pieces (including more pieces than key tiles, so
+    some are empty) and merged give the unsplit result's accuracy."""
+    wl = make_prefill_case(800 + sum(case["ctx"]) + splits, case["ctx"], case["lens"], [], case["H"], case["Hk"],
+                           128)
+    got = _run(pk, wl, splits)
+    ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
+    assert_attention_close(got, ref, f"prefill split={splits} {case}")
+    check_device_error(0)
+
+
+def test_prefill_mixed_workload_auto_split_sampled_rows(pk):
+    wl = make_workload("mixed")
+    got = _run(pk, wl, 0)
+    ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    rng = np.random.default_rng(6)
+    n_rows = int(wl.q_start_loc[-1])
+    rows = [(int(r), int(h)) for r, h in zip(rng.integers(0, n_rows, 24), rng.integers(0, 32, 24))]
+    rows += [(0, 0), (511, 31), (512, 5), (n_rows - 1, 7)]
+    ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale, rows=rows)
+    for r, h in rows:
+        assert_attention_close(got[r, h], ref[r, h], f"mixed split prefill row {(r, h)}")
     check_device_error(0)
