@@ -21,15 +21,19 @@
  *        an allocator".
  *
  * Common conventions
- *  - Every pointer argument of pa_decode, pa_reshape_and_cache, pa_copy_blocks
- *    and pa_prefill_paged is DEVICE memory owned by the caller, 16-byte
- *    aligned; bf16 tensors are raw 16-bit patterns. The library allocates no
- *    device memory in these calls; it owns only a 4-byte device error word
- *    per device.
- *  - KV pool layout: k_pool and v_pool are bf16
+ *  - Every pointer argument of the kernel entry points (pa_decode*,
+ *    pa_reshape_and_cache*, pa_copy_blocks, pa_prefill_paged*) is DEVICE
+ *    memory owned by the caller, 16-byte aligned unless stated otherwise;
+ *    bf16 tensors are raw 16-bit patterns. The one exception is the host
+ *    side of pa_swap_out_blocks / pa_swap_in_blocks (page-locked HOST
+ *    memory). The library allocates no device memory in these calls; it
+ *    owns a 4-byte device error word per device and the fixed scratch of
+ *    pa_decode_noalloc. The pa_bm_* block manager works on host memory only.
+ *  - KV pool layout: k_pool and v_pool are bf16 (or, for the fp8 entry
+ *    points, E4M3 bytes)
  *        [num_blocks][n_kv_heads][block_size][head_dim]
  *    so that one (block, kv-head) tile - block_size tokens of one head - is a
- *    contiguous block_size*head_dim*2 bytes. block_size must be 16 (the
+ *    contiguous block_size*head_dim*element_size bytes. block_size must be 16 (the
  *    pages' block size), head_dim 64 or 128, n_heads a multiple of
  *    n_kv_heads with group n_heads/n_kv_heads in {1, 2, 4, 8}; query head h
  *    reads KV head h / (n_heads / n_kv_heads).
