@@ -37,6 +37,7 @@
 //     weight, which on short causal rows with cancelling values exceeds an
 //     absolute error of 2e-3; the two-term P is accurate to ~2^-16.
 // The normalised output O / l is written once at the end.
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -222,25 +223,19 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 const int blk = w.group * 32 + lane;
                 w.ids = blk < nblk ? trow[blk] : -1;
             }
-            int y[kBPT];
-#pragma unroll
-            for (int b = 0; b < kBPT; ++b) {
-                const int bid = __shfl_sync(kFull, w.ids, (j & 3) * kBPT + b);
-                const int blk = j * kBPT + b;
-                bool ok = blk < nblk;
-                if (ok && (bid < 0 || bid >= P.num_blocks)) {
-                    if (lane == 0) pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
-                    ok = false;
-                }
-                y[b] = ok ? (bid * Hk + kvh) * kBS : P.oob_row;  // out of range: zero fill
+            // lane l < 16 moves box (block b = l / 2, dims 64 g .. 64 g + 63, g = l % 2)
+            const int b = (lane >> 1) & (kBPT - 1), g = lane & 1;
+            const int bid = __shfl_sync(kFull, w.ids, (j & 3) * kBPT + b);
+            const int blk = j * kBPT + b;
+            bool ok = blk < nblk;
+            if (ok && (bid < 0 || bid >= P.num_blocks)) {
+                if (lane < 2 * kBPT && g == 0) pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
+                ok = false;
             }
-            if (lane == 0) {
-                pa::mbar_arrive_expect_tx(bar, 32768);
-#pragma unroll
-                for (int b = 0; b < kBPT; ++b)
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) tc::tma_load_2d(dst + g * 16384 + b * 2048, map, g * 64, y[b], bar);
-            }
+            const int y = ok ? (bid * Hk + kvh) * kBS : P.oob_row;  // out of range: zero fill
+            if (lane == 0) pa::mbar_arrive_expect_tx(bar, 32768);
+            __syncwarp();
+            if (lane < 2 * kBPT) tc::tma_load_2d(dst + g * 16384 + b * 2048, map, g * 64, y, bar);
             __syncwarp();
         };
         auto issue_k = [&](int j) {
@@ -272,15 +267,23 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             pa::mbar_wait(&v_full[t % kVS], (uint32_t)((t / kVS) & 1), nullptr, 5000000ull);
     } else if (warp == 8) {
         // ---------------------------------------------------------- MMA issuer
+        // Matrix descriptors differ only in the start-address field (bits
+        // 0-13, byte address / 16); every operand lies inside the shared
+        // allocation, so offsets added to the low word never leave the field.
+        const uint64_t dq = tc::smem_desc(pa::smem_u32(sm + kQ), 16, 1024);
+        const uint64_t dk = tc::smem_desc(pa::smem_u32(sm + kK0), 16, 1024);
+        const uint64_t dv = tc::smem_desc(pa::smem_u32(sm + kV0), 16384, 1024);
+        auto at = [](uint64_t d, uint32_t off16) {
+            return ((uint64_t)(uint32_t)(d >> 32) << 32) | (uint32_t)((uint32_t)d + off16);
+        };
         auto issue_qk = [&](int x, int j) {  // S_x = Q_x K_j^T
             if (lane == 0) {
-                const uint32_t qs = pa::smem_u32(sm + kQ + x * 32768);
-                const uint32_t kst = pa::smem_u32(sm + kK0 + (j % kKS) * 32768);
+                const uint32_t qo = x * (32768 >> 4), ko = (j % kKS) * (32768 >> 4);
+                const uint32_t dst = tbase + x * 256;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t ad = tc::smem_desc(qs + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc(kst + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                    tc::mma_bf16(tbase + x * 256, ad, bd, ID_QK, ks > 0 ? 1u : 0u);
+                    const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                    tc::mma_bf16(dst, at(dq, qo + o), at(dk, ko + o), ID_QK, ks > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&s_full[x]);
                 if (x == 1) tc::mma_commit(&k_free[j % kKS]);  // the stage's last reader
@@ -289,16 +292,14 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         };
         auto issue_pv = [&](int x, int j) {  // O_x += P_hi V_j + P_lo V_j, P in S_x's columns
             if (lane == 0) {
-                const uint32_t vs = pa::smem_u32(sm + kV0 + (j % kVS) * 32768);
-                const uint32_t pcol = tbase + x * 256;
+                const uint32_t vo = (j % kVS) * (32768 >> 4);
+                const uint32_t pcol = tbase + x * 256, dst = pcol + 128;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t bd = tc::smem_desc(vs + ks * 2048, 16384, 1024);
-                        tc::mma_bf16_ts(tbase + x * 256 + 128, pcol + (ks >> 2) * 64 + part * 32 + (ks & 3) * 8, bd, ID_PV,
-                                        (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
-                    }
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16_ts(dst, pcol + (ks >> 1) * 32 + part * 16 + (ks & 1) * 8, at(dv, vo + ks * (2048 >> 4)),
+                                        ID_PV, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
                 tc::mma_commit(&pv_done[x]);
                 if (x == 1) tc::mma_commit(&v_free[j % kVS]);  // the stage's last reader
             }
@@ -370,32 +371,41 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 }
                 tc::fence_async_smem();
             }
-            const bool need_mask = kb + kKT - 1 > pos;
-            // pass 1: row maximum over the 128 scores (four loads, one wait)
-            float tmax;
-            {
-                uint32_t sr[kKT];
+            // Keys beyond a row's position are masked. Only the tiles on the
+            // diagonal have such keys; a warp takes the masking code only when
+            // one of its rows needs it (a warp-uniform branch), so the other
+            // tiles run the plain loops.
+            const bool mask_warp = __any_sync(kFull, kb + kKT - 1 > pos);
+            const int lim0 = pos - kb;  // keys k > lim0 of the tile are not visible
+            // pass 1: row maximum over the 128 scores, a quarter at a time
+            float tmax = -INFINITY;
+            auto pass1 = [&](auto masked) {
+#pragma unroll 1
+                for (int qd = 0; qd < 4; ++qd) {
+                    uint32_t sr[32];
+                    tc::tmem_ld32(tS + 32 * qd, sr);
+                    tc::tmem_wait_ld();
+                    if constexpr (decltype(masked)::value) {
+                        const int lim = lim0 - 32 * qd;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
-                tc::tmem_wait_ld();
-                if (need_mask) {  // causal mask: keys k > pos - kb are not visible
-                    const int lim = pos - kb;
+                        for (int k = 0; k < 32; ++k)
+                            if (k > lim) sr[k] = __float_as_uint(-INFINITY);
+                    }
+                    float mx[4];
 #pragma unroll
-                    for (int k = 0; k < kKT; ++k)
-                        if (k > lim) sr[k] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < 4; ++c) mx[c] = __uint_as_float(sr[c]);
+#pragma unroll
+                    for (int k = 4; k + 8 <= 32; k += 8)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            mx[c] = max3f(mx[c], __uint_as_float(sr[k + 2 * c]), __uint_as_float(sr[k + 2 * c + 1]));
+                    tmax = max3f(tmax, max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])),
+                                 max3f(__uint_as_float(sr[28]), __uint_as_float(sr[29]),
+                                       fmaxf(__uint_as_float(sr[30]), __uint_as_float(sr[31]))));
                 }
-                float mx[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) mx[c] = __uint_as_float(sr[c]);
-#pragma unroll
-                for (int k = 4; k + 8 <= kKT; k += 8)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        mx[c] = max3f(mx[c], __uint_as_float(sr[k + 2 * c]), __uint_as_float(sr[k + 2 * c + 1]));
-                tmax = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]));
-#pragma unroll
-                for (int k = kKT - 4; k < kKT; ++k) tmax = fmaxf(tmax, __uint_as_float(sr[k]));
-            }
+            };
+            if (mask_warp) pass1(std::true_type{});
+            else pass1(std::false_type{});
             tmax *= sc;
             const bool rescale = tmax > m_used + kRescaleThreshold;
             float alpha = 1.f;
@@ -403,39 +413,48 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
                 m_used = tmax;
             }
-            // pass 2, per half of 64 keys: p = 2^(s*scale - m) as P_hi + P_lo.
-            // Half h's scores sit in columns 64h..64h+63; P_hi of its keys
-            // 2w, 2w+1 goes to column 64h + w and P_lo to 64h + 32 + w, so a
-            // half only overwrites columns it has already read.
+            // pass 2, per quarter of 32 keys: p = 2^(s*scale - m) as P_hi + P_lo.
+            // Quarter q's scores sit in columns 32q..32q+31; P_hi of its keys
+            // 2w, 2w+1 goes to column 32q + w and P_lo to 32q + 16 + w, so a
+            // quarter only overwrites columns it has already read. P_hi is p
+            // truncated to bf16 (a byte permute), P_lo the remainder rounded to
+            // bf16: together within 2^-16 of p. Both passes loop over quarters
+            // without unrolling: the smaller body keeps the softmax warps out of
+            // instruction-fetch stalls.
             float2 psum2 = make_float2(0.f, 0.f);
             const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_used, -m_used);
             const float2 neg1 = make_float2(-1.f, -1.f);
+            auto pass2 = [&](auto masked) {
+#pragma unroll 1
+                for (int qd = 0; qd < 4; ++qd) {
+                    uint32_t raw[32];
+                    tc::tmem_ld32(tS + 32 * qd, raw);
+                    tc::tmem_wait_ld();
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t raw[64];
-                tc::tmem_ld32(tS + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(raw));
-                tc::tmem_ld32(tS + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
-                tc::tmem_wait_ld();
-                uint32_t hi[32], lo[32];
-#pragma unroll
-                for (int w = 0; w < 32; ++w) {
-                    const int k = 64 * half + 2 * w;
-                    float2 e = __ffma2_rn(make_float2(__uint_as_float(raw[2 * w]), __uint_as_float(raw[2 * w + 1])),
-                                          sc2, nm2);
-                    if (need_mask) {  // masked keys give p = 0 (also for a zero scale)
-                        if (k > pos - kb) e.x = -INFINITY;
-                        if (k + 1 > pos - kb) e.y = -INFINITY;
+                    for (int w = 0; w < 16; ++w) {
+                        float2 e = __ffma2_rn(make_float2(__uint_as_float(raw[2 * w]), __uint_as_float(raw[2 * w + 1])),
+                                              sc2, nm2);
+                        if constexpr (decltype(masked)::value) {  // masked keys give p = 0 (also for a zero scale)
+                            const int k = 32 * qd + 2 * w;
+                            if (k > lim0) e.x = -INFINITY;
+                            if (k + 1 > lim0) e.y = -INFINITY;
+                        }
+                        e.x = pa::fast_exp2(e.x);
+                        e.y = pa::fast_exp2(e.y);
+                        psum2 = __fadd2_rn(psum2, e);
+                        const uint32_t bx = __float_as_uint(e.x), by = __float_as_uint(e.y);
+                        hi[w] = __byte_perm(bx, by, 0x7632);
+                        const float2 rr = __ffma2_rn(
+                            make_float2(__uint_as_float(bx & 0xffff0000u), __uint_as_float(by & 0xffff0000u)), neg1, e);
+                        lo[w] = pa::float2_to_bf16x2(rr.x, rr.y);
                     }
-                    e.x = pa::fast_exp2(e.x);
-                    e.y = pa::fast_exp2(e.y);
-                    psum2 = __fadd2_rn(psum2, e);
-                    hi[w] = pa::float2_to_bf16x2(e.x, e.y);
-                    const float2 r = __ffma2_rn(pa::bf16x2_to_float2(hi[w]), neg1, e);
-                    lo[w] = pa::float2_to_bf16x2(r.x, r.y);
+                    tc::tmem_st16(tS + 32 * qd, hi);
+                    tc::tmem_st16(tS + 32 * qd + 16, lo);
                 }
-                tc::tmem_st32(tS + 64 * half, hi);
-                tc::tmem_st32(tS + 64 * half + 32, lo);
-            }
+            };
+            if (mask_warp) pass2(std::true_type{});
+            else pass2(std::false_type{});
             const float psum = psum2.x + psum2.y;
             l = l * alpha + psum;
             // a larger maximum rescales O_x: PV_x(j-1) must have landed first
