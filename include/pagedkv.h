@@ -308,20 +308,24 @@ int pa_prefill_paged(void* out, const void* q, const void* k_pool, const void* v
                      int max_chunk_len, int num_blocks, pa_stream_t stream);
 
 /*
- * pa_prefill_paged with the key range of each query-tile pair optionally
- * split into pieces, so that the grid fills whole waves of the GPU's SMs
- * (one prefill CTA runs per SM). Each piece keeps its un-normalised output,
- * reference maximum and sum in the workspace; a merge kernel combines the
- * pieces (O = sum_p O_p 2^(m_p - M), l = sum_p l_p 2^(m_p - M), out = O / l).
- *  splits     pieces per pair: 0 = chosen from the grid size and the
- *             device's SM count, 1 = no split (no workspace needed), 2..64
+ * pa_prefill_paged with the key range of query-tile pairs split into pieces,
+ * so that the work fills the GPU's SMs evenly (one prefill CTA runs per SM).
+ * Each piece keeps its un-normalised output, reference maximum and sum in
+ * the workspace; a merge kernel combines the pieces (O = sum_p O_p 2^(m_p -
+ * M), l = sum_p l_p 2^(m_p - M), out = O / l).
+ *  splits     0 = balanced: a small planning kernel counts every pair's key
+ *             tiles, and one CTA per SM takes an equal share of all of them
+ *             in order (a pair cut by a share boundary becomes pieces);
+ *             1 = no split (no workspace needed); 2..64 = every pair cut
+ *             into that many equal pieces
  *  workspace  DEVICE memory, 16-byte aligned, of at least
  *             pa_prefill_workspace_bytes(n_seqs, n_heads, n_kv_heads,
  *             max_chunk_len, splits) bytes (query it with the same
  *             arguments and the same current device); PA_ERR_WORKSPACE if
  *             missing or too small. Contents need no initialisation.
- * Returns 0 from pa_prefill_workspace_bytes for arguments
- * pa_prefill_paged_ex would reject, and for splits = 1.
+ * pa_prefill_workspace_bytes returns 0 for arguments pa_prefill_paged_ex
+ * would reject, for splits = 1, and for splits = 0 when no device is
+ * visible (the balanced size depends on the device's SM count).
  */
 size_t pa_prefill_workspace_bytes(int n_seqs, int n_heads, int n_kv_heads, int max_chunk_len, int splits);
 int pa_prefill_paged_ex(void* out, const void* q, const void* k_pool, const void* v_pool,

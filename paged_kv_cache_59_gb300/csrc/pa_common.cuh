@@ -61,6 +61,12 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
                  : "memory");
 }
 
+// Invalidates a barrier whose phases have all completed, before its memory
+// is initialised again.
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Makes barrier initialisation visible to the async (bulk-copy) proxy.
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

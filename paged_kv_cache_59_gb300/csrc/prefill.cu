@@ -78,8 +78,15 @@ struct PrefillParams {
     int max_blocks;
     int num_blocks;
     int oob_row;  // a TMA row coordinate past the end of the pool (zero fill)
-    int splits;   // pieces per query-tile pair (1: no split)
-    float* part;  // splits > 1: per-piece partials [item][piece][tile][row][kPartStride]
+    int splits;   // per-pair mode: pieces per query-tile pair (1: no split)
+    float* part;  // partials of pieces: [item][piece] (per-pair mode) or [CTA][2] (balanced mode),
+                  // each [tile][row][kPartStride]
+    // balanced mode (null in per-pair mode): ustart[it] = key tiles of the
+    // items before item it, it = (sequence * n_kv_heads + kv head) * n_qp + pair;
+    // ustart[n_items] = all key tiles
+    long long* ustart;
+    int n_items;
+    int n_qp;
     unsigned int* err;
 };
 
@@ -136,402 +143,516 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     uint64_t* p_full = bars + 12;   // [2] per query tile, 4 arrivals (one per warp)
     uint64_t* pv_done = bars + 14;  // [2] per query tile
     uint64_t* drain = bars + 16;
+    constexpr int kNumBars = 17;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
 
-    const int qp = blockIdx.x / P.splits, sp = blockIdx.x % P.splits, kvh = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int H = P.n_heads, Hk = P.n_kv_heads, h0 = kvh * G;
+    const int H = P.n_heads, Hk = P.n_kv_heads;
     if (pa::smem_u32(sm) & 1023u) {  // never expected; refuse rather than mis-swizzle
         if (threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_LAYOUT);
         return;
     }
-    const int q0 = P.qsl[s];
-    const int L = P.qsl[s + 1] - q0;
-    const int i0 = qp * 2 * QT;  // first chunk token of query tile A; tile B follows
-    if (i0 >= L) return;         // CTA-uniform, before any barrier or TMEM use
-    const int ctx = P.ctx[s];
-    if (ctx < L) {  // the chunk must be in the cache already
-        if (threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_CONTEXT);
-        return;
+    // Segments. Per-pair mode: piece sp of pair (qp, kv head, sequence) from
+    // the grid position. Balanced mode: an equal share [u, u_end) of the key
+    // tiles of all items in order; each segment is the part of one item in
+    // it. Only a CTA's first and last segments can be partial items; their
+    // partials go to the CTA's slots 0 and 1.
+    long long u = 0, u_end = 0;
+    if (P.ustart) {
+        const long long U = P.ustart[P.n_items];
+        u = U * blockIdx.x / gridDim.x;
+        u_end = U * (blockIdx.x + 1) / gridDim.x;
     }
-    const int nblk = min((ctx + kBS - 1) / kBS, P.max_blocks);
-    const int first_pos = ctx - L;
-    // both tiles walk the key tiles up to the last row of the pair (tile A's
-    // extra tiles beyond its own rows are fully masked)
-    const int p_last = first_pos + min(i0 + 2 * QT, L) - 1;
-    const int n_kt_all = p_last / kKT + 1;
-    // this CTA's piece of the key tiles (all of them when not split)
-    int kt0, kt1;
-    piece_range(n_kt_all, sp, P.splits, kt0, kt1);
-    const int n_kt = kt1 - kt0;  // tiles this CTA walks; local tile j is key tile kt0 + j
-    if (n_kt <= 0) return;       // CTA-uniform; the merge skips empty pieces
+    const long long u_begin = u;
+    bool have_tmem = false;
+    uint32_t tbase = 0;
+    int n_run = 0;  // segments run so far
+    for (int seg = 0;; ++seg) {
+        int s, kvh, qp, kt0 = 0, kt1 = 0;
+        bool direct = true;
+        float* part_base = nullptr;
+        if (P.ustart) {
+            if (u >= u_end) break;
+            int lo = 0, hi = P.n_items - 1;  // the item holding unit u: the last with ustart <= u
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (P.ustart[mid] <= u) lo = mid;
+                else hi = mid - 1;
+            }
+            const long long ua = P.ustart[lo], ub = P.ustart[lo + 1], ue = ub < u_end ? ub : u_end;
+            kt0 = (int)(u - ua);
+            kt1 = (int)(ue - ua);
+            direct = u == ua && ue == ub;
+            part_base = P.part + (size_t)(blockIdx.x * 2 + (u == u_begin ? 0 : 1)) * 2 * 128 * kPartStride;
+            u = ue;
+            s = lo / (Hk * P.n_qp);
+            kvh = (lo / P.n_qp) % Hk;
+            qp = lo % P.n_qp;
+        } else {
+            if (seg > 0) break;
+            qp = blockIdx.x / P.splits;
+            kvh = blockIdx.y;
+            s = blockIdx.z;
+        }
+        const int h0 = kvh * G;
+        const int q0 = P.qsl[s];
+        const int L = P.qsl[s + 1] - q0;
+        const int i0 = qp * 2 * QT;  // first chunk token of query tile A; tile B follows
+        if (i0 >= L) continue;       // segment-uniform, before any barrier or TMEM use
+        const int ctx = P.ctx[s];
+        if (ctx < L) {  // the chunk must be in the cache already
+            if (threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_CONTEXT);
+            continue;
+        }
+        const int nblk = min((ctx + kBS - 1) / kBS, P.max_blocks);
+        const int first_pos = ctx - L;
+        // both tiles walk the key tiles up to the last row of the pair (tile A's
+        // extra tiles beyond its own rows are fully masked)
+        const int p_last = first_pos + min(i0 + 2 * QT, L) - 1;
+        const int n_kt_all = p_last / kKT + 1;
+        if (!P.ustart) {  // this CTA's piece of the key tiles (all of them when not split)
+            const int sp = blockIdx.x % P.splits;
+            piece_range(n_kt_all, sp, P.splits, kt0, kt1);
+            direct = P.splits <= 1;
+            if (!direct) {
+                const size_t item = ((size_t)s * Hk + kvh) * (gridDim.x / P.splits) + qp;
+                part_base = P.part + (item * P.splits + sp) * 2 * 128 * kPartStride;
+            }
+        }
+        kt1 = min(kt1, n_kt_all);
+        const int n_kt = kt1 - kt0;  // tiles this segment walks; local tile j is key tile kt0 + j
+        if (n_kt <= 0) continue;     // segment-uniform; the merge skips empty pieces
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kKS; ++i) {
-            pa::mbar_init(&k_full[i], 1);
-            pa::mbar_init(&k_free[i], 1);
+        if (threadIdx.x == 0) {
+            if (n_run > 0) {  // every phase of the last segment has completed
+                for (int b = 0; b < kNumBars; ++b) pa::mbar_inval(&bars[b]);
+            } else {
+                *abort_flag = 0;
+            }
+            for (int i = 0; i < kKS; ++i) {
+                pa::mbar_init(&k_full[i], 1);
+                pa::mbar_init(&k_free[i], 1);
+            }
+            for (int i = 0; i < kVS; ++i) {
+                pa::mbar_init(&v_full[i], 1);
+                pa::mbar_init(&v_free[i], 1);
+            }
+            for (int x = 0; x < 2; ++x) {
+                pa::mbar_init(&s_full[x], 1);
+                pa::mbar_init(&p_full[x], 4);
+                pa::mbar_init(&pv_done[x], 1);
+            }
+            pa::mbar_init(drain, 1);
+            pa::fence_mbar_init();
         }
-        for (int i = 0; i < kVS; ++i) {
-            pa::mbar_init(&v_full[i], 1);
-            pa::mbar_init(&v_free[i], 1);
+        if (warp == 0 && !have_tmem) {
+            tc::tmem_alloc(tslot, kTmemCols);
+            tc::tmem_relinquish();
         }
-        for (int x = 0; x < 2; ++x) {
-            pa::mbar_init(&s_full[x], 1);
-            pa::mbar_init(&p_full[x], 4);
-            pa::mbar_init(&pv_done[x], 1);
-        }
-        pa::mbar_init(drain, 1);
-        *abort_flag = 0;
-        pa::fence_mbar_init();
-    }
-    if (warp == 0) {
-        tc::tmem_alloc(tslot, kTmemCols);
-        tc::tmem_relinquish();
-    }
-    // ---- Q tiles: tile X row r = (chunk token i0 + X*QT + r/G, head h0 + r%G)
-    if (warp < 8) {
-        const int x = warp >> 2, r = threadIdx.x & 127;
-        const int i = i0 + x * QT + r / G;
-        const uint4* src = reinterpret_cast<const uint4*>(P.q + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
+        // ---- Q tiles: tile X row r = (chunk token i0 + X*QT + r/G, head h0 + r%G)
+        if (warp < 8) {
+            const int x = warp >> 2, r = threadIdx.x & 127;
+            const int i = i0 + x * QT + r / G;
+            const uint4* src = reinterpret_cast<const uint4*>(P.q + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const uint4 v = i < L ? src[c] : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sm + kQ + x * 32768 + (c >> 3) * 16384 + tc::sw128_offset(r, c & 7)) = v;
-        }
-    }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tbase = *tslot;
-
-    constexpr uint32_t ID_QK = tc::idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t ID_PV = tc::idesc_bf16_f32(128, 128, 0, 1);
-
-    if (warp == 9) {
-        // ------------------------------------------------------- TMA producer
-        // K(j) goes to K stage j%3 once both QKs of K(j-3) are done (k_free);
-        // V(j) to V stage j%2 once PV_B(j-2), the last reader of V(j-2), is
-        // done. K(j+1) is issued before V(j): its stage frees first.
-        const int32_t* trow = P.tables + (size_t)s * P.max_blocks;
-        struct Ids { int ids = -1, group = -1; };  // block ids of key tiles 4g..4g+3, one per lane
-        Ids idk, idv;
-        auto issue_tile = [&](Ids& w, const CUtensorMap* map, unsigned char* dst, uint64_t* bar, int j) {
-            if ((j >> 2) != w.group) {  // warp-collective
-                w.group = j >> 2;
-                const int blk = w.group * 32 + lane;
-                w.ids = blk < nblk ? trow[blk] : -1;
-            }
-            // lane l < 16 moves box (block b = l / 2, dims 64 g .. 64 g + 63, g = l % 2)
-            const int b = (lane >> 1) & (kBPT - 1), g = lane & 1;
-            const int bid = __shfl_sync(kFull, w.ids, (j & 3) * kBPT + b);
-            const int blk = j * kBPT + b;
-            bool ok = blk < nblk;
-            if (ok && (bid < 0 || bid >= P.num_blocks)) {
-                if (lane < 2 * kBPT && g == 0) pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
-                ok = false;
-            }
-            const int y = ok ? (bid * Hk + kvh) * kBS : P.oob_row;  // out of range: zero fill
-            if (lane == 0) pa::mbar_arrive_expect_tx(bar, 32768);
-            __syncwarp();
-            if (lane < 2 * kBPT) tc::tma_load_2d(dst + g * 16384 + b * 2048, map, g * 64, y, bar);
-            __syncwarp();
-        };
-        auto issue_k = [&](int j) {
-            issue_tile(idk, &tmK, sm + kK0 + (j % kKS) * 32768, &k_full[j % kKS], kt0 + j);
-        };
-        auto issue_v = [&](int j) {
-            issue_tile(idv, &tmV, sm + kV0 + (j % kVS) * 32768, &v_full[j % kVS], kt0 + j);
-        };
-        int nk = 0, nv = 0;  // loads issued
-        bool ok = true;
-        for (; nk < kKS && nk < n_kt; ++nk) issue_k(nk);
-        for (; nv < kVS && nv < n_kt; ++nv) issue_v(nv);
-        while (ok && (nk < n_kt || nv < n_kt)) {
-            if (nk < n_kt && nk <= nv + 1) {  // K(nk) replaces K(nk-3)
-                ok = wait_bar(&k_free[nk % kKS], (uint32_t)(((nk - kKS) / kKS) & 1), P.err, abort_flag);
-                if (!ok) break;
-                issue_k(nk++);
-            } else {  // V(nv) replaces V(nv-2)
-                ok = wait_bar(&v_free[nv % kVS], (uint32_t)(((nv - kVS) / kVS) & 1), P.err, abort_flag);
-                if (!ok) break;
-                issue_v(nv++);
+            for (int c = 0; c < 16; ++c) {
+                const uint4 v = i < L ? src[c] : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(sm + kQ + x * 32768 + (c >> 3) * 16384 + tc::sw128_offset(r, c & 7)) = v;
             }
         }
-        // every issued copy has landed before the CTA may exit (bounded; in
-        // the normal case the MMA warp has already consumed them all)
-        for (int t = (nk > kKS ? nk - kKS : 0); t < nk; ++t)
-            pa::mbar_wait(&k_full[t % kKS], (uint32_t)((t / kKS) & 1), nullptr, 5000000ull);
-        for (int t = (nv > kVS ? nv - kVS : 0); t < nv; ++t)
-            pa::mbar_wait(&v_full[t % kVS], (uint32_t)((t / kVS) & 1), nullptr, 5000000ull);
-    } else if (warp == 8) {
-        // ---------------------------------------------------------- MMA issuer
-        // Matrix descriptors differ only in the start-address field (bits
-        // 0-13, byte address / 16); every operand lies inside the shared
-        // allocation, so offsets added to the low word never leave the field.
-        const uint64_t dq = tc::smem_desc(pa::smem_u32(sm + kQ), 16, 1024);
-        const uint64_t dk = tc::smem_desc(pa::smem_u32(sm + kK0), 16, 1024);
-        const uint64_t dv = tc::smem_desc(pa::smem_u32(sm + kV0), 16384, 1024);
-        auto at = [](uint64_t d, uint32_t off16) {
-            return ((uint64_t)(uint32_t)(d >> 32) << 32) | (uint32_t)((uint32_t)d + off16);
-        };
-        auto issue_qk = [&](int x, int j) {  // S_x = Q_x K_j^T
-            if (lane == 0) {
-                const uint32_t qo = x * (32768 >> 4), ko = (j % kKS) * (32768 >> 4);
-                const uint32_t dst = tbase + x * 256;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                    tc::mma_bf16(dst, at(dq, qo + o), at(dk, ko + o), ID_QK, ks > 0 ? 1u : 0u);
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        tbase = *tslot;
+        have_tmem = true;
+
+        constexpr uint32_t ID_QK = tc::idesc_bf16_f32(128, 128, 0, 0);
+        constexpr uint32_t ID_PV = tc::idesc_bf16_f32(128, 128, 0, 1);
+
+        if (warp == 9) {
+            // ------------------------------------------------------- TMA producer
+            // K(j) goes to K stage j%3 once both QKs of K(j-3) are done (k_free);
+            // V(j) to V stage j%2 once PV_B(j-2), the last reader of V(j-2), is
+            // done. K(j+1) is issued before V(j): its stage frees first.
+            const int32_t* trow = P.tables + (size_t)s * P.max_blocks;
+            struct Ids { int ids = -1, group = -1; };  // block ids of key tiles 4g..4g+3, one per lane
+            Ids idk, idv;
+            auto issue_tile = [&](Ids& w, const CUtensorMap* map, unsigned char* dst, uint64_t* bar, int j) {
+                if ((j >> 2) != w.group) {  // warp-collective
+                    w.group = j >> 2;
+                    const int blk = w.group * 32 + lane;
+                    w.ids = blk < nblk ? trow[blk] : -1;
                 }
-                tc::mma_commit(&s_full[x]);
-                if (x == 1) tc::mma_commit(&k_free[j % kKS]);  // the stage's last reader
+                // lane l < 16 moves box (block b = l / 2, dims 64 g .. 64 g + 63, g = l % 2)
+                const int b = (lane >> 1) & (kBPT - 1), g = lane & 1;
+                const int bid = __shfl_sync(kFull, w.ids, (j & 3) * kBPT + b);
+                const int blk = j * kBPT + b;
+                bool ok = blk < nblk;
+                if (ok && (bid < 0 || bid >= P.num_blocks)) {
+                    if (lane < 2 * kBPT && g == 0) pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
+                    ok = false;
+                }
+                const int y = ok ? (bid * Hk + kvh) * kBS : P.oob_row;  // out of range: zero fill
+                if (lane == 0) pa::mbar_arrive_expect_tx(bar, 32768);
+                __syncwarp();
+                if (lane < 2 * kBPT) tc::tma_load_2d(dst + g * 16384 + b * 2048, map, g * 64, y, bar);
+                __syncwarp();
+            };
+            auto issue_k = [&](int j) {
+                issue_tile(idk, &tmK, sm + kK0 + (j % kKS) * 32768, &k_full[j % kKS], kt0 + j);
+            };
+            auto issue_v = [&](int j) {
+                issue_tile(idv, &tmV, sm + kV0 + (j % kVS) * 32768, &v_full[j % kVS], kt0 + j);
+            };
+            int nk = 0, nv = 0;  // loads issued
+            bool ok = true;
+            for (; nk < kKS && nk < n_kt; ++nk) issue_k(nk);
+            for (; nv < kVS && nv < n_kt; ++nv) issue_v(nv);
+            while (ok && (nk < n_kt || nv < n_kt)) {
+                if (nk < n_kt && nk <= nv + 1) {  // K(nk) replaces K(nk-3)
+                    ok = wait_bar(&k_free[nk % kKS], (uint32_t)(((nk - kKS) / kKS) & 1), P.err, abort_flag);
+                    if (!ok) break;
+                    issue_k(nk++);
+                } else {  // V(nv) replaces V(nv-2)
+                    ok = wait_bar(&v_free[nv % kVS], (uint32_t)(((nv - kVS) / kVS) & 1), P.err, abort_flag);
+                    if (!ok) break;
+                    issue_v(nv++);
+                }
             }
-            __syncwarp();
-        };
-        auto issue_pv = [&](int x, int j) {  // O_x += P_hi V_j + P_lo V_j, P in S_x's columns
-            if (lane == 0) {
-                const uint32_t vo = (j % kVS) * (32768 >> 4);
-                const uint32_t pcol = tbase + x * 256, dst = pcol + 128;
+            // every issued copy has landed before the CTA may exit (bounded; in
+            // the normal case the MMA warp has already consumed them all)
+            for (int t = (nk > kKS ? nk - kKS : 0); t < nk; ++t)
+                pa::mbar_wait(&k_full[t % kKS], (uint32_t)((t / kKS) & 1), nullptr, 5000000ull);
+            for (int t = (nv > kVS ? nv - kVS : 0); t < nv; ++t)
+                pa::mbar_wait(&v_full[t % kVS], (uint32_t)((t / kVS) & 1), nullptr, 5000000ull);
+        } else if (warp == 8) {
+            // ---------------------------------------------------------- MMA issuer
+            // Matrix descriptors differ only in the start-address field (bits
+            // 0-13, byte address / 16); every operand lies inside the shared
+            // allocation, so offsets added to the low word never leave the field.
+            const uint64_t dq = tc::smem_desc(pa::smem_u32(sm + kQ), 16, 1024);
+            const uint64_t dk = tc::smem_desc(pa::smem_u32(sm + kK0), 16, 1024);
+            const uint64_t dv = tc::smem_desc(pa::smem_u32(sm + kV0), 16384, 1024);
+            auto at = [](uint64_t d, uint32_t off16) {
+                return ((uint64_t)(uint32_t)(d >> 32) << 32) | (uint32_t)((uint32_t)d + off16);
+            };
+            auto issue_qk = [&](int x, int j) {  // S_x = Q_x K_j^T
+                if (lane == 0) {
+                    const uint32_t qo = x * (32768 >> 4), ko = (j % kKS) * (32768 >> 4);
+                    const uint32_t dst = tbase + x * 256;
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                        tc::mma_bf16(dst, at(dq, qo + o), at(dk, ko + o), ID_QK, ks > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(&s_full[x]);
+                    if (x == 1) tc::mma_commit(&k_free[j % kKS]);  // the stage's last reader
+                }
+                __syncwarp();
+            };
+            auto issue_pv = [&](int x, int j) {  // O_x += P_hi V_j + P_lo V_j, P in S_x's columns
+                if (lane == 0) {
+                    const uint32_t vo = (j % kVS) * (32768 >> 4);
+                    const uint32_t pcol = tbase + x * 256, dst = pcol + 128;
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_bf16_ts(dst, pcol + (ks >> 1) * 32 + part * 16 + (ks & 1) * 8, at(dv, vo + ks * (2048 >> 4)),
-                                        ID_PV, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
-                tc::mma_commit(&pv_done[x]);
-                if (x == 1) tc::mma_commit(&v_free[j % kVS]);  // the stage's last reader
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_bf16_ts(dst, pcol + (ks >> 1) * 32 + part * 16 + (ks & 1) * 8, at(dv, vo + ks * (2048 >> 4)),
+                                            ID_PV, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+                    tc::mma_commit(&pv_done[x]);
+                    if (x == 1) tc::mma_commit(&v_free[j % kVS]);  // the stage's last reader
+                }
+                __syncwarp();
+            };
+            // The tensor core runs the MMAs of this thread in issue order, so
+            // QK_x(j+1) may follow PV_x(j) (which reads P out of S_x's columns)
+            // without a wait.
+            bool ok = wait_bar(&k_full[0], 0, P.err, abort_flag);
+            if (ok) {
+                tc::fence_after_sync();
+                issue_qk(0, 0);
+                issue_qk(1, 0);
             }
-            __syncwarp();
-        };
-        // The tensor core runs the MMAs of this thread in issue order, so
-        // QK_x(j+1) may follow PV_x(j) (which reads P out of S_x's columns)
-        // without a wait.
-        bool ok = wait_bar(&k_full[0], 0, P.err, abort_flag);
-        if (ok) {
-            tc::fence_after_sync();
-            issue_qk(0, 0);
-            issue_qk(1, 0);
-        }
-        for (int j = 0; j < n_kt && ok; ++j) {
-            const uint32_t par = (uint32_t)(j & 1);
-            ok = wait_bar(&p_full[0], par, P.err, abort_flag);
-            if (ok) ok = wait_bar(&v_full[j % kVS], (uint32_t)((j / kVS) & 1), P.err, abort_flag);
-            if (!ok) break;
-            tc::fence_after_sync();
-            issue_pv(0, j);
-            if (j + 1 < n_kt) {
-                ok = wait_bar(&k_full[(j + 1) % kKS], (uint32_t)(((j + 1) / kKS) & 1), P.err, abort_flag);
-                if (!ok) break;
-                issue_qk(0, j + 1);
-            }
-            ok = wait_bar(&p_full[1], par, P.err, abort_flag);
-            if (!ok) break;
-            tc::fence_after_sync();
-            issue_pv(1, j);
-            if (j + 1 < n_kt) issue_qk(1, j + 1);
-        }
-        // drain: every issued MMA has completed before the CTA can release its
-        // shared and tensor memory (bounded wait)
-        if (lane == 0) tc::mma_commit(drain);
-        __syncwarp();
-        pa::mbar_wait(drain, 0, nullptr, 10000000ull);
-    } else {
-        // --------------------------------------- softmax warpgroup of tile x
-        // warp w serves TMEM lanes 32*(w%4) .. +31 (rows). After a failed wait
-        // (timeout) the warps keep iterating without waiting.
-        const int x = warp >> 2;
-        const int r = threadIdx.x & 127;  // matrix row = TMEM lane
-        const int i = i0 + x * QT + r / G;
-        const int pos = first_pos + i;  // this row's position (padding rows: beyond the chunk)
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tbase + x * 256 + lane_base;
-        const uint32_t tO = tS + 128;
-        const float sc = P.scale_log2;
-        float m_used = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < n_kt; ++j) {
-            if (ok) ok = wait_bar(&s_full[x], (uint32_t)(j & 1), P.err, abort_flag);
-            ok = __all_sync(kFull, ok);
-            tc::fence_after_sync();
-            const int kb = (kt0 + j) * kKT;
-            // V rows of the sequence's last, partial block hold whatever the pool
-            // has there: zero them so that p = 0 never meets a NaN (tile A's
-            // warpgroup, once V_j has landed and before PV_A(j), the first PV
-            // reading it)
-            if (x == 0 && (ctx & (kBS - 1)) && ctx > kb && ctx < kb + kKT) {
+            for (int j = 0; j < n_kt && ok; ++j) {
+                const uint32_t par = (uint32_t)(j & 1);
+                ok = wait_bar(&p_full[0], par, P.err, abort_flag);
                 if (ok) ok = wait_bar(&v_full[j % kVS], (uint32_t)((j / kVS) & 1), P.err, abort_flag);
-                ok = __all_sync(kFull, ok);
-                const int z0 = ctx - kb, z1 = min(((ctx + kBS - 1) & ~(kBS - 1)) - kb, kKT);
-                unsigned char* vs = sm + kV0 + (j % kVS) * 32768;
-                for (int e = r; e < (z1 - z0) * 16; e += 128) {
-                    const int row = z0 + (e >> 4), g = (e >> 3) & 1, c = e & 7;
-                    *reinterpret_cast<uint4*>(vs + g * 16384 + tc::sw128_offset(row, c)) = make_uint4(0, 0, 0, 0);
+                if (!ok) break;
+                tc::fence_after_sync();
+                issue_pv(0, j);
+                if (j + 1 < n_kt) {
+                    ok = wait_bar(&k_full[(j + 1) % kKS], (uint32_t)(((j + 1) / kKS) & 1), P.err, abort_flag);
+                    if (!ok) break;
+                    issue_qk(0, j + 1);
                 }
-                tc::fence_async_smem();
+                ok = wait_bar(&p_full[1], par, P.err, abort_flag);
+                if (!ok) break;
+                tc::fence_after_sync();
+                issue_pv(1, j);
+                if (j + 1 < n_kt) issue_qk(1, j + 1);
             }
-            // Keys beyond a row's position are masked. Only the tiles on the
-            // diagonal have such keys; a warp takes the masking code only when
-            // one of its rows needs it (a warp-uniform branch), so the other
-            // tiles run the plain loops.
-            const bool mask_warp = __any_sync(kFull, kb + kKT - 1 > pos);
-            const int lim0 = pos - kb;  // keys k > lim0 of the tile are not visible
-            // pass 1: row maximum over the 128 scores, a quarter at a time
-            float tmax = -INFINITY;
-            auto pass1 = [&](auto masked) {
-#pragma unroll 1
-                for (int qd = 0; qd < 4; ++qd) {
-                    uint32_t sr[32];
-                    tc::tmem_ld32(tS + 32 * qd, sr);
-                    tc::tmem_wait_ld();
-                    if constexpr (decltype(masked)::value) {
-                        const int lim = lim0 - 32 * qd;
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            if (k > lim) sr[k] = __float_as_uint(-INFINITY);
-                    }
-                    float mx[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) mx[c] = __uint_as_float(sr[c]);
-#pragma unroll
-                    for (int k = 4; k + 8 <= 32; k += 8)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            mx[c] = max3f(mx[c], __uint_as_float(sr[k + 2 * c]), __uint_as_float(sr[k + 2 * c + 1]));
-                    tmax = max3f(tmax, max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])),
-                                 max3f(__uint_as_float(sr[28]), __uint_as_float(sr[29]),
-                                       fmaxf(__uint_as_float(sr[30]), __uint_as_float(sr[31]))));
-                }
-            };
-            if (mask_warp) pass1(std::true_type{});
-            else pass1(std::false_type{});
-            tmax *= sc;
-            const bool rescale = tmax > m_used + kRescaleThreshold;
-            float alpha = 1.f;
-            if (rescale) {
-                alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
-                m_used = tmax;
+            // drain: every issued MMA has completed before the CTA can release its
+            // shared and tensor memory (bounded wait)
+            if (lane == 0) tc::mma_commit(drain);
+            __syncwarp();
+            pa::mbar_wait(drain, 0, nullptr, 10000000ull);
+            if (ok) {  // the stages' last frees (never waited for) land before the barriers are reused
+                for (int t = max(0, n_kt - kKS); t < n_kt; ++t)
+                    pa::mbar_wait(&k_free[t % kKS], (uint32_t)((t / kKS) & 1), nullptr, 10000000ull);
+                for (int t = max(0, n_kt - kVS); t < n_kt; ++t)
+                    pa::mbar_wait(&v_free[t % kVS], (uint32_t)((t / kVS) & 1), nullptr, 10000000ull);
             }
-            // pass 2, per quarter of 32 keys: p = 2^(s*scale - m) as P_hi + P_lo.
-            // Quarter q's scores sit in columns 32q..32q+31; P_hi of its keys
-            // 2w, 2w+1 goes to column 32q + w and P_lo to 32q + 16 + w, so a
-            // quarter only overwrites columns it has already read. P_hi is p
-            // truncated to bf16 (a byte permute), P_lo the remainder rounded to
-            // bf16: together within 2^-16 of p. Both passes loop over quarters
-            // without unrolling: the smaller body keeps the softmax warps out of
-            // instruction-fetch stalls.
-            float2 psum2 = make_float2(0.f, 0.f);
-            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_used, -m_used);
-            const float2 neg1 = make_float2(-1.f, -1.f);
-            auto pass2 = [&](auto masked) {
-#pragma unroll 1
-                for (int qd = 0; qd < 4; ++qd) {
-                    uint32_t raw[32];
-                    tc::tmem_ld32(tS + 32 * qd, raw);
-                    tc::tmem_wait_ld();
-                    uint32_t hi[16], lo[16];
-#pragma unroll
-                    for (int w = 0; w < 16; ++w) {
-                        float2 e = __ffma2_rn(make_float2(__uint_as_float(raw[2 * w]), __uint_as_float(raw[2 * w + 1])),
-                                              sc2, nm2);
-                        if constexpr (decltype(masked)::value) {  // masked keys give p = 0 (also for a zero scale)
-                            const int k = 32 * qd + 2 * w;
-                            if (k > lim0) e.x = -INFINITY;
-                            if (k + 1 > lim0) e.y = -INFINITY;
-                        }
-                        e.x = pa::fast_exp2(e.x);
-                        e.y = pa::fast_exp2(e.y);
-                        psum2 = __fadd2_rn(psum2, e);
-                        const uint32_t bx = __float_as_uint(e.x), by = __float_as_uint(e.y);
-                        hi[w] = __byte_perm(bx, by, 0x7632);
-                        const float2 rr = __ffma2_rn(
-                            make_float2(__uint_as_float(bx & 0xffff0000u), __uint_as_float(by & 0xffff0000u)), neg1, e);
-                        lo[w] = pa::float2_to_bf16x2(rr.x, rr.y);
-                    }
-                    tc::tmem_st16(tS + 32 * qd, hi);
-                    tc::tmem_st16(tS + 32 * qd + 16, lo);
-                }
-            };
-            if (mask_warp) pass2(std::true_type{});
-            else pass2(std::false_type{});
-            const float psum = psum2.x + psum2.y;
-            l = l * alpha + psum;
-            // a larger maximum rescales O_x: PV_x(j-1) must have landed first
-            if (j > 0 && __any_sync(kFull, rescale)) {
-                if (ok) ok = wait_bar(&pv_done[x], (uint32_t)((j - 1) & 1), P.err, abort_flag);
+        } else {
+            // --------------------------------------- softmax warpgroup of tile x
+            // warp w serves TMEM lanes 32*(w%4) .. +31 (rows). After a failed wait
+            // (timeout) the warps keep iterating without waiting.
+            const int x = warp >> 2;
+            const int r = threadIdx.x & 127;  // matrix row = TMEM lane
+            const int i = i0 + x * QT + r / G;
+            const int pos = first_pos + i;  // this row's position (padding rows: beyond the chunk)
+            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+            const uint32_t tS = tbase + x * 256 + lane_base;
+            const uint32_t tO = tS + 128;
+            const float sc = P.scale_log2;
+            float m_used = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < n_kt; ++j) {
+                if (ok) ok = wait_bar(&s_full[x], (uint32_t)(j & 1), P.err, abort_flag);
                 ok = __all_sync(kFull, ok);
                 tc::fence_after_sync();
+                const int kb = (kt0 + j) * kKT;
+                // V rows of the sequence's last, partial block hold whatever the pool
+                // has there: zero them so that p = 0 never meets a NaN (tile A's
+                // warpgroup, once V_j has landed and before PV_A(j), the first PV
+                // reading it)
+                if (x == 0 && (ctx & (kBS - 1)) && ctx > kb && ctx < kb + kKT) {
+                    if (ok) ok = wait_bar(&v_full[j % kVS], (uint32_t)((j / kVS) & 1), P.err, abort_flag);
+                    ok = __all_sync(kFull, ok);
+                    const int z0 = ctx - kb, z1 = min(((ctx + kBS - 1) & ~(kBS - 1)) - kb, kKT);
+                    unsigned char* vs = sm + kV0 + (j % kVS) * 32768;
+                    for (int e = r; e < (z1 - z0) * 16; e += 128) {
+                        const int row = z0 + (e >> 4), g = (e >> 3) & 1, c = e & 7;
+                        *reinterpret_cast<uint4*>(vs + g * 16384 + tc::sw128_offset(row, c)) = make_uint4(0, 0, 0, 0);
+                    }
+                    tc::fence_async_smem();
+                }
+                // Keys beyond a row's position are masked. Only the tiles on the
+                // diagonal have such keys; a warp takes the masking code only when
+                // one of its rows needs it (a warp-uniform branch), so the other
+                // tiles run the plain loops.
+                const bool mask_warp = __any_sync(kFull, kb + kKT - 1 > pos);
+                const int lim0 = pos - kb;  // keys k > lim0 of the tile are not visible
+                // pass 1: row maximum over the 128 scores, a quarter at a time
+                float tmax = -INFINITY;
+                auto pass1 = [&](auto masked) {
+#pragma unroll 1
+                    for (int qd = 0; qd < 4; ++qd) {
+                        uint32_t sr[32];
+                        tc::tmem_ld32(tS + 32 * qd, sr);
+                        tc::tmem_wait_ld();
+                        if constexpr (decltype(masked)::value) {
+                            const int lim = lim0 - 32 * qd;
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                if (k > lim) sr[k] = __float_as_uint(-INFINITY);
+                        }
+                        float mx[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) mx[c] = __uint_as_float(sr[c]);
+#pragma unroll
+                        for (int k = 4; k + 8 <= 32; k += 8)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                mx[c] = max3f(mx[c], __uint_as_float(sr[k + 2 * c]), __uint_as_float(sr[k + 2 * c + 1]));
+                        tmax = max3f(tmax, max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])),
+                                     max3f(__uint_as_float(sr[28]), __uint_as_float(sr[29]),
+                                           fmaxf(__uint_as_float(sr[30]), __uint_as_float(sr[31]))));
+                    }
+                };
+                if (mask_warp) pass1(std::true_type{});
+                else pass1(std::false_type{});
+                tmax *= sc;
+                const bool rescale = tmax > m_used + kRescaleThreshold;
+                float alpha = 1.f;
+                if (rescale) {
+                    alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
+                    m_used = tmax;
+                }
+                // pass 2, per quarter of 32 keys: p = 2^(s*scale - m) as P_hi + P_lo.
+                // Quarter q's scores sit in columns 32q..32q+31; P_hi of its keys
+                // 2w, 2w+1 goes to column 32q + w and P_lo to 32q + 16 + w, so a
+                // quarter only overwrites columns it has already read. P_hi is p
+                // truncated to bf16 (a byte permute), P_lo the remainder rounded to
+                // bf16: together within 2^-16 of p. Both passes loop over quarters
+                // without unrolling: the smaller body keeps the softmax warps out of
+                // instruction-fetch stalls.
+                float2 psum2 = make_float2(0.f, 0.f);
+                const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_used, -m_used);
+                const float2 neg1 = make_float2(-1.f, -1.f);
+                auto pass2 = [&](auto masked) {
+#pragma unroll 1
+                    for (int qd = 0; qd < 4; ++qd) {
+                        uint32_t raw[32];
+                        tc::tmem_ld32(tS + 32 * qd, raw);
+                        tc::tmem_wait_ld();
+                        uint32_t hi[16], lo[16];
+#pragma unroll
+                        for (int w = 0; w < 16; ++w) {
+                            float2 e = __ffma2_rn(make_float2(__uint_as_float(raw[2 * w]), __uint_as_float(raw[2 * w + 1])),
+                                                  sc2, nm2);
+                            if constexpr (decltype(masked)::value) {  // masked keys give p = 0 (also for a zero scale)
+                                const int k = 32 * qd + 2 * w;
+                                if (k > lim0) e.x = -INFINITY;
+                                if (k + 1 > lim0) e.y = -INFINITY;
+                            }
+                            e.x = pa::fast_exp2(e.x);
+                            e.y = pa::fast_exp2(e.y);
+                            psum2 = __fadd2_rn(psum2, e);
+                            const uint32_t bx = __float_as_uint(e.x), by = __float_as_uint(e.y);
+                            hi[w] = __byte_perm(bx, by, 0x7632);
+                            const float2 rr = __ffma2_rn(
+                                make_float2(__uint_as_float(bx & 0xffff0000u), __uint_as_float(by & 0xffff0000u)), neg1, e);
+                            lo[w] = pa::float2_to_bf16x2(rr.x, rr.y);
+                        }
+                        tc::tmem_st16(tS + 32 * qd, hi);
+                        tc::tmem_st16(tS + 32 * qd + 16, lo);
+                    }
+                };
+                if (mask_warp) pass2(std::true_type{});
+                else pass2(std::false_type{});
+                const float psum = psum2.x + psum2.y;
+                l = l * alpha + psum;
+                // a larger maximum rescales O_x: PV_x(j-1) must have landed first
+                if (j > 0 && __any_sync(kFull, rescale)) {
+                    if (ok) ok = wait_bar(&pv_done[x], (uint32_t)((j - 1) & 1), P.err, abort_flag);
+                    ok = __all_sync(kFull, ok);
+                    tc::fence_after_sync();
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t raw[32];
+                        tc::tmem_ld32(tO + c * 32, raw);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) raw[k] = __float_as_uint(__uint_as_float(raw[k]) * alpha);
+                        tc::tmem_st32(tO + c * 32, raw);
+                    }
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) pa::mbar_arrive(&p_full[x]);
+            }
+            tc::tmem_wait_st();  // no store may be pending when the columns are released
+            if (ok) ok = wait_bar(&pv_done[x], (uint32_t)((n_kt - 1) & 1), P.err, abort_flag);
+            ok = __all_sync(kFull, ok);
+            if (ok && !direct) {
+                // a piece: keep O, m and l for the merge
+                tc::fence_after_sync();
+                float* dst = part_base + ((size_t)x * 128 + r) * kPartStride;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t raw[32];
                     tc::tmem_ld32(tO + c * 32, raw);
                     tc::tmem_wait_ld();
+                    if (i < L) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) raw[k] = __float_as_uint(__uint_as_float(raw[k]) * alpha);
-                    tc::tmem_st32(tO + c * 32, raw);
+                        for (int k = 0; k < 32; k += 4)
+                            *reinterpret_cast<float4*>(dst + c * 32 + k) =
+                                make_float4(__uint_as_float(raw[k]), __uint_as_float(raw[k + 1]),
+                                            __uint_as_float(raw[k + 2]), __uint_as_float(raw[k + 3]));
+                    }
                 }
-            }
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) pa::mbar_arrive(&p_full[x]);
-        }
-        tc::tmem_wait_st();  // no store may be pending when the columns are released
-        if (ok) ok = wait_bar(&pv_done[x], (uint32_t)((n_kt - 1) & 1), P.err, abort_flag);
-        ok = __all_sync(kFull, ok);
-        if (ok && P.splits > 1) {
-            // a piece: keep O, m and l for the merge
-            tc::fence_after_sync();
-            const size_t item = ((size_t)s * Hk + kvh) * (gridDim.x / P.splits) + qp;
-            float* dst = P.part + (((item * P.splits + sp) * 2 + x) * 128 + r) * kPartStride;
+                if (i < L) *reinterpret_cast<float2*>(dst + 128) = make_float2(m_used, l);
+            } else if (ok) {
+                tc::fence_after_sync();
+                const float inv = 1.f / l;
+                uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t raw[32];
-                tc::tmem_ld32(tO + c * 32, raw);
-                tc::tmem_wait_ld();
-                if (i < L) {
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t raw[32];
+                    tc::tmem_ld32(tO + c * 32, raw);
+                    tc::tmem_wait_ld();
+                    if (i < L) {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4)
-                        *reinterpret_cast<float4*>(dst + c * 32 + k) =
-                            make_float4(__uint_as_float(raw[k]), __uint_as_float(raw[k + 1]),
-                                        __uint_as_float(raw[k + 2]), __uint_as_float(raw[k + 3]));
-                }
-            }
-            if (i < L) *reinterpret_cast<float2*>(dst + 128) = make_float2(m_used, l);
-        } else if (ok) {
-            tc::fence_after_sync();
-            const float inv = 1.f / l;
-            uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t raw[32];
-                tc::tmem_ld32(tO + c * 32, raw);
-                tc::tmem_wait_ld();
-                if (i < L) {
-#pragma unroll
-                    for (int k = 0; k < 32; k += 8) {
-                        uint4 w;
-                        w.x = pa::float2_to_bf16x2(__uint_as_float(raw[k]) * inv, __uint_as_float(raw[k + 1]) * inv);
-                        w.y = pa::float2_to_bf16x2(__uint_as_float(raw[k + 2]) * inv, __uint_as_float(raw[k + 3]) * inv);
-                        w.z = pa::float2_to_bf16x2(__uint_as_float(raw[k + 4]) * inv, __uint_as_float(raw[k + 5]) * inv);
-                        w.w = pa::float2_to_bf16x2(__uint_as_float(raw[k + 6]) * inv, __uint_as_float(raw[k + 7]) * inv);
-                        dst[(c * 32 + k) / 8] = w;
+                        for (int k = 0; k < 32; k += 8) {
+                            uint4 w;
+                            w.x = pa::float2_to_bf16x2(__uint_as_float(raw[k]) * inv, __uint_as_float(raw[k + 1]) * inv);
+                            w.y = pa::float2_to_bf16x2(__uint_as_float(raw[k + 2]) * inv, __uint_as_float(raw[k + 3]) * inv);
+                            w.z = pa::float2_to_bf16x2(__uint_as_float(raw[k + 4]) * inv, __uint_as_float(raw[k + 5]) * inv);
+                            w.w = pa::float2_to_bf16x2(__uint_as_float(raw[k + 6]) * inv, __uint_as_float(raw[k + 7]) * inv);
+                            dst[(c * 32 + k) / 8] = w;
+                        }
                     }
                 }
             }
         }
+        tc::fence_before_sync();
+        __syncthreads();  // end of the segment: every role is done with smem, TMEM and the barriers
+        ++n_run;
+    }  // segments
+    if (have_tmem && warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
+}
+
+// Key tiles of item it = (sequence * n_kv_heads + kv head) * n_qp + pair:
+// 0 if the pair has no rows. A chunk that is not in the cache (ctx < L) has
+// none either, and flags the device error once per sequence.
+template <int G>
+__device__ int item_tiles(const PrefillParams& P, int it) {
+    constexpr int QT = kRows / G;
+    const int per_seq = P.n_kv_heads * P.n_qp;
+    const int s = it / per_seq, qp = it % P.n_qp;
+    const int q0 = P.qsl[s], L = P.qsl[s + 1] - q0, i0 = qp * 2 * QT;
+    if (i0 >= L) return 0;
+    const int ctx = P.ctx[s];
+    if (ctx < L) {
+        if (it % per_seq == 0) pa::set_error(P.err, PA_DEVERR_CONTEXT);
+        return 0;
     }
-    tc::fence_before_sync();
+    return (ctx - L + min(i0 + 2 * QT, L) - 1) / kKT + 1;
+}
+
+// Balanced mode: ustart = exclusive prefix sum of the items' key tiles, one
+// block of 1024 threads (each a run of consecutive items).
+template <int G>
+__global__ void __launch_bounds__(1024) pa_prefill_plan_kernel(const PrefillParams P) {
+    __shared__ long long wsum[32];
+    const int n = P.n_items, t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int per = (n + 1023) / 1024;
+    const int b0 = min(n, t * per), b1 = min(n, b0 + per);
+    long long mine = 0;
+    for (int it = b0; it < b1; ++it) mine += item_tiles<G>(P, it);
+    long long incl = mine;  // inclusive prefix within the warp
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[wid] = incl;
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
+    if (wid == 0) {
+        long long v = wsum[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += y;
+        }
+        wsum[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    long long base = incl - mine + (wid > 0 ? wsum[wid - 1] : 0);
+    for (int it = b0; it < b1; ++it) {
+        P.ustart[it] = base;
+        base += item_tiles<G>(P, it);
+    }
+    if (t == 1023) P.ustart[n] = base;
 }
 
 // Merges the pieces of a split query-tile pair: one warp per (chunk row, query
 // head). O = sum_p O_p 2^(m_p - M), l = sum_p l_p 2^(m_p - M), out = O / l.
 template <int G>
 __global__ void __launch_bounds__(128)
-pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int n_qp) {
+pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int n_qp, int n_cta) {
     constexpr int QT = kRows / G;
     pa::grid_dependency_wait();  // every piece's partial is written
     const long long w = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -554,19 +675,50 @@ pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int
     const int p_last = ctx - L + min(i0 + 2 * QT, L) - 1;
     const int n_kt_all = p_last / kKT + 1;
     const size_t item = ((size_t)s * Hk + kvh) * n_qp + qp;
+    // the pieces: per-pair mode, piece sp of `splits` (empty ones skipped);
+    // balanced mode, one per CTA c0..c1 whose share holds some of the pair's
+    // key tiles (c0 wrote it to its slot 1 unless the pair starts its share),
+    // none if one CTA ran the whole pair
+    long long U = 0, ua = 0;
+    int c0 = 0, n_pieces;
+    if (P.ustart) {
+        U = P.ustart[P.n_items];
+        ua = P.ustart[item];
+        const long long ub = P.ustart[item + 1];
+        if (ub <= ua) return;
+        c0 = (int)(((ua + 1) * n_cta - 1) / U);  // the CTA whose share holds unit ua
+        const int c1 = (int)((ub * n_cta - 1) / U);
+        if (c1 == c0) return;
+        n_pieces = c1 - c0 + 1;
+    } else {
+        n_pieces = P.splits;
+    }
+    auto piece = [&](int k) -> const float* {
+        size_t slot;
+        if (P.ustart) {
+            // with fewer key tiles than CTAs some shares are empty: skip them
+            const int c = c0 + k;
+            const long long s0 = U * c / n_cta, s1 = U * (c + 1) / n_cta;
+            if (s1 <= s0) return nullptr;
+            slot = (size_t)c * 2 + ((k == 0 && s0 < ua) ? 1 : 0);
+        } else {
+            int a, b;
+            piece_range(n_kt_all, k, P.splits, a, b);
+            if (b <= a) return nullptr;
+            slot = item * P.splits + k;
+        }
+        return P.part + ((slot * 2 + x) * 128 + r) * kPartStride;
+    };
     float M = -INFINITY;
-    for (int sp = 0; sp < P.splits; ++sp) {
-        int a, b;
-        piece_range(n_kt_all, sp, P.splits, a, b);
-        if (b > a) M = fmaxf(M, P.part[(((item * P.splits + sp) * 2 + x) * 128 + r) * kPartStride + 128]);
+    for (int k = 0; k < n_pieces; ++k) {
+        const float* src = piece(k);
+        if (src) M = fmaxf(M, src[128]);
     }
     float l = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sp = 0; sp < P.splits; ++sp) {
-        int a, b;
-        piece_range(n_kt_all, sp, P.splits, a, b);
-        if (b <= a) continue;
-        const float* src = P.part + (((item * P.splits + sp) * 2 + x) * 128 + r) * kPartStride;
+    for (int k = 0; k < n_pieces; ++k) {
+        const float* src = piece(k);
+        if (!src) continue;
         const float m = src[128];
         const float f = m == -INFINITY ? 0.f : pa::fast_exp2(m - M);
         l += src[129] * f;
@@ -582,7 +734,7 @@ pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int
 
 template <int G>
 int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtensorMap& tv, int n_seqs,
-                   int max_chunk_len, int n_rows, cudaStream_t stream) {
+                   int max_chunk_len, int n_rows, int n_cta, cudaStream_t stream) {
     auto kern = pa_prefill_tc_kernel<G>;
     static bool attr_done[64] = {false};
     int dev = 0;
@@ -595,14 +747,19 @@ int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtenso
     }
     constexpr int QT = kRows / G;
     const int n_qp = (max_chunk_len + 2 * QT - 1) / (2 * QT);
-    dim3 grid(n_qp * Pp.splits, Pp.n_kv_heads, n_seqs);
-    kern<<<grid, 320, kSmemBytes, stream>>>(Pp, tk, tv);
+    if (Pp.ustart) {  // balanced mode: plan, then one CTA per SM
+        pa_prefill_plan_kernel<G><<<1, 1024, 0, stream>>>(Pp);
+        kern<<<n_cta, 320, kSmemBytes, stream>>>(Pp, tk, tv);
+    } else {
+        dim3 grid(n_qp * Pp.splits, Pp.n_kv_heads, n_seqs);
+        kern<<<grid, 320, kSmemBytes, stream>>>(Pp, tk, tv);
+    }
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    if (Pp.splits <= 1) return PA_OK;
+    if (!Pp.ustart && Pp.splits <= 1) return PA_OK;
     // rows of all chunks: the merge finds each row's sequence in q_start_loc
     const long long warps = (long long)n_rows * Pp.n_heads;
     return pa_launch_pdl(pa_prefill_merge_kernel<G>, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, stream, Pp,
-                         n_seqs, n_rows, n_qp);
+                         n_seqs, n_rows, n_qp, n_cta);
 }
 
 }  // namespace
@@ -623,21 +780,15 @@ int pairs_per_seq(int G, int max_chunk_len) {
     return (max_chunk_len + 2 * QT - 1) / (2 * QT);
 }
 
-// Pieces per query-tile pair for splits = 0: one CTA runs per SM, so a grid
-// of fewer pairs than SMs leaves SMs idle; splitting each pair's key range
-// into S pieces (S = SMs / pairs, at most 8) puts them to work. A grid of a
-// wave or more is not split: measured on the mixed batch (256 pairs on 152
-// SMs), 2..8 pieces per pair ran 1-6% slower than none, as CTAs that share
-// the GPU with fewer others run faster and make up the partial last wave.
-int auto_splits(long long n_items) {
-    const int sms = sm_count();
-    if (sms <= 0 || n_items <= 0 || n_items * 2 > sms) return 1;
-    const long long S = sms / n_items;
-    return (int)(S > 8 ? 8 : S);
-}
-
 size_t part_bytes(long long n_items, int splits) {
     return splits > 1 ? (size_t)n_items * splits * 2 * 128 * kPartStride * sizeof(float) : 0;
+}
+
+// Balanced mode (splits = 0): one CTA per SM, each with two partial slots,
+// then the items' tile prefix (n_items + 1 entries).
+size_t balanced_part_bytes(int n_cta) { return (size_t)n_cta * 2 * 2 * 128 * kPartStride * sizeof(float); }
+size_t balanced_bytes(long long n_items, int n_cta) {
+    return balanced_part_bytes(n_cta) + (size_t)(n_items + 1) * sizeof(long long);
 }
 
 int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
@@ -663,9 +814,11 @@ int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_poo
     if (rows + kBS > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
     const int n_qp = pairs_per_seq(G, max_chunk_len);
     const long long n_items = (long long)n_qp * n_kv_heads * n_seqs;
-    if (splits == 0) splits = auto_splits(n_items);
-    if ((long long)n_qp * splits > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    const size_t need = part_bytes(n_items, splits);
+    if (n_items > 0x3fffffffLL) return PA_ERR_UNSUPPORTED;
+    const int n_cta = splits == 0 ? sm_count() : 0;
+    if (splits == 0 && n_cta <= 0) return PA_ERR_CUDA;
+    if ((long long)n_qp * (splits > 0 ? splits : 1) > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    const size_t need = splits == 0 ? balanced_bytes(n_items, n_cta) : part_bytes(n_items, splits);
     if (need > 0 && (!workspace || workspace_bytes < need || !pa_aligned16(workspace))) return PA_ERR_WORKSPACE;
     unsigned int* err = pa_device_error_ptr();
     if (!err) return PA_ERR_CUDA;
@@ -685,18 +838,22 @@ int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_poo
     Pp.max_blocks = max_blocks_per_seq;
     Pp.num_blocks = num_blocks;
     Pp.oob_row = (int)rows;
-    Pp.splits = splits;
+    Pp.splits = splits > 0 ? splits : 1;
     Pp.part = need ? static_cast<float*>(workspace) : nullptr;
+    Pp.ustart = splits == 0 ? reinterpret_cast<long long*>(static_cast<char*>(workspace) + balanced_part_bytes(n_cta))
+                            : nullptr;
+    Pp.n_items = (int)n_items;
+    Pp.n_qp = n_qp;
     Pp.err = err;
     // chunk rows bound for the merge grid (rows past the last chunk exit)
     const long long n_rows = (long long)n_seqs * max_chunk_len;
     if (n_rows > 0x7fffffffLL || n_rows * n_heads > 0x7fffffffLL * 4LL) return PA_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (G) {
-        case 1: return launch_prefill<1>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
-        case 2: return launch_prefill<2>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
-        case 4: return launch_prefill<4>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
-        default: return launch_prefill<8>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
+        case 1: return launch_prefill<1>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, n_cta, st);
+        case 2: return launch_prefill<2>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, n_cta, st);
+        case 4: return launch_prefill<4>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, n_cta, st);
+        default: return launch_prefill<8>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, n_cta, st);
     }
 }
 
@@ -710,7 +867,9 @@ extern "C" size_t pa_prefill_workspace_bytes(int n_seqs, int n_heads, int n_kv_h
     const int G = n_heads / n_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return 0;
     const long long n_items = (long long)pairs_per_seq(G, max_chunk_len) * n_kv_heads * n_seqs;
-    return part_bytes(n_items, splits == 0 ? auto_splits(n_items) : splits);
+    if (splits > 0) return part_bytes(n_items, splits);
+    const int n_cta = sm_count();
+    return n_cta > 0 ? balanced_bytes(n_items, n_cta) : 0;
 }
 
 extern "C" int pa_prefill_paged_ex(void* out, const void* q, const void* k_pool, const void* v_pool,

@@ -296,6 +296,11 @@ def test_prefill_workspace_formula_and_errors(capi):
     assert capi.pa_prefill_workspace_bytes(4, 32, 6, 512, 2) == 0   # group 32/6: not supported
     assert capi.pa_prefill_workspace_bytes(0, 32, 8, 512, 2) == 0
     assert capi.pa_prefill_workspace_bytes(4, 32, 8, 512, 65) == 0
+    # balanced (splits 0): two partial slots per SM plus the items' key-tile prefix; 0 with no device
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 0
+    want = sms * 2 * 2 * 128 * 132 * 4 + (pairs * 8 * 4 + 1) * 8 if sms else 0
+    assert capi.pa_prefill_workspace_bytes(4, 32, 8, 512, 0) == want
     p = C.c_void_p(4096)
     args = [C.c_void_p(8192), p, p, p, p, p, p, C.c_float(0.1), 32, 8, 128, 16, 2, 4, 512, 16]
     assert capi.pa_prefill_paged_ex(*args, 3, None, 0, None) == -3      # split needs a workspace

@@ -117,3 +117,20 @@ def test_prefill_mixed_workload_auto_split_sampled_rows(pk):
     for r, h in rows:
         assert_attention_close(got[r, h], ref[r, h], f"mixed split prefill row {(r, h)}")
     check_device_error(0)
+
+
+@pytest.mark.parametrize("seed,n_seqs,ctx_hi,len_hi", [(21, 24, 600, 150), (22, 7, 4000, 300)])
+def test_prefill_balanced_shares_cross_pairs(pk, seed, n_seqs, ctx_hi, len_hi):
+    """Balanced mode (splits 0) with more key tiles than CTAs: a CTA's share
+    starts inside one pair, may hold whole pairs, and ends inside another, so
+    both partial slots, direct outputs and multi-piece merges occur; uneven
+    sequences leave pairs past the shorter chunks empty."""
+    rng = np.random.default_rng(seed)
+    ctx = [int(c) for c in rng.integers(50, ctx_hi, n_seqs)]
+    lens = [int(min(c, n)) for c, n in zip(ctx, rng.integers(1, len_hi, n_seqs))]
+    wl = make_prefill_case(seed, ctx, lens, [], 16, 8, 128)
+    got = _run(pk, wl, 0)
+    ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
+    assert_attention_close(got, ref, f"prefill balanced seed={seed}")
+    check_device_error(0)
