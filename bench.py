@@ -424,12 +424,13 @@ def run_ours(args):
         pf_avg = sum(pf_ms) / len(pf_ms)
         tpk, tpk_kind = measured_tensor_peak()
         result["config"]["step"] = ("pa_reshape_and_cache (decode tokens + chunk tokens) + "
-                                    "pa_prefill_paged (tcgen05) + pa_decode")
+                                    "pa_prefill_paged_ex (tcgen05, balanced) + pa_decode")
         result["config"]["prefill_flop_per_step"] = pf_flops
-        result["config"]["prefill_splits"] = ("auto: %d bytes of partials" % ws_pf.numel()
+        result["config"]["prefill_splits"] = ("balanced (0): %d bytes of workspace" % ws_pf.numel()
                                               if ws_pf is not None else 1)
         result["prefill_roofline"] = {
-            "bound": "tensor", "kernel": "pa_prefill_tc_kernel (+ pa_prefill_merge_kernel when split)",
+            "bound": "tensor",
+            "kernel": "pa_prefill_plan_kernel + pa_prefill_tc_kernel (one CTA per SM) + pa_prefill_merge_kernel",
             "achieved": round(pf_flops / (pf_avg / 1e3) / 1e12, 1), "peak": tpk,
             "peak_source": tpk_kind, "unit": "TFLOP/s",
             "frac": round(pf_flops / (pf_avg / 1e3) / 1e12 / tpk, 4),

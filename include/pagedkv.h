@@ -313,9 +313,10 @@ int pa_prefill_paged(void* out, const void* q, const void* k_pool, const void* v
  * Each piece keeps its un-normalised output, reference maximum and sum in
  * the workspace; a merge kernel combines the pieces (O = sum_p O_p 2^(m_p -
  * M), l = sum_p l_p 2^(m_p - M), out = O / l).
- *  splits     0 = balanced: a small planning kernel counts every pair's key
- *             tiles, and one CTA per SM takes an equal share of all of them
- *             in order (a pair cut by a share boundary becomes pieces);
+ *  splits     0 = balanced: a small planning kernel lists the pairs with
+ *             rows; all but the last partial wave's run whole, those of the
+ *             last partial wave are cut into a few equal key ranges, and one
+ *             CTA per SM takes list entries in order from a counter;
  *             1 = no split (no workspace needed); 2..64 = every pair cut
  *             into that many equal pieces
  *  workspace  DEVICE memory, 16-byte aligned, of at least

@@ -79,14 +79,19 @@ struct PrefillParams {
     int num_blocks;
     int oob_row;  // a TMA row coordinate past the end of the pool (zero fill)
     int splits;   // per-pair mode: pieces per query-tile pair (1: no split)
-    float* part;  // partials of pieces: [item][piece] (per-pair mode) or [CTA][2] (balanced mode),
+    float* part;  // partials of pieces: [item][piece] (per-pair mode) or [slot] (balanced mode),
                   // each [tile][row][kPartStride]
-    // balanced mode (null in per-pair mode): ustart[it] = key tiles of the
-    // items before item it, it = (sequence * n_kv_heads + kv head) * n_qp + pair;
-    // ustart[n_items] = all key tiles
-    long long* ustart;
+    // Balanced mode (work null in per-pair mode). Item it = (sequence *
+    // n_kv_heads + kv head) * n_qp + pair. The planning kernel writes the
+    // work list: every non-empty item whole, in item order, except the items
+    // of the last partial wave, which are cut into sched[2] equal key ranges
+    // (piece-major); CTAs take entries in order from the counter sched[0].
+    int4* work;      // entries (item, first key tile, end key tile, partial slot or -1); sched[1] of them
+    int* item_slot;  // [n_items] first partial slot of a cut item, -1 otherwise
+    int* sched;      // counter, entries, pieces per cut item
     int n_items;
     int n_qp;
+    int n_cta;
     unsigned int* err;
 };
 
@@ -154,17 +159,9 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         return;
     }
     // Segments. Per-pair mode: piece sp of pair (qp, kv head, sequence) from
-    // the grid position. Balanced mode: an equal share [u, u_end) of the key
-    // tiles of all items in order; each segment is the part of one item in
-    // it. Only a CTA's first and last segments can be partial items; their
-    // partials go to the CTA's slots 0 and 1.
-    long long u = 0, u_end = 0;
-    if (P.ustart) {
-        const long long U = P.ustart[P.n_items];
-        u = U * blockIdx.x / gridDim.x;
-        u_end = U * (blockIdx.x + 1) / gridDim.x;
-    }
-    const long long u_begin = u;
+    // the grid position. Balanced mode: the work-list entries this CTA takes
+    // from the counter, one at a time.
+    int* next = reinterpret_cast<int*>(sm + kMisc + 8);  // [2] the entry taken, by segment parity
     bool have_tmem = false;
     uint32_t tbase = 0;
     int n_run = 0;  // segments run so far
@@ -172,23 +169,19 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         int s, kvh, qp, kt0 = 0, kt1 = 0;
         bool direct = true;
         float* part_base = nullptr;
-        if (P.ustart) {
-            if (u >= u_end) break;
-            int lo = 0, hi = P.n_items - 1;  // the item holding unit u: the last with ustart <= u
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (P.ustart[mid] <= u) lo = mid;
-                else hi = mid - 1;
-            }
-            const long long ua = P.ustart[lo], ub = P.ustart[lo + 1], ue = ub < u_end ? ub : u_end;
-            kt0 = (int)(u - ua);
-            kt1 = (int)(ue - ua);
-            direct = u == ua && ue == ub;
-            part_base = P.part + (size_t)(blockIdx.x * 2 + (u == u_begin ? 0 : 1)) * 2 * 128 * kPartStride;
-            u = ue;
-            s = lo / (Hk * P.n_qp);
-            kvh = (lo / P.n_qp) % Hk;
-            qp = lo % P.n_qp;
+        if (P.work) {
+            if (threadIdx.x == 0) next[seg & 1] = atomicAdd(&P.sched[0], 1);
+            __syncthreads();
+            const int w = next[seg & 1];
+            if (w >= P.sched[1]) break;
+            const int4 e = P.work[w];
+            kt0 = e.y;
+            kt1 = e.z;
+            direct = e.w < 0;
+            if (!direct) part_base = P.part + (size_t)e.w * 2 * 128 * kPartStride;
+            s = e.x / (Hk * P.n_qp);
+            kvh = (e.x / P.n_qp) % Hk;
+            qp = e.x % P.n_qp;
         } else {
             if (seg > 0) break;
             qp = blockIdx.x / P.splits;
@@ -211,7 +204,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         // extra tiles beyond its own rows are fully masked)
         const int p_last = first_pos + min(i0 + 2 * QT, L) - 1;
         const int n_kt_all = p_last / kKT + 1;
-        if (!P.ustart) {  // this CTA's piece of the key tiles (all of them when not split)
+        if (!P.work) {  // this CTA's piece of the key tiles (all of them when not split)
             const int sp = blockIdx.x % P.splits;
             piece_range(n_kt_all, sp, P.splits, kt0, kt1);
             direct = P.splits <= 1;
@@ -614,45 +607,88 @@ __device__ int item_tiles(const PrefillParams& P, int it) {
     return (ctx - L + min(i0 + 2 * QT, L) - 1) / kKT + 1;
 }
 
-// Balanced mode: ustart = exclusive prefix sum of the items' key tiles, one
-// block of 1024 threads (each a run of consecutive items).
+// Balanced mode: the work list. One block of 1024 threads, each a run of
+// consecutive items. With P non-empty items and C CTAs (one per SM), the
+// first P - R items run whole (full waves, in item order so that the pairs of
+// one KV head run side by side and share their K/V tiles in L2); the last
+// R = P mod C items would fill only part of a wave, so each is cut into S
+// equal key ranges, S (1..8, R*S <= 4C) minimising ceil(R*S/C)/S + 0.03 S
+// (the wave fraction the tail takes plus a per-piece cost); its pieces are
+// listed piece-major, so the pieces running together again share key ranges.
 template <int G>
 __global__ void __launch_bounds__(1024) pa_prefill_plan_kernel(const PrefillParams P) {
-    __shared__ long long wsum[32];
+    __shared__ int wsum[32];
+    __shared__ int sh[3];  // P, R, S
     const int n = P.n_items, t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int per = (n + 1023) / 1024;
     const int b0 = min(n, t * per), b1 = min(n, b0 + per);
-    long long mine = 0;
-    for (int it = b0; it < b1; ++it) mine += item_tiles<G>(P, it);
-    long long incl = mine;  // inclusive prefix within the warp
+    int mine = 0;
+    for (int it = b0; it < b1; ++it) mine += item_tiles<G>(P, it) > 0;
+    int incl = mine;  // inclusive count within the warp
     for (int o = 1; o < 32; o <<= 1) {
-        const long long v = __shfl_up_sync(kFull, incl, o);
+        const int v = __shfl_up_sync(kFull, incl, o);
         if (lane >= o) incl += v;
     }
     if (lane == 31) wsum[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-        long long v = wsum[lane];
+        int v = wsum[lane];
         for (int o = 1; o < 32; o <<= 1) {
-            const long long y = __shfl_up_sync(kFull, v, o);
+            const int y = __shfl_up_sync(kFull, v, o);
             if (lane >= o) v += y;
         }
         wsum[lane] = v;  // inclusive over warps
     }
     __syncthreads();
-    long long base = incl - mine + (wid > 0 ? wsum[wid - 1] : 0);
-    for (int it = b0; it < b1; ++it) {
-        P.ustart[it] = base;
-        base += item_tiles<G>(P, it);
+    if (t == 0) {
+        const int np = wsum[31], C = P.n_cta;
+        int R = np % C, S = 1;
+        float best = 2.f;
+        for (int c = 1; c <= 8 && R * c <= 4 * C; ++c) {
+            const float cost = (float)((R * c + C - 1) / C) / c + 0.03f * c;
+            if (cost < best) {
+                best = cost;
+                S = c;
+            }
+        }
+        if (S == 1) R = 0;  // no cut: the tail runs whole
+        sh[0] = np;
+        sh[1] = R;
+        sh[2] = S;
+        P.sched[0] = 0;
+        P.sched[1] = np - R + R * S;
+        P.sched[2] = S;
     }
-    if (t == 1023) P.ustart[n] = base;
+    __syncthreads();
+    const int np = sh[0], R = sh[1], S = sh[2], whole = np - R;
+    int rank = incl - mine + (wid > 0 ? wsum[wid - 1] : 0);
+    for (int it = b0; it < b1; ++it) {
+        const int nk = item_tiles<G>(P, it);
+        if (nk <= 0) {
+            P.item_slot[it] = -1;
+            continue;
+        }
+        if (rank < whole) {
+            P.work[rank] = make_int4(it, 0, nk, -1);
+            P.item_slot[it] = -1;
+        } else {
+            const int ti = rank - whole;
+            for (int sp = 0; sp < S; ++sp) {
+                int a, b;
+                piece_range(nk, sp, S, a, b);
+                P.work[whole + sp * R + ti] = make_int4(it, a, b, ti * S + sp);
+            }
+            P.item_slot[it] = ti * S;
+        }
+        ++rank;
+    }
 }
 
 // Merges the pieces of a split query-tile pair: one warp per (chunk row, query
 // head). O = sum_p O_p 2^(m_p - M), l = sum_p l_p 2^(m_p - M), out = O / l.
 template <int G>
 __global__ void __launch_bounds__(128)
-pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int n_qp, int n_cta) {
+pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int n_qp) {
     constexpr int QT = kRows / G;
     pa::grid_dependency_wait();  // every piece's partial is written
     const long long w = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -675,38 +711,23 @@ pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int
     const int p_last = ctx - L + min(i0 + 2 * QT, L) - 1;
     const int n_kt_all = p_last / kKT + 1;
     const size_t item = ((size_t)s * Hk + kvh) * n_qp + qp;
-    // the pieces: per-pair mode, piece sp of `splits` (empty ones skipped);
-    // balanced mode, one per CTA c0..c1 whose share holds some of the pair's
-    // key tiles (c0 wrote it to its slot 1 unless the pair starts its share),
-    // none if one CTA ran the whole pair
-    long long U = 0, ua = 0;
-    int c0 = 0, n_pieces;
-    if (P.ustart) {
-        U = P.ustart[P.n_items];
-        ua = P.ustart[item];
-        const long long ub = P.ustart[item + 1];
-        if (ub <= ua) return;
-        c0 = (int)(((ua + 1) * n_cta - 1) / U);  // the CTA whose share holds unit ua
-        const int c1 = (int)((ub * n_cta - 1) / U);
-        if (c1 == c0) return;
-        n_pieces = c1 - c0 + 1;
+    // the pieces: piece sp of `splits` (per-pair mode) or of sched[2] for an
+    // item cut in balanced mode (none for an item that ran whole); empty
+    // pieces are skipped
+    int n_pieces, slot0;
+    if (P.work) {
+        slot0 = P.item_slot[item];
+        if (slot0 < 0) return;
+        n_pieces = P.sched[2];
     } else {
         n_pieces = P.splits;
+        slot0 = 0;
     }
     auto piece = [&](int k) -> const float* {
-        size_t slot;
-        if (P.ustart) {
-            // with fewer key tiles than CTAs some shares are empty: skip them
-            const int c = c0 + k;
-            const long long s0 = U * c / n_cta, s1 = U * (c + 1) / n_cta;
-            if (s1 <= s0) return nullptr;
-            slot = (size_t)c * 2 + ((k == 0 && s0 < ua) ? 1 : 0);
-        } else {
-            int a, b;
-            piece_range(n_kt_all, k, P.splits, a, b);
-            if (b <= a) return nullptr;
-            slot = item * P.splits + k;
-        }
+        int a, b;
+        piece_range(n_kt_all, k, n_pieces, a, b);
+        if (b <= a) return nullptr;
+        const size_t slot = P.work ? (size_t)slot0 + k : item * P.splits + k;
         return P.part + ((slot * 2 + x) * 128 + r) * kPartStride;
     };
     float M = -INFINITY;
@@ -734,7 +755,7 @@ pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int
 
 template <int G>
 int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtensorMap& tv, int n_seqs,
-                   int max_chunk_len, int n_rows, int n_cta, cudaStream_t stream) {
+                   int max_chunk_len, int n_rows, cudaStream_t stream) {
     auto kern = pa_prefill_tc_kernel<G>;
     static bool attr_done[64] = {false};
     int dev = 0;
@@ -747,19 +768,19 @@ int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtenso
     }
     constexpr int QT = kRows / G;
     const int n_qp = (max_chunk_len + 2 * QT - 1) / (2 * QT);
-    if (Pp.ustart) {  // balanced mode: plan, then one CTA per SM
+    if (Pp.work) {  // balanced mode: plan, then one CTA per SM taking work-list entries
         pa_prefill_plan_kernel<G><<<1, 1024, 0, stream>>>(Pp);
-        kern<<<n_cta, 320, kSmemBytes, stream>>>(Pp, tk, tv);
+        kern<<<Pp.n_cta, 320, kSmemBytes, stream>>>(Pp, tk, tv);
     } else {
         dim3 grid(n_qp * Pp.splits, Pp.n_kv_heads, n_seqs);
         kern<<<grid, 320, kSmemBytes, stream>>>(Pp, tk, tv);
     }
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    if (!Pp.ustart && Pp.splits <= 1) return PA_OK;
+    if (!Pp.work && Pp.splits <= 1) return PA_OK;
     // rows of all chunks: the merge finds each row's sequence in q_start_loc
     const long long warps = (long long)n_rows * Pp.n_heads;
     return pa_launch_pdl(pa_prefill_merge_kernel<G>, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, stream, Pp,
-                         n_seqs, n_rows, n_qp, n_cta);
+                         n_seqs, n_rows, n_qp);
 }
 
 }  // namespace
@@ -784,11 +805,20 @@ size_t part_bytes(long long n_items, int splits) {
     return splits > 1 ? (size_t)n_items * splits * 2 * 128 * kPartStride * sizeof(float) : 0;
 }
 
-// Balanced mode (splits = 0): one CTA per SM, each with two partial slots,
-// then the items' tile prefix (n_items + 1 entries).
-size_t balanced_part_bytes(int n_cta) { return (size_t)n_cta * 2 * 2 * 128 * kPartStride * sizeof(float); }
-size_t balanced_bytes(long long n_items, int n_cta) {
-    return balanced_part_bytes(n_cta) + (size_t)(n_items + 1) * sizeof(long long);
+// Balanced mode (splits = 0): partial slots for the cut items (at most 4
+// per CTA), the work list (n_items + 4 * n_cta entries), the item slots and
+// the counters, each part 16-byte aligned.
+struct BalancedLayout {
+    size_t part, work, item_slot, sched, total;
+};
+BalancedLayout balanced_layout(long long n_items, int n_cta) {
+    BalancedLayout b;
+    b.part = 0;
+    b.work = (size_t)4 * n_cta * 2 * 128 * kPartStride * sizeof(float);
+    b.item_slot = b.work + (size_t)(n_items + 4LL * n_cta) * sizeof(int4);
+    b.sched = b.item_slot + (((size_t)n_items * sizeof(int) + 15) & ~(size_t)15);
+    b.total = b.sched + 16;
+    return b;
 }
 
 int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
@@ -818,7 +848,7 @@ int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_poo
     const int n_cta = splits == 0 ? sm_count() : 0;
     if (splits == 0 && n_cta <= 0) return PA_ERR_CUDA;
     if ((long long)n_qp * (splits > 0 ? splits : 1) > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    const size_t need = splits == 0 ? balanced_bytes(n_items, n_cta) : part_bytes(n_items, splits);
+    const size_t need = splits == 0 ? balanced_layout(n_items, n_cta).total : part_bytes(n_items, splits);
     if (need > 0 && (!workspace || workspace_bytes < need || !pa_aligned16(workspace))) return PA_ERR_WORKSPACE;
     unsigned int* err = pa_device_error_ptr();
     if (!err) return PA_ERR_CUDA;
@@ -840,20 +870,29 @@ int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_poo
     Pp.oob_row = (int)rows;
     Pp.splits = splits > 0 ? splits : 1;
     Pp.part = need ? static_cast<float*>(workspace) : nullptr;
-    Pp.ustart = splits == 0 ? reinterpret_cast<long long*>(static_cast<char*>(workspace) + balanced_part_bytes(n_cta))
-                            : nullptr;
+    Pp.work = nullptr;
+    Pp.item_slot = nullptr;
+    Pp.sched = nullptr;
+    if (splits == 0) {
+        const BalancedLayout bl = balanced_layout(n_items, n_cta);
+        char* w = static_cast<char*>(workspace);
+        Pp.work = reinterpret_cast<int4*>(w + bl.work);
+        Pp.item_slot = reinterpret_cast<int*>(w + bl.item_slot);
+        Pp.sched = reinterpret_cast<int*>(w + bl.sched);
+    }
     Pp.n_items = (int)n_items;
     Pp.n_qp = n_qp;
+    Pp.n_cta = n_cta;
     Pp.err = err;
     // chunk rows bound for the merge grid (rows past the last chunk exit)
     const long long n_rows = (long long)n_seqs * max_chunk_len;
     if (n_rows > 0x7fffffffLL || n_rows * n_heads > 0x7fffffffLL * 4LL) return PA_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (G) {
-        case 1: return launch_prefill<1>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, n_cta, st);
-        case 2: return launch_prefill<2>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, n_cta, st);
-        case 4: return launch_prefill<4>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, n_cta, st);
-        default: return launch_prefill<8>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, n_cta, st);
+        case 1: return launch_prefill<1>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
+        case 2: return launch_prefill<2>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
+        case 4: return launch_prefill<4>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
+        default: return launch_prefill<8>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
     }
 }
 
@@ -869,7 +908,7 @@ extern "C" size_t pa_prefill_workspace_bytes(int n_seqs, int n_heads, int n_kv_h
     const long long n_items = (long long)pairs_per_seq(G, max_chunk_len) * n_kv_heads * n_seqs;
     if (splits > 0) return part_bytes(n_items, splits);
     const int n_cta = sm_count();
-    return n_cta > 0 ? balanced_bytes(n_items, n_cta) : 0;
+    return n_cta > 0 ? balanced_layout(n_items, n_cta).total : 0;
 }
 
 extern "C" int pa_prefill_paged_ex(void* out, const void* q, const void* k_pool, const void* v_pool,
