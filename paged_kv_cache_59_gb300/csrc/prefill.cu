@@ -27,16 +27,23 @@
 //     thread execute in issue order, so S_X(j+1) is issued right behind the
 //     PV MMA that still reads P(j) out of the same columns;
 //   - one softmax warpgroup per query tile (thread = row) reads S_X from
-//     tensor memory (once whole for the row maximum, then by halves for the
-//     exponentials), applies the scale, the causal mask and an online
-//     softmax in fp32 (base 2) with a lazily updated maximum (O_X is
-//     rescaled in tensor memory only when a row's maximum grows by more than
-//     8, so un-normalised p <= 2^8), and writes P back into S_X's columns as
-//     two bf16 terms, P = P_hi + P_lo (P_lo = the rounding residual),
-//     consumed by two MMAs. A single bf16 P costs up to ~2^-9 relative per
-//     weight, which on short causal rows with cancelling values exceeds an
-//     absolute error of 2e-3; the two-term P is accurate to ~2^-16.
+//     tensor memory twice, a quarter of 32 columns at a time (row maximum,
+//     then exponentials), applies the scale, the causal mask (diagonal tiles
+//     only) and an online softmax in fp32 (base 2) with a lazily updated
+//     maximum (O_X is rescaled in tensor memory only when a row's maximum
+//     grows by more than 8, so un-normalised p <= 2^8), and writes P back
+//     into S_X's columns as two bf16 terms, P = P_hi + P_lo (P_hi = p
+//     truncated, P_lo = the remainder rounded), consumed by two MMAs. A
+//     single bf16 P costs up to ~2^-9 relative per weight, which on short
+//     causal rows with cancelling values exceeds an absolute error of 2e-3;
+//     the two-term P is accurate to ~2^-16.
 // The normalised output O / l is written once at the end.
+//
+// Scheduling. Per-pair mode: one CTA per (pair, KV head, sequence), or per
+// piece of its key range. Balanced mode: one CTA per SM takes entries of a
+// work list in order (whole pairs for the full waves, pieces of the pairs of
+// the last partial wave) and runs them one after another, re-initialising
+// its barriers between entries; pieces leave partials for a merge kernel.
 #include <type_traits>
 #include <cuda_bf16.h>
 #include <math.h>
