@@ -95,7 +95,7 @@ struct PrefillParams {
     // (piece-major); CTAs take entries in order from the counter sched[0].
     int4* work;      // entries (item, first key tile, end key tile, partial slot or -1); sched[1] of them
     int* item_slot;  // [n_items] first partial slot of a cut item, -1 otherwise
-    int* sched;      // counter, entries, pieces per cut item
+    int* sched;      // counter, entries, pieces per cut item, cut items
     int n_items;
     int n_qp;
     int n_cta;
@@ -665,6 +665,7 @@ __global__ void __launch_bounds__(1024) pa_prefill_plan_kernel(const PrefillPara
         P.sched[0] = 0;
         P.sched[1] = np - R + R * S;
         P.sched[2] = S;
+        P.sched[3] = R;
     }
     __syncthreads();
     const int np = sh[0], R = sh[1], S = sh[2], whole = np - R;
@@ -691,8 +692,64 @@ __global__ void __launch_bounds__(1024) pa_prefill_plan_kernel(const PrefillPara
     }
 }
 
-// Merges the pieces of a split query-tile pair: one warp per (chunk row, query
-// head). O = sum_p O_p 2^(m_p - M), l = sum_p l_p 2^(m_p - M), out = O / l.
+// Combines the pieces of one output row: O = sum_k O_k 2^(m_k - M),
+// l = sum_k l_k 2^(m_k - M), out = O / l (lane: 4 of the 128 dims). Piece k
+// covers key tiles piece_range(n_kt_all, k, n_pieces); empty ones wrote
+// nothing and are skipped. Lane k reads piece k's (m, l) (n_pieces <= 64),
+// then every piece's O slice is loaded in one batch.
+template <typename PartOf>
+__device__ __forceinline__ void merge_row(int n_pieces, int n_kt_all, PartOf part_of, int lane, uint16_t* out_row) {
+    float m_mine = -INFINITY, l_mine = 0.f;
+    for (int k = lane; k < n_pieces; k += 32) {
+        int a, b;
+        piece_range(n_kt_all, k, n_pieces, a, b);
+        if (b > a) {
+            const float2 ml = *reinterpret_cast<const float2*>(part_of(k) + 128);
+            if (ml.x > m_mine) {  // keep the larger reference; rescale the other sum
+                l_mine = l_mine * (m_mine == -INFINITY ? 0.f : pa::fast_exp2(m_mine - ml.x)) + ml.y;
+                m_mine = ml.x;
+            } else {
+                l_mine += ml.x == -INFINITY ? 0.f : ml.y * pa::fast_exp2(ml.x - m_mine);
+            }
+        }
+    }
+    float M = m_mine;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    float l = m_mine == -INFINITY ? 0.f : l_mine * pa::fast_exp2(m_mine - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < n_pieces; k0 += 8) {
+        float4 v[8];
+        float f[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int k = k0 + u;
+            int a = 0, b = 0;
+            if (k < n_pieces) piece_range(n_kt_all, k, n_pieces, a, b);
+            f[u] = 0.f;
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (b > a) {
+                const float* src = part_of(k);
+                const float m = src[128];
+                f[u] = m == -INFINITY ? 0.f : pa::fast_exp2(m - M);
+                v[u] = *reinterpret_cast<const float4*>(src + lane * 4);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            acc.x += v[u].x * f[u]; acc.y += v[u].y * f[u]; acc.z += v[u].z * f[u]; acc.w += v[u].w * f[u];
+        }
+    }
+    const float inv = 1.f / l;
+    uint2 pk;
+    pk.x = pa::float2_to_bf16x2(acc.x * inv, acc.y * inv);
+    pk.y = pa::float2_to_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(out_row + lane * 4) = pk;
+}
+
+// Per-pair mode with splits > 1: one warp per (chunk row, query head).
 template <int G>
 __global__ void __launch_bounds__(128)
 pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int n_qp) {
@@ -715,49 +772,34 @@ pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int
     if (i < 0 || i >= L || ctx < L) return;
     const int qp = i / (2 * QT), x = (i % (2 * QT)) / QT, r = (i % QT) * G + h % G, kvh = h / G;
     const int i0 = qp * 2 * QT;
-    const int p_last = ctx - L + min(i0 + 2 * QT, L) - 1;
-    const int n_kt_all = p_last / kKT + 1;
+    const int n_kt_all = (ctx - L + min(i0 + 2 * QT, L) - 1) / kKT + 1;
     const size_t item = ((size_t)s * Hk + kvh) * n_qp + qp;
-    // the pieces: piece sp of `splits` (per-pair mode) or of sched[2] for an
-    // item cut in balanced mode (none for an item that ran whole); empty
-    // pieces are skipped
-    int n_pieces, slot0;
-    if (P.work) {
-        slot0 = P.item_slot[item];
-        if (slot0 < 0) return;
-        n_pieces = P.sched[2];
-    } else {
-        n_pieces = P.splits;
-        slot0 = 0;
-    }
-    auto piece = [&](int k) -> const float* {
-        int a, b;
-        piece_range(n_kt_all, k, n_pieces, a, b);
-        if (b <= a) return nullptr;
-        const size_t slot = P.work ? (size_t)slot0 + k : item * P.splits + k;
-        return P.part + ((slot * 2 + x) * 128 + r) * kPartStride;
-    };
-    float M = -INFINITY;
-    for (int k = 0; k < n_pieces; ++k) {
-        const float* src = piece(k);
-        if (src) M = fmaxf(M, src[128]);
-    }
-    float l = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < n_pieces; ++k) {
-        const float* src = piece(k);
-        if (!src) continue;
-        const float m = src[128];
-        const float f = m == -INFINITY ? 0.f : pa::fast_exp2(m - M);
-        l += src[129] * f;
-        const float4 v = *reinterpret_cast<const float4*>(src + lane * 4);
-        o.x += v.x * f; o.y += v.y * f; o.z += v.z * f; o.w += v.w * f;
-    }
-    const float inv = 1.f / l;
-    uint2 pk;
-    pk.x = pa::float2_to_bf16x2(o.x * inv, o.y * inv);
-    pk.y = pa::float2_to_bf16x2(o.z * inv, o.w * inv);
-    *reinterpret_cast<uint2*>(P.out + ((size_t)t * H + h) * kD + lane * 4) = pk;
+    merge_row(P.splits, n_kt_all,
+              [&](int k) { return P.part + (((item * P.splits + k) * 2 + x) * 128 + r) * kPartStride; }, lane,
+              P.out + ((size_t)t * H + h) * kD);
+}
+
+// Balanced mode: one warp per (row, head) of the cut pairs, warp w = 256 *
+// (cut pair) + 128 * (query tile) + (tile row); the cut pairs are the
+// piece-0 entries of the work list's tail.
+template <int G>
+__global__ void __launch_bounds__(128) pa_prefill_merge_cut_kernel(const PrefillParams P) {
+    constexpr int QT = kRows / G;
+    pa::grid_dependency_wait();  // every piece's partial is written
+    const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    const int S = P.sched[2], R = P.sched[3];
+    const int t = w >> 8, x = (w >> 7) & 1, r = w & 127;
+    if (t >= R) return;
+    const int item = P.work[P.sched[1] - R * S + t].x;
+    const int Hk = P.n_kv_heads;
+    const int s = item / (Hk * P.n_qp), kvh = (item / P.n_qp) % Hk, qp = item % P.n_qp;
+    const int q0 = P.qsl[s], L = P.qsl[s + 1] - q0, ctx = P.ctx[s];
+    const int i0 = qp * 2 * QT, i = i0 + x * QT + r / G;
+    if (i >= L) return;
+    const int n_kt_all = (ctx - L + min(i0 + 2 * QT, L) - 1) / kKT + 1;
+    const size_t slot0 = (size_t)t * S;
+    merge_row(S, n_kt_all, [&](int k) { return P.part + (((slot0 + k) * 2 + x) * 128 + r) * kPartStride; }, lane,
+              P.out + ((size_t)(q0 + i) * P.n_heads + kvh * G + r % G) * kD);
 }
 
 template <int G>
@@ -783,7 +825,10 @@ int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtenso
         kern<<<grid, 320, kSmemBytes, stream>>>(Pp, tk, tv);
     }
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    if (!Pp.work && Pp.splits <= 1) return PA_OK;
+    if (Pp.work)  // the cut pairs (fewer than one per CTA): 256 rows each
+        return pa_launch_pdl(pa_prefill_merge_cut_kernel<G>, dim3((unsigned)Pp.n_cta * 64), dim3(128), 0, stream,
+                             Pp);
+    if (Pp.splits <= 1) return PA_OK;
     // rows of all chunks: the merge finds each row's sequence in q_start_loc
     const long long warps = (long long)n_rows * Pp.n_heads;
     return pa_launch_pdl(pa_prefill_merge_kernel<G>, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, stream, Pp,
