@@ -134,3 +134,37 @@ def test_prefill_balanced_shares_cross_pairs(pk, seed, n_seqs, ctx_hi, len_hi):
     ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
     assert_attention_close(got, ref, f"prefill balanced seed={seed}")
     check_device_error(0)
+
+
+@pytest.mark.parametrize("splits", [None, 0])
+def test_prefill_chunk_not_in_cache_is_flagged_and_spares_others(pk, splits):
+    """A sequence whose context is shorter than its chunk sets PA_DEVERR_CONTEXT,
+    writes nothing, and leaves the other sequence's rows exact (per-pair and
+    balanced scheduling)."""
+    wl = make_prefill_case(941, [300, 40], [37, 20], [], 32, 8, 128)
+    ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    rows = [(r, h) for r in range(37) for h in range(32)]
+    ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale, rows=rows)
+    wl.pf_ctx = wl.pf_ctx.copy()
+    wl.pf_ctx[1] = 10                                   # 20 chunk rows, 10 cached tokens
+    got = _run(pk, wl, splits)
+    for r, h in rows:
+        assert_attention_close(got[r, h], ref[r, h], f"row {(r, h)}")
+    assert (got[37:] == 0x7FC0).all()                   # untouched (the pre-filled NaN pattern)
+    check_device_error(16)                              # PA_DEVERR_CONTEXT
+
+
+@pytest.mark.parametrize("splits", [None, 0])
+def test_prefill_bad_block_id_is_flagged_not_faulted(pk, splits):
+    """A block-table entry outside the pool sets PA_DEVERR_BLOCK_ID; that block
+    loads as zeros and the other sequence's rows stay exact."""
+    wl = make_prefill_case(942, [300, 500], [37, 64], [], 32, 8, 128)
+    ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    rows = [(r, h) for r in range(37) for h in range(32)]
+    ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale, rows=rows)
+    wl.pf_tables = wl.pf_tables.copy()
+    wl.pf_tables[1, 3] = wl.num_blocks + 5             # sequence 1, tokens 48..63
+    got = _run(pk, wl, splits)
+    for r, h in rows:
+        assert_attention_close(got[r, h], ref[r, h], f"row {(r, h)}")
+    check_device_error(1)                               # PA_DEVERR_BLOCK_ID
