@@ -491,7 +491,10 @@ pa_decode_partition_kernel(const DecodeParams P) {
 
 namespace {
 
-// Split-K merge: one warp per (sequence, query head) row.
+// Split-K merge: one warp per (sequence, query head) row. Lane p reads the
+// (m, l) of partitions p, p+32, ...; a warp reduction gives M and L; then the
+// partitions' output slices are loaded eight at a time, so a row costs two
+// rounds of memory latency rather than one per partition.
 template <int D>
 __global__ void __launch_bounds__(128)
 pa_decode_merge_kernel(const DecodeParams P, int n_rows) {
@@ -509,24 +512,50 @@ pa_decode_merge_kernel(const DecodeParams P, int n_rows) {
     const int nparts = min((nblk - blk_first + P.part_blocks - 1) / P.part_blocks, P.max_parts);
     if (nparts <= 1) return;  // the partition kernel wrote this row
     const size_t slot0 = (size_t)row * P.max_parts;
-    float M = -INFINITY;
-    for (int p = 0; p < nparts; ++p) M = fmaxf(M, P.ws_ml[(slot0 + p) * 2]);
-    float L = 0.f;
+    float m_mine = -INFINITY, l_mine = 0.f;  // this lane's partitions, relative to m_mine
+    for (int p = lane; p < nparts; p += 32) {
+        const float2 ml = *reinterpret_cast<const float2*>(P.ws_ml + (slot0 + p) * 2);
+        if (ml.x > m_mine) {
+            l_mine = (m_mine == -INFINITY ? 0.f : l_mine * pa::fast_exp2(m_mine - ml.x)) + ml.y;
+            m_mine = ml.x;
+        } else if (ml.x != -INFINITY) {
+            l_mine += ml.y * pa::fast_exp2(ml.x - m_mine);
+        }
+    }
+    float M = m_mine;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    float L = m_mine == -INFINITY ? 0.f : l_mine * pa::fast_exp2(m_mine - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
     float acc[PER];
 #pragma unroll
     for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-    for (int p = 0; p < nparts; ++p) {
-        const float2 ml = *reinterpret_cast<const float2*>(P.ws_ml + (slot0 + p) * 2);
-        const float f = pa::fast_exp2(ml.x - M);
-        L += ml.y * f;
-        const float* op = P.ws_o + (slot0 + p) * D + lane * PER;
-        if constexpr (PER == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(op);
-            acc[0] += v.x * f; acc[1] += v.y * f; acc[2] += v.z * f; acc[3] += v.w * f;
-        } else {
-            const float2 v = *reinterpret_cast<const float2*>(op);
-            acc[0] += v.x * f; acc[1] += v.y * f;
+    for (int p0 = 0; p0 < nparts; p0 += 8) {
+        float f[8], v[8][PER];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int p = p0 + u;
+            f[u] = 0.f;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) v[u][k] = 0.f;
+            if (p < nparts) {
+                const float m = P.ws_ml[(slot0 + p) * 2];
+                f[u] = m == -INFINITY ? 0.f : pa::fast_exp2(m - M);
+                const float* op = P.ws_o + (slot0 + p) * D + lane * PER;
+                if constexpr (PER == 4) {
+                    const float4 w = *reinterpret_cast<const float4*>(op);
+                    v[u][0] = w.x; v[u][1] = w.y; v[u][2] = w.z; v[u][3] = w.w;
+                } else {
+                    const float2 w = *reinterpret_cast<const float2*>(op);
+                    v[u][0] = w.x; v[u][1] = w.y;
+                }
+            }
         }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int k = 0; k < PER; ++k) acc[k] += v[u][k] * f[u];
     }
     const float inv = 1.f / L;
     uint32_t* dst = reinterpret_cast<uint32_t*>(P.out + (size_t)row * D + lane * PER);
