@@ -103,6 +103,21 @@ def measured_tensor_peak():
     return 1700.0, "fallback sustained bf16 TFLOP/s"
 
 
+def unique_kv_tokens(tables, ctx, window=None) -> int:
+    """Distinct (physical block, offset) slots attended by the batch: positions
+    0..ctx-1, or the last window+1 of them with a sliding window."""
+    import numpy as np
+    ids = []
+    for b, c in enumerate(ctx):
+        c = int(c)
+        first = max(0, c - 1 - window) if window is not None else 0
+        if c <= first:
+            continue
+        pos = np.arange(first, c)
+        ids.append(tables[b, pos // 16].astype(np.int64) * 16 + pos % 16)
+    return int(np.unique(np.concatenate(ids)).size) if ids else 0
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     for f in ("decode.cu", "pa_common.cuh"):
@@ -231,13 +246,16 @@ def run_ours(args):
     B = len(wl.dec_ctx)
     max_ctx = int(wl.dec_ctx.max())
     window = wl.meta.get("window")
+    # algorithmic KV bytes: the distinct cached tokens the batch attends to (a
+    # block shared by several tables, like a common prompt prefix, counts once)
+    uniq_tok = unique_kv_tokens(wl.dec_tables, wl.dec_ctx, window)
     if window is not None:   # tokens each query attends to: ctx-1-W .. ctx-1
         sum_ctx = int(sum(min(int(c), window + 1) for c in wl.dec_ctx))
     else:
         sum_ctx = int(wl.dec_ctx.sum())
     fp8 = wl.meta.get("kv_dtype") == "fp8_e4m3"
     eb = 1 if fp8 else 2                       # bytes per cached element
-    kv_bytes = sum_ctx * Hk * D * 2 * eb
+    kv_bytes = uniq_tok * Hk * D * 2 * eb
     alg_bytes = (kv_bytes + 2 * wl.q.nbytes + wl.dec_tables.nbytes + wl.dec_ctx.nbytes)
 
     def to_dev(a):
@@ -385,7 +403,8 @@ def run_ours(args):
         "config": {
             "workload": wl.name,
             "n_seqs": B, "n_heads": H, "n_kv_heads": Hk, "head_dim": D, "block_size": 16,
-            "sum_context_tokens": sum_ctx, "max_context": max_ctx, "num_blocks": wl.num_blocks,
+            "sum_context_tokens": sum_ctx, "distinct_cached_tokens_read": uniq_tok,
+            "max_context": max_ctx, "num_blocks": wl.num_blocks,
             "kv_bytes_per_step": kv_bytes,
             "step": ("pa_reshape_and_cache_fp8 (1 new token/seq, encoded) + pa_decode_fp8 (partition "
                      "kernel + split-K merge)" if fp8 else
