@@ -120,6 +120,11 @@ size_t pa_decode_workspace_bytes(int n_seqs, int n_heads, int head_dim,
  * Arithmetic: bf16 inputs, fp32 dot products, fp32 online softmax (base-2
  * exponent with scale*log2(e) folded into q), fp32 split-K merge, bf16 output
  * rounded to nearest even.
+ * Kernels: groups of up to 4 query heads per KV head use warp-shuffle fp32 dot
+ * products on the CUDA cores. A group of 8 at head_dim 128 (bf16) would make
+ * that kernel bound by its FMA work, far below HBM speed, so it runs its two
+ * products as warp-level tensor-core MMAs (see pa_decode_tc), unless the pool
+ * has more than 2^31 - 16 rows of 16 tokens x KV heads.
  */
 int pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
               const int32_t* block_tables, const int32_t* context_lens, float scale,
@@ -129,6 +134,26 @@ int pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
 
 /* pa_decode with an explicit partition size (see pa_decode_workspace_bytes). */
 int pa_decode_ex(void* out, const void* q, const void* k_pool, const void* v_pool,
+                 const int32_t* block_tables, const int32_t* context_lens, float scale,
+                 int n_heads, int n_kv_heads, int head_dim, int block_size,
+                 int n_seqs, int max_blocks_per_seq, int max_context_len, int num_blocks,
+                 int partition_tokens, void* workspace, size_t workspace_bytes,
+                 pa_stream_t stream);
+
+/*
+ * pa_decode_ex on the tensor-core partition kernel at every group size. Each
+ * 16-token block's products are warp-level mma.sync instructions:
+ *     S[16 x 16] = Q[16 x 128] . K^T  (the group's G heads are the first G of
+ *                                      16 rows; the rest are zero)
+ *     O[16 x 128] += P . V            (P as two bf16 terms, P_hi = p
+ *                                      truncated and P_lo = the rounded rest)
+ * with fp32 accumulation. K and V tiles arrive by 2-D TMA in 128-byte-swizzled
+ * shared memory. Softmax, partitions, workspace, errors and the split-K merge
+ * are as for pa_decode_ex.
+ * Requires head_dim 128 and a pool of at most 2^31 - 16 rows (num_blocks *
+ * n_kv_heads * 16), else PA_ERR_UNSUPPORTED.
+ */
+int pa_decode_tc(void* out, const void* q, const void* k_pool, const void* v_pool,
                  const int32_t* block_tables, const int32_t* context_lens, float scale,
                  int n_heads, int n_kv_heads, int head_dim, int block_size,
                  int n_seqs, int max_blocks_per_seq, int max_context_len, int num_blocks,

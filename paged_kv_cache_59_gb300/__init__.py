@@ -20,7 +20,7 @@ from . import _capi
 from ._capi import PagedKVError, check, load  # noqa: F401
 
 __all__ = [
-    "pa_decode", "pa_decode_workspace_bytes", "decode_workspace", "pa_decode_noalloc", "pa_reshape_and_cache",
+    "pa_decode", "pa_decode_tc", "pa_decode_workspace_bytes", "decode_workspace", "pa_decode_noalloc", "pa_reshape_and_cache",
     "pa_copy_blocks", "pa_prefill_paged", "pa_prefill_paged_ex", "pa_prefill_workspace_bytes",
     "prefill_workspace", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_window",
     "pa_swap_out_blocks", "pa_swap_in_blocks", "pa_get_device_error",
@@ -75,9 +75,11 @@ def decode_workspace(q, max_context_len: int, partition_tokens: int = 0):
 
 
 def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,
-              max_context_len: int, workspace=None, partition_tokens: int = 0, stream=None) -> None:
+              max_context_len: int, workspace=None, partition_tokens: int = 0, stream=None,
+              tensor_cores: bool = False) -> None:
     """out[b][h] = softmax(scale * q[b][h] . K_b^T) V_b over each sequence's
-    paged K/V. q, out: [n_seqs][n_heads][head_dim]."""
+    paged K/V. q, out: [n_seqs][n_heads][head_dim]. tensor_cores=True calls
+    pa_decode_tc (the warp-level MMA kernel at every group size)."""
     torch = _torch()
     n_seqs, n_heads, head_dim = q.shape
     num_blocks, n_kv_heads, block_size, hd2 = k_pool.shape
@@ -89,13 +91,21 @@ def pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,
     if workspace is not None:
         ws_ptr = _ptr(workspace, "workspace")
         ws_bytes = workspace.numel() * workspace.element_size()
-    st = load().pa_decode_ex(
+    lib = load()
+    st = (lib.pa_decode_tc if tensor_cores else lib.pa_decode_ex)(
         _ptr(out, "out", bf16=True), _ptr(q, "q", bf16=True), _ptr(k_pool, "k_pool", bf16=True),
         _ptr(v_pool, "v_pool", bf16=True), _ptr(block_tables, "block_tables", dtype=torch.int32),
         _ptr(context_lens, "context_lens", dtype=torch.int32), float(scale), n_heads, n_kv_heads,
         head_dim, block_size, n_seqs, block_tables.shape[1], int(max_context_len), num_blocks,
         int(partition_tokens), ws_ptr, ws_bytes, _stream(stream))
-    check("pa_decode", st)
+    check("pa_decode_tc" if tensor_cores else "pa_decode", st)
+
+
+def pa_decode_tc(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,
+                 max_context_len: int, workspace=None, partition_tokens: int = 0, stream=None) -> None:
+    """pa_decode on the tensor-core (warp-level MMA) partition kernel, any group size."""
+    pa_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale, max_context_len, workspace,
+              partition_tokens, stream, tensor_cores=True)
 
 
 def pa_decode_noalloc(out, q, k_pool, v_pool, block_tables, context_lens, scale: float,

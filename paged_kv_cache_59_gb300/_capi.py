@@ -41,6 +41,8 @@ SIGNATURES = {
                         vp, C.c_size_t, vp]),
     "pa_decode_ex": (i32, [vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32, i32,
                            i32, vp, C.c_size_t, vp]),
+    "pa_decode_tc": (i32, [vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32, i32,
+                           i32, vp, C.c_size_t, vp]),
     "pa_decode_noalloc": (i32, [vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32,
                                 i32, vp]),
     "pa_reshape_and_cache": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),

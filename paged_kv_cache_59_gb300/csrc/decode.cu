@@ -38,6 +38,7 @@
 #include <math.h>
 
 #include "pa_common.cuh"
+#include "tc_sm100.cuh"
 
 namespace {
 
@@ -487,6 +488,297 @@ pa_decode_partition_kernel(const DecodeParams P) {
     }
 }
 
+// ------------------------------------------------------------------------
+// Tensor-core variant of the partition kernel for large query groups
+// (head_dim 128, bf16 cache). With G = 8 query heads per KV head the CUDA-core
+// kernel above needs 255 registers, runs 8 warps per SM and is bound by its
+// FMA work, not by HBM. Here each tile's two products are warp-level
+// mma.sync tensor-core instructions (M = 16 rows, of which the G query heads
+// are the first G; N = 8; K = 16): a tile costs 16 + 32 of them instead of
+// ~1,000 FMA and shuffle instructions. tcgen05 needs M >= 64, which would
+// waste 7/8 of every instruction on padding rows for this shape.
+//   S[16 x 16 tokens] = Q[16 x 128] . K^T   (A = q in registers, B = K via ldmatrix)
+//   O[16 x 128]      += P . V               (A = P, reused from S's accumulator
+//                                            layout; B = V via ldmatrix.trans)
+// P enters as two bf16 terms (P_hi = p truncated, P_lo = the rounded
+// remainder), as in the prefill, so the weights keep ~16 significant bits.
+// K and V tiles arrive by 2-D TMA in 128B-swizzled layout (16 rows x 64 dims
+// per box), so the ldmatrix row reads are free of bank conflicts.
+namespace mma {
+
+constexpr int kNW = 4;          // warps per CTA
+constexpr int kS = 2;           // stages per warp
+constexpr int kStage = 8192;    // K 4 KiB + V 4 KiB, each two 2 KiB boxes
+constexpr int kSmem = kNW * kS * kStage + kNW * kS * 8;
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// byte offset of (row, 8-element chunk `dims8` of 0..15) in a tile stored as
+// two 128B-swizzled boxes of 16 rows x 64 dims
+__device__ __forceinline__ uint32_t sw_off(int row, int dims8) {
+    return (uint32_t)((dims8 >> 3) * 2048 + row * 128 + (((dims8 & 7) ^ (row & 7)) << 4));
+}
+
+}  // namespace mma
+
+template <int G>
+__global__ void __launch_bounds__(mma::kNW * 32, 3)
+pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV) {
+    using namespace mma;
+    constexpr int D = 128, NW = kNW, S = kS;
+    static_assert(G <= 8, "query heads of a group fill the first G of 16 MMA rows");
+    extern __shared__ __align__(1024) unsigned char smem_mma[];
+    unsigned char* stages = smem_mma;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_mma + NW * S * kStage);
+
+    const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;  // MMA fragment row group and column pair
+    const int H = P.n_heads, Hk = P.n_kv_heads;
+    const int h0 = kvh * G;
+    pa::launch_dependents();
+    pa::grid_dependency_wait();
+    if (pa::smem_u32(smem_mma) & 1023u) {  // never expected; refuse rather than mis-swizzle
+        if (threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_LAYOUT);
+        return;
+    }
+    const int ctx = P.ctx[b];
+    if (ctx <= 0) {  // empty sequence: zero output rows, written once
+        if (p == 0) {
+            for (int e = threadIdx.x; e < G * D / 2; e += NW * 32) {
+                int h = e / (D / 2), d2 = e % (D / 2);
+                reinterpret_cast<uint32_t*>(P.out + ((size_t)b * H + h0 + h) * D)[d2] = 0u;
+            }
+        }
+        return;
+    }
+    int nblk = (ctx + kBS - 1) / kBS;
+    const int first_pos = first_position(P, ctx);
+    int blk_first = first_pos / kBS;
+    int nparts = (nblk - blk_first + P.part_blocks - 1) / P.part_blocks;
+    if (nblk > P.max_blocks || nparts > P.max_parts) {  // caller broke the bounds it passed
+        if (p == 0 && threadIdx.x == 0) pa::set_error(P.err, PA_DEVERR_CONTEXT);
+        nblk = min(nblk, P.max_blocks);
+        blk_first = min(blk_first, nblk);
+        nparts = min((nblk - blk_first + P.part_blocks - 1) / P.part_blocks, P.max_parts);
+        nblk = min(nblk, blk_first + nparts * P.part_blocks);
+    }
+    if (p >= nparts) return;
+    const int blk_begin = blk_first + p * P.part_blocks;
+    const int nb_local = min(blk_begin + P.part_blocks, nblk) - blk_begin;
+    const int my_n = nb_local > warp ? (nb_local - warp + NW - 1) / NW : 0;  // <= 32
+
+    unsigned char* my_stages = stages + (size_t)warp * S * kStage;
+    uint64_t* my_bars = bars + warp * S;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) pa::mbar_init(&my_bars[s], 1);
+        pa::fence_mbar_init();
+    }
+    __syncwarp();
+
+    int my_bid = -1;  // one block-table entry per lane: local block warp + NW*lane
+    if (lane < my_n) my_bid = P.tables[(size_t)b * P.max_blocks + blk_begin + warp + NW * lane];
+
+    const uint64_t pol = pa::l2_evict_first_policy();
+    auto issue = [&](int i) {  // all lanes call (shuffle); lanes 0..3 issue the four boxes
+        const int bid = __shfl_sync(kFull, my_bid, i);
+        const int st = i % S;
+        uint64_t* bar = &my_bars[st];
+        unsigned char* dst = my_stages + (size_t)st * kStage;
+        if (bid >= 0 && bid < P.num_blocks) {
+            if (lane == 0) pa::mbar_arrive_expect_tx(bar, kStage);
+            __syncwarp();
+            if (lane < 4) {  // lane: bit 1 = V, bit 0 = dims 64..127
+                const int y = (bid * Hk + kvh) * kBS;
+                tc::tma_load_2d_hint(dst + (lane >> 1) * 4096 + (lane & 1) * 2048, (lane >> 1) ? &tmV : &tmK,
+                                     (lane & 1) * 64, y, bar, pol);
+            }
+        } else if (lane == 0) {
+            pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
+            pa::mbar_arrive(bar);  // completes the phase with no data
+        }
+    };
+
+    // q as the A operand: rows g < G are the group's heads, rows g+8 are zero;
+    // per k-step of 16 dims a lane holds dims 2t, 2t+1 and 2t+8, 2t+9
+    uint32_t qa[8][2];
+    {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(P.q + ((size_t)b * H + h0 + (g < G ? g : 0)) * D);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            qa[ks][0] = g < G ? qrow[ks * 8 + t] : 0u;
+            qa[ks][1] = g < G ? qrow[ks * 8 + 4 + t] : 0u;
+        }
+    }
+    float o[16][4];  // O fragments: rows g (head g) and g+8 (padding), dims 8n + 2t, +1
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[n][k] = 0.f;
+    float m_used = -INFINITY, l_run = 0.f;  // row g, base-2 units; l over this lane's columns
+    const float sc = P.scale_log2;
+
+    for (int s = 0; s < S && s < my_n; ++s) issue(s);
+    int consumed = 0;
+    bool aborted = false;
+    for (int i = 0; i < my_n; ++i) {
+        const int st = i % S;
+        const bool ok = pa::mbar_wait(&my_bars[st], (uint32_t)((i / S) & 1), P.err);
+        if (__any_sync(kFull, !ok)) {
+            aborted = true;
+            break;
+        }
+        consumed = i + 1;
+        const int bid = __shfl_sync(kFull, my_bid, i);
+        if (bid >= 0 && bid < P.num_blocks) {
+            const uint32_t kb = pa::smem_u32(my_stages + (size_t)st * kStage), vb = kb + 4096;
+            const int tok0 = (blk_begin + warp + NW * i) * kBS;
+            // ---- S = Q K^T: two n-tiles of 8 tokens
+            float s_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int m = lane >> 3, row = 8 * (m >> 1) + (lane & 7), kh = m & 1;  // matrix: (token half, k half)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t b00, b01, b10, b11;
+                    ldsm_x4(kb + sw_off(row, 2 * ks + kh), b00, b01, b10, b11);
+                    mma16816(s_acc[0], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
+                    mma16816(s_acc[1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
+                }
+            }
+            // ---- online softmax of row g over the tile's 16 tokens (this lane: 2t, 2t+1, 8+2t, 9+2t)
+            float sv[4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int pos = tok0 + 8 * n + 2 * t + k;
+                    sv[2 * n + k] = (pos < ctx && pos >= first_pos) ? s_acc[n][k] * sc : -INFINITY;
+                }
+            float tmax = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+            tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
+            tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
+            if (tmax > m_used + 8.f) {  // lazy rescale: p <= 2^8 un-normalised
+                const float alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
+                l_run *= alpha;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    o[n][0] *= alpha;
+                    o[n][1] *= alpha;
+                }
+                m_used = tmax;
+            }
+            const float mref = m_used == -INFINITY ? 0.f : m_used;  // a row with no visible key yet
+            float pv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                pv[k] = pa::fast_exp2(sv[k] - mref);
+                l_run += pv[k];
+            }
+            // P as the A operand (rows g; rows g+8 zero): P_hi truncated, P_lo the rounded rest
+            uint32_t ph[2], pl[2];
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const uint32_t bx = __float_as_uint(pv[2 * n]), by = __float_as_uint(pv[2 * n + 1]);
+                ph[n] = __byte_perm(bx, by, 0x7632);
+                pl[n] = pa::float2_to_bf16x2(pv[2 * n] - __uint_as_float(bx & 0xffff0000u),
+                                             pv[2 * n + 1] - __uint_as_float(by & 0xffff0000u));
+            }
+            // V rows of the sequence's last, partial block past the context hold
+            // whatever the pool has there (p = 0 must not meet a NaN): zero them
+            if (ctx < tok0 + kBS) {
+                const int r0 = ctx - tok0;
+                unsigned char* vt = my_stages + (size_t)st * kStage + 4096;
+                for (int e = lane; e < (kBS - r0) * 32; e += 32)  // a row: 2 boxes x 128 B
+                    *reinterpret_cast<uint2*>(vt + ((e & 31) >> 4) * 2048 + (r0 + (e >> 5)) * 128 + (e & 15) * 8) =
+                        make_uint2(0u, 0u);
+                tc::fence_async_smem();  // before the stage's next TMA fill
+                __syncwarp();
+            }
+            // ---- O += P V: 16 n-tiles of 8 dims, k = the tile's 16 tokens
+            {
+                const int m = lane >> 3, row = 8 * (m & 1) + (lane & 7), dh = m >> 1;  // matrix: (token half, dim half)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t b0a, b1a, b0b, b1b;
+                    ldsm_x4_t(vb + sw_off(row, 2 * j + dh), b0a, b1a, b0b, b1b);
+                    mma16816(o[2 * j], ph[0], 0u, ph[1], 0u, b0a, b1a);
+                    mma16816(o[2 * j], pl[0], 0u, pl[1], 0u, b0a, b1a);
+                    mma16816(o[2 * j + 1], ph[0], 0u, ph[1], 0u, b0b, b1b);
+                    mma16816(o[2 * j + 1], pl[0], 0u, pl[1], 0u, b0b, b1b);
+                }
+            }
+        }
+        __syncwarp();
+        if (i + S < my_n) issue(i + S);
+    }
+    if (aborted) {
+        // drain copies still in flight (bounded) before the stage memory is reused
+        for (int i = consumed; i < my_n && i < consumed + S; ++i)
+            pa::mbar_wait(&my_bars[i % S], (uint32_t)((i / S) & 1), P.err, 10000000ull);
+    }
+    l_run += __shfl_xor_sync(kFull, l_run, 1);
+    l_run += __shfl_xor_sync(kFull, l_run, 2);
+
+    __syncthreads();  // every warp is done with its ring: reuse it for the merge
+    float* mo = reinterpret_cast<float*>(stages);  // [NW][G][D]
+    float* mm = mo + NW * G * D;                   // [NW][G] max
+    float* ml = mm + NW * G;                       // [NW][G] sum
+    if (g < G) {
+        float* dst = mo + ((size_t)warp * G + g) * D + 2 * t;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) *reinterpret_cast<float2*>(dst + 8 * n) = make_float2(o[n][0], o[n][1]);
+        if (t == 0) {
+            mm[warp * G + g] = m_used;
+            ml[warp * G + g] = l_run;
+        }
+    }
+    __syncthreads();
+
+    const bool single = (nparts == 1);
+    for (int e = threadIdx.x; e < G * D / 2; e += NW * 32) {
+        const int h = e / (D / 2), d = (e % (D / 2)) * 2;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * G + h]);
+        float L = 0.f, O0 = 0.f, O1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float f = (mm[w * G + h] == -INFINITY) ? 0.f : pa::fast_exp2(mm[w * G + h] - M);
+            L += ml[w * G + h] * f;
+            const float2 ov = *reinterpret_cast<const float2*>(mo + ((size_t)w * G + h) * D + d);
+            O0 += ov.x * f;
+            O1 += ov.y * f;
+        }
+        const size_t row = (size_t)b * H + h0 + h;
+        if (single) {
+            const float inv = 1.f / L;
+            reinterpret_cast<uint32_t*>(P.out + row * D)[d / 2] = pa::float2_to_bf16x2(O0 * inv, O1 * inv);
+        } else {
+            const size_t slot = row * P.max_parts + p;
+            *reinterpret_cast<float2*>(P.ws_o + slot * D + d) = make_float2(O0, O1);
+            if (d == 0) *reinterpret_cast<float2*>(P.ws_ml + slot * 2) = make_float2(M, L);
+        }
+    }
+}
+
 }  // namespace
 
 namespace {
@@ -615,6 +907,28 @@ int dispatch_group(int G, const DecodeParams& P, int n_seqs, cudaStream_t stream
     }
 }
 
+// The tensor-core partition kernel (head_dim 128, bf16 cache): K and V pools
+// as 2-D TMA maps of [num_blocks * n_kv_heads * 16 rows][128 dims].
+template <int G>
+int launch_partition_mma(const DecodeParams& P, int n_seqs, cudaStream_t stream) {
+    auto kern = pa_decode_mma_kernel<G>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, mma::kSmem) != cudaSuccess)
+            return PA_ERR_CUDA;
+        attr_done[dev] = true;
+    }
+    const uint64_t rows = (uint64_t)P.num_blocks * P.n_kv_heads * kBS;
+    CUtensorMap tk, tv;
+    if (!pa_make_tmap_2d_bf16(&tk, P.k_pool, 128, rows, 256, 64, kBS) ||
+        !pa_make_tmap_2d_bf16(&tv, P.v_pool, 128, rows, 256, 64, kBS))
+        return PA_ERR_CUDA;
+    dim3 grid(P.max_parts, P.n_kv_heads, n_seqs);
+    return pa_launch_pdl(kern, grid, dim3(mma::kNW * 32), mma::kSmem, stream, P, tk, tv);
+}
+
 constexpr int kDefaultPartitionTokens = 512;
 
 int resolve_partition_tokens(int pt) {
@@ -648,7 +962,7 @@ int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void
                 const int32_t* context_lens, float scale, int n_heads, int n_kv_heads, int head_dim,
                 int block_size, int n_seqs, int max_blocks_per_seq, int max_context_len, int num_blocks,
                 int window, int partition_tokens, void* workspace, size_t workspace_bytes,
-                pa_stream_t stream) {
+                pa_stream_t stream, bool force_tc = false) {
     if (n_seqs < 0 || max_context_len < 0 || num_blocks < 0 || max_blocks_per_seq < 0 ||
         n_heads <= 0 || n_kv_heads <= 0)
         return PA_ERR_INVALID_ARG;
@@ -658,6 +972,8 @@ int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void
     const int G = n_heads / n_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
     if (n_kv_heads > 65535 || n_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    const bool tc_rows_ok = (long long)num_blocks * n_kv_heads * kBS + kBS <= 0x7fffffffLL;  // TMA coordinates
+    if (force_tc && (eb != 2 || head_dim != 128 || !tc_rows_ok)) return PA_ERR_UNSUPPORTED;
     if ((long long)max_blocks_per_seq * kBS < (long long)max_context_len) return PA_ERR_INVALID_ARG;
     const int pt = resolve_partition_tokens(partition_tokens);
     if (pt < 0) return PA_ERR_INVALID_ARG;
@@ -708,7 +1024,18 @@ int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int st;
-    if (eb == 1)
+    // groups of 8 heads at head_dim 128 (bf16) run on the tensor cores, unless
+    // the pool has too many rows for a TMA coordinate; pa_decode_tc asks for
+    // the tensor-core kernel at every group size
+    const bool tensor = force_tc || (eb == 2 && head_dim == 128 && G == 8 && tc_rows_ok);
+    if (tensor) {
+        switch (G) {
+            case 1: st = launch_partition_mma<1>(P, n_seqs, s); break;
+            case 2: st = launch_partition_mma<2>(P, n_seqs, s); break;
+            case 4: st = launch_partition_mma<4>(P, n_seqs, s); break;
+            default: st = launch_partition_mma<8>(P, n_seqs, s); break;
+        }
+    } else if (eb == 1)
         st = head_dim == 128 ? dispatch_group<128, 1>(G, P, n_seqs, s) : dispatch_group<64, 1>(G, P, n_seqs, s);
     else
         st = head_dim == 128 ? dispatch_group<128, 2>(G, P, n_seqs, s) : dispatch_group<64, 2>(G, P, n_seqs, s);
@@ -731,6 +1058,18 @@ extern "C" int pa_decode_ex(void* out, const void* q, const void* k_pool, const 
                        n_heads, n_kv_heads, head_dim, block_size, n_seqs, max_blocks_per_seq,
                        max_context_len, num_blocks, -1, partition_tokens, workspace, workspace_bytes,
                        stream);
+}
+
+extern "C" int pa_decode_tc(void* out, const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, const int32_t* context_lens, float scale,
+                            int n_heads, int n_kv_heads, int head_dim, int block_size, int n_seqs,
+                            int max_blocks_per_seq, int max_context_len, int num_blocks,
+                            int partition_tokens, void* workspace, size_t workspace_bytes,
+                            pa_stream_t stream) {
+    return decode_impl(2, out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens, scale,
+                       n_heads, n_kv_heads, head_dim, block_size, n_seqs, max_blocks_per_seq,
+                       max_context_len, num_blocks, -1, partition_tokens, workspace, workspace_bytes,
+                       stream, true);
 }
 
 extern "C" int pa_decode_window(void* out, const void* q, const void* k_pool, const void* v_pool,

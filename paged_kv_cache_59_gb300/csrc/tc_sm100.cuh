@@ -144,6 +144,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* m
         : "memory");
 }
 
+// The same load with an L2 cache policy (e.g. evict-first for a stream read once).
+__device__ __forceinline__ void tma_load_2d_hint(void* dst_smem, const CUtensorMap* map, int x, int y,
+                                                 uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(pa::smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(pa::smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // Offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a
 // 128B-swizzled region whose rows are 128 bytes: chunks are permuted by
 // XOR with the row index modulo 8 (the pattern TMA and the tensor cores use

@@ -320,3 +320,12 @@ def test_prefill_argument_errors_need_no_device(capi):
     assert capi.pa_prefill_paged(*args, 8, 8, 128, 16, -1, 4, 64, 16, None) == -1
     assert capi.pa_prefill_paged(*args, 8, 8, 128, 16, 0, 4, 64, 16, None) == 0
     assert capi.pa_prefill_paged(C.c_void_p(4100), *args[1:], 8, 8, 128, 16, 2, 4, 64, 16, None) == -1
+
+
+def test_decode_tc_unsupported_shapes_need_no_device(capi):
+    p = C.c_void_p(4096)
+    args = [p, p, p, p, p, p, C.c_float(0.1)]
+    # head_dim 64 has no tensor-core kernel; a pool too large for int32 TMA rows
+    assert capi.pa_decode_tc(*args, 8, 8, 64, 16, 2, 4, 64, 16, 0, None, 0, None) == -2
+    assert capi.pa_decode_tc(*args, 8, 8, 128, 16, 2, 4, 64, 20000000, 0, None, 0, None) == -2
+    assert capi.pa_decode_tc(*args, 8, 8, 128, 16, 0, 4, 64, 16, 0, None, 0, None) == 0   # no sequences

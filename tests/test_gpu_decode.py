@@ -79,8 +79,9 @@ def test_long_context_partitions(pk, pt):
     check_device_error(0)
 
 
-def test_zero_context_rows_are_zero(pk):
-    wl = make_decode_case(300, [0, 20, 0, 33], 8, 2, 128)
+@pytest.mark.parametrize("H,Hk", [(8, 2), (64, 8)])   # group 8 at head_dim 128: tensor-core kernel
+def test_zero_context_rows_are_zero(pk, H, Hk):
+    wl = make_decode_case(300, [0, 20, 0, 33], H, Hk, 128)
     got = gpu_decode(pk, wl.q, dev(wl.k_pool), dev(wl.v_pool), wl.dec_tables, wl.dec_ctx,
                      wl.scale, 33, 64)
     assert np.all(got[0] == 0) and np.all(got[2] == 0)
@@ -88,9 +89,10 @@ def test_zero_context_rows_are_zero(pk):
     assert_attention_close(got, ref, "zero ctx")
 
 
-def test_hot_logits_do_not_overflow(pk):
+@pytest.mark.parametrize("H,Hk", [(8, 2), (64, 8)])
+def test_hot_logits_do_not_overflow(pk, H, Hk):
     """q scaled x20: logits of order +-100, exp without max-subtraction would overflow."""
-    wl = make_decode_case(301, [77, 500, 1], 8, 2, 128)
+    wl = make_decode_case(301, [77, 500, 1], H, Hk, 128)
     qf = bf16_to_f64(wl.q) * 20.0
     q_hot = ((qf.astype(np.float32).view(np.uint32) + 0x8000) >> 16).astype(np.uint16)
     got = gpu_decode(pk, q_hot, dev(wl.k_pool), dev(wl.v_pool), wl.dec_tables, wl.dec_ctx,
@@ -99,8 +101,9 @@ def test_hot_logits_do_not_overflow(pk):
     assert_attention_close(got, ref, "hot")
 
 
-def test_block_permutation_gives_identical_bits(pk):
-    wl = make_decode_case(302, [40, 300, 1000, 16], 32, 8, 128)
+@pytest.mark.parametrize("H,Hk", [(32, 8), (64, 8)])
+def test_block_permutation_gives_identical_bits(pk, H, Hk):
+    wl = make_decode_case(302, [40, 300, 1000, 16], H, Hk, 128)
     a = gpu_decode(pk, wl.q, dev(wl.k_pool), dev(wl.v_pool), wl.dec_tables, wl.dec_ctx,
                    wl.scale, 1000, 256)
     pi = np.random.default_rng(9).permutation(wl.num_blocks)
@@ -113,8 +116,9 @@ def test_block_permutation_gives_identical_bits(pk):
     assert np.array_equal(a, b)
 
 
-def test_bad_block_id_is_flagged_not_faulted(pk):
-    wl = make_decode_case(303, [40, 40], 4, 4, 64)
+@pytest.mark.parametrize("H,Hk,D", [(4, 4, 64), (64, 8, 128)])
+def test_bad_block_id_is_flagged_not_faulted(pk, H, Hk, D):
+    wl = make_decode_case(303, [40, 40], H, Hk, D)
     tabs = wl.dec_tables.copy()
     tabs[1, 1] = wl.num_blocks + 5
     got = gpu_decode(pk, wl.q, dev(wl.k_pool), dev(wl.v_pool), tabs, wl.dec_ctx, wl.scale, 40)
