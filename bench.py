@@ -120,7 +120,7 @@ def unique_kv_tokens(tables, ctx, window=None) -> int:
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cu", "pa_common.cuh"):
+    for f in ("decode.cu", "pa_common.cuh", "tc_sm100.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_59_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
