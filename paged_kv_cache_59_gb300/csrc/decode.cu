@@ -506,10 +506,19 @@ pa_decode_partition_kernel(const DecodeParams P) {
 // per box), so the ldmatrix row reads are free of bank conflicts.
 namespace mma {
 
-constexpr int kNW = 4;          // warps per CTA
-constexpr int kS = 2;           // stages per warp
-constexpr int kStage = 8192;    // K 4 KiB + V 4 KiB, each two 2 KiB boxes
-constexpr int kSmem = kNW * kS * kStage + kNW * kS * 8;
+constexpr int kNW = 4;  // warps per CTA
+constexpr int kS = 2;   // stages per warp
+// Per warp, bf16 cache: kS stages of K 4 KiB + V 4 KiB (each two 2 KiB boxes,
+// 16 rows x 64 dims). E4M3 cache: kS stages of K 2 KiB + V 2 KiB (one box of
+// 16 rows x 128 codes each) and one 4 KiB fp16 tile the V codes are widened
+// into (K's codes are widened in registers, straight from the stage).
+template <int EB>
+struct Lay {
+    static constexpr int kStage = EB == 2 ? 8192 : 4096;
+    static constexpr int kConv = EB == 2 ? 0 : 4096;
+    static constexpr int kWarp = kS * kStage + kConv;
+    static constexpr int kSmem = kNW * kWarp + kNW * kS * 8;
+};
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -518,6 +527,37 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// the same with fp16 operands (an E4M3 cache widened exactly to fp16)
+__device__ __forceinline__ void mma16816_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+template <int EB>
+__device__ __forceinline__ void mma_t(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    if constexpr (EB == 2) mma16816(c, a0, 0u, a2, 0u, b0, b1);
+    else mma16816_f16(c, a0, 0u, a2, 0u, b0, b1);
+}
+__device__ __forceinline__ uint32_t f2_to_h2(float a, float b) {  // fp16x2, a in the low half
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+__device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
+    float a, b;
+    asm("{\n\t.reg .f16 x, y;\n\tmov.b32 {x, y}, %2;\n\tcvt.f32.f16 %0, x;\n\tcvt.f32.f16 %1, y;\n\t}"
+        : "=f"(a), "=f"(b)
+        : "r"(h));
+    return make_float2(a, b);
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t c) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+    return r;
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -537,16 +577,17 @@ __device__ __forceinline__ uint32_t sw_off(int row, int dims8) {
 
 }  // namespace mma
 
-template <int G>
+template <int G, int EB>
 __global__ void __launch_bounds__(mma::kNW * 32, 3)
 pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
     using namespace mma;
     constexpr int D = 128, NW = kNW, S = kS;
+    constexpr int kStage = Lay<EB>::kStage, kWarp = Lay<EB>::kWarp;
     static_assert(G <= 8, "query heads of a group fill the first G of 16 MMA rows");
     extern __shared__ __align__(1024) unsigned char smem_mma[];
     unsigned char* stages = smem_mma;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_mma + NW * S * kStage);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_mma + NW * kWarp);
 
     const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -585,7 +626,8 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
     const int nb_local = min(blk_begin + P.part_blocks, nblk) - blk_begin;
     const int my_n = nb_local > warp ? (nb_local - warp + NW - 1) / NW : 0;  // <= 32
 
-    unsigned char* my_stages = stages + (size_t)warp * S * kStage;
+    unsigned char* my_stages = stages + (size_t)warp * kWarp;
+    unsigned char* my_conv = my_stages + S * kStage;  // E4M3 cache: the widened tile pair
     uint64_t* my_bars = bars + warp * S;
     if (lane == 0) {
 #pragma unroll
@@ -606,10 +648,14 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
         if (bid >= 0 && bid < P.num_blocks) {
             if (lane == 0) pa::mbar_arrive_expect_tx(bar, kStage);
             __syncwarp();
-            if (lane < 4) {  // lane: bit 1 = V, bit 0 = dims 64..127
-                const int y = (bid * Hk + kvh) * kBS;
-                tc::tma_load_2d_hint(dst + (lane >> 1) * 4096 + (lane & 1) * 2048, (lane >> 1) ? &tmV : &tmK,
-                                     (lane & 1) * 64, y, bar, pol);
+            const int y = (bid * Hk + kvh) * kBS;
+            if constexpr (EB == 2) {
+                if (lane < 4)  // lane: bit 1 = V, bit 0 = dims 64..127
+                    tc::tma_load_2d_hint(dst + (lane >> 1) * 4096 + (lane & 1) * 2048,
+                                         (lane >> 1) ? &tmV : &tmK, (lane & 1) * 64, y, bar, pol);
+            } else {
+                if (lane < 2)  // lane 1 = V; one box of 16 rows x 128 codes
+                    tc::tma_load_2d_hint(dst + lane * 2048, lane ? &tmV : &tmK, 0, y, bar, pol);
             }
         } else if (lane == 0) {
             pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
@@ -624,8 +670,18 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(P.q + ((size_t)b * H + h0 + (g < G ? g : 0)) * D);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            qa[ks][0] = g < G ? qrow[ks * 8 + t] : 0u;
-            qa[ks][1] = g < G ? qrow[ks * 8 + 4 + t] : 0u;
+            // bf16 cache: k = 2t, 2t+1 | 2t+8, 2t+9 are dims 16ks + 2t.. | 16ks + 2t + 8..; E4M3
+            // cache: the same k are dims 16ks + 4t, +1 | +2, +3, so that a lane's K codes are
+            // four consecutive bytes (the sum over the k-step is unchanged)
+            qa[ks][0] = g < G ? qrow[EB == 2 ? ks * 8 + t : ks * 8 + 2 * t] : 0u;
+            qa[ks][1] = g < G ? qrow[EB == 2 ? ks * 8 + 4 + t : ks * 8 + 2 * t + 1] : 0u;
+            if constexpr (EB == 1) {  // bf16 -> fp16 for the fp16 MMA (exact for |q| in the fp16 range)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float2 f = pa::bf16x2_to_float2(qa[ks][k]);
+                    qa[ks][k] = f2_to_h2(f.x, f.y);
+                }
+            }
         }
     }
     float o[16][4];  // O fragments: rows g (head g) and g+8 (padding), dims 8n + 2t, +1
@@ -634,7 +690,8 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
 #pragma unroll
         for (int k = 0; k < 4; ++k) o[n][k] = 0.f;
     float m_used = -INFINITY, l_run = 0.f;  // row g, base-2 units; l over this lane's columns
-    const float sc = P.scale_log2;
+    // E4M3 cache: q.(code*s_k) = s_k (q.code), folded into the score scale
+    const float sc = EB == 1 ? P.scale_log2 * P.k_scale[kvh] : P.scale_log2;
 
     for (int s = 0; s < S && s < my_n; ++s) issue(s);
     int consumed = 0;
@@ -649,19 +706,57 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
         consumed = i + 1;
         const int bid = __shfl_sync(kFull, my_bid, i);
         if (bid >= 0 && bid < P.num_blocks) {
-            const uint32_t kb = pa::smem_u32(my_stages + (size_t)st * kStage), vb = kb + 4096;
+            if constexpr (EB == 1) {
+                // widen the V codes into the fp16 tile (same swizzled layout as a bf16 tile):
+                // lane (row r = lane/2, half) takes 64 codes = 4 chunks of 16
+                const unsigned char* raw = my_stages + (size_t)st * kStage;
+                const int r = lane >> 1, hf = lane & 1;
+#pragma unroll
+                for (int kv = 1; kv < 2; ++kv) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int c = hf * 4 + j;  // 16-code chunk of the 128-code row
+                        const uint4 w = *reinterpret_cast<const uint4*>(raw + kv * 2048 + r * 128 +
+                                                                        ((c ^ (r & 7)) << 4));
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                        uint32_t h[8];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            h[2 * k] = e4m3x2_to_h2((uint16_t)(ws[k] & 0xffffu));
+                            h[2 * k + 1] = e4m3x2_to_h2((uint16_t)(ws[k] >> 16));
+                        }
+                        unsigned char* cv = my_conv;
+                        *reinterpret_cast<uint4*>(cv + sw_off(r, 2 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
+                        *reinterpret_cast<uint4*>(cv + sw_off(r, 2 * c + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+                    }
+                }
+            }
+            const uint32_t kb = pa::smem_u32(my_stages + (size_t)st * kStage);
+            const uint32_t vb = EB == 2 ? kb + 4096 : pa::smem_u32(my_conv);
             const int tok0 = (blk_begin + warp + NW * i) * kBS;
             // ---- S = Q K^T: two n-tiles of 8 tokens
             float s_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            {
+            if constexpr (EB == 2) {
                 const int m = lane >> 3, row = 8 * (m >> 1) + (lane & 7), kh = m & 1;  // matrix: (token half, k half)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t b00, b01, b10, b11;
                     ldsm_x4(kb + sw_off(row, 2 * ks + kh), b00, b01, b10, b11);
-                    mma16816(s_acc[0], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
-                    mma16816(s_acc[1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
+                    mma_t<EB>(s_acc[0], qa[ks][0], qa[ks][1], b00, b01);
+                    mma_t<EB>(s_acc[1], qa[ks][0], qa[ks][1], b10, b11);
                 }
+            } else {  // K codes of token row 8nt + g, dims 16ks + 4t .. +3, widened in registers
+                const unsigned char* rk = my_stages + (size_t)st * kStage;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int row = 8 * nt + g;
+                        const uint32_t w =
+                            *reinterpret_cast<const uint32_t*>(rk + row * 128 + ((ks ^ (row & 7)) << 4) + 4 * t);
+                        mma_t<EB>(s_acc[nt], qa[ks][0], qa[ks][1], e4m3x2_to_h2((uint16_t)(w & 0xffffu)),
+                                  e4m3x2_to_h2((uint16_t)(w >> 16)));
+                    }
             }
             // ---- online softmax of row g over the tile's 16 tokens (this lane: 2t, 2t+1, 8+2t, 9+2t)
             float sv[4];
@@ -696,16 +791,23 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
             uint32_t ph[2], pl[2];
 #pragma unroll
             for (int n = 0; n < 2; ++n) {
-                const uint32_t bx = __float_as_uint(pv[2 * n]), by = __float_as_uint(pv[2 * n + 1]);
-                ph[n] = __byte_perm(bx, by, 0x7632);
-                pl[n] = pa::float2_to_bf16x2(pv[2 * n] - __uint_as_float(bx & 0xffff0000u),
-                                             pv[2 * n + 1] - __uint_as_float(by & 0xffff0000u));
+                if constexpr (EB == 2) {
+                    const uint32_t bx = __float_as_uint(pv[2 * n]), by = __float_as_uint(pv[2 * n + 1]);
+                    ph[n] = __byte_perm(bx, by, 0x7632);
+                    pl[n] = pa::float2_to_bf16x2(pv[2 * n] - __uint_as_float(bx & 0xffff0000u),
+                                                 pv[2 * n + 1] - __uint_as_float(by & 0xffff0000u));
+                } else {  // fp16 terms: P_hi rounded, P_lo the rounded remainder
+                    ph[n] = f2_to_h2(pv[2 * n], pv[2 * n + 1]);
+                    const float2 hf = h2_to_f2(ph[n]);
+                    pl[n] = f2_to_h2(pv[2 * n] - hf.x, pv[2 * n + 1] - hf.y);
+                }
             }
+            if constexpr (EB == 1) __syncwarp();  // the widened V tile is complete
             // V rows of the sequence's last, partial block past the context hold
             // whatever the pool has there (p = 0 must not meet a NaN): zero them
             if (ctx < tok0 + kBS) {
                 const int r0 = ctx - tok0;
-                unsigned char* vt = my_stages + (size_t)st * kStage + 4096;
+                unsigned char* vt = EB == 2 ? my_stages + (size_t)st * kStage + 4096 : my_conv;
                 for (int e = lane; e < (kBS - r0) * 32; e += 32)  // a row: 2 boxes x 128 B
                     *reinterpret_cast<uint2*>(vt + ((e & 31) >> 4) * 2048 + (r0 + (e >> 5)) * 128 + (e & 15) * 8) =
                         make_uint2(0u, 0u);
@@ -719,10 +821,10 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
                 for (int j = 0; j < 8; ++j) {
                     uint32_t b0a, b1a, b0b, b1b;
                     ldsm_x4_t(vb + sw_off(row, 2 * j + dh), b0a, b1a, b0b, b1b);
-                    mma16816(o[2 * j], ph[0], 0u, ph[1], 0u, b0a, b1a);
-                    mma16816(o[2 * j], pl[0], 0u, pl[1], 0u, b0a, b1a);
-                    mma16816(o[2 * j + 1], ph[0], 0u, ph[1], 0u, b0b, b1b);
-                    mma16816(o[2 * j + 1], pl[0], 0u, pl[1], 0u, b0b, b1b);
+                    mma_t<EB>(o[2 * j], ph[0], ph[1], b0a, b1a);
+                    mma_t<EB>(o[2 * j], pl[0], pl[1], b0a, b1a);
+                    mma_t<EB>(o[2 * j + 1], ph[0], ph[1], b0b, b1b);
+                    mma_t<EB>(o[2 * j + 1], pl[0], pl[1], b0b, b1b);
                 }
             }
         }
@@ -766,6 +868,10 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
             const float2 ov = *reinterpret_cast<const float2*>(mo + ((size_t)w * G + h) * D + d);
             O0 += ov.x * f;
             O1 += ov.y * f;
+        }
+        if constexpr (EB == 1) {  // sum p (code * s_v) = s_v * sum p code
+            O0 *= P.v_scale[kvh];
+            O1 *= P.v_scale[kvh];
         }
         const size_t row = (size_t)b * H + h0 + h;
         if (single) {
@@ -909,24 +1015,27 @@ int dispatch_group(int G, const DecodeParams& P, int n_seqs, cudaStream_t stream
 
 // The tensor-core partition kernel (head_dim 128, bf16 cache): K and V pools
 // as 2-D TMA maps of [num_blocks * n_kv_heads * 16 rows][128 dims].
-template <int G>
+template <int G, int EB>
 int launch_partition_mma(const DecodeParams& P, int n_seqs, cudaStream_t stream) {
-    auto kern = pa_decode_mma_kernel<G>;
+    auto kern = pa_decode_mma_kernel<G, EB>;
+    constexpr int kSmem = mma::Lay<EB>::kSmem;
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, mma::kSmem) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
             return PA_ERR_CUDA;
         attr_done[dev] = true;
     }
     const uint64_t rows = (uint64_t)P.num_blocks * P.n_kv_heads * kBS;
     CUtensorMap tk, tv;
-    if (!pa_make_tmap_2d_bf16(&tk, P.k_pool, 128, rows, 256, 64, kBS) ||
-        !pa_make_tmap_2d_bf16(&tv, P.v_pool, 128, rows, 256, 64, kBS))
-        return PA_ERR_CUDA;
+    const bool maps = EB == 2 ? pa_make_tmap_2d_bf16(&tk, P.k_pool, 128, rows, 256, 64, kBS) &&
+                                    pa_make_tmap_2d_bf16(&tv, P.v_pool, 128, rows, 256, 64, kBS)
+                              : pa_make_tmap_2d_u8(&tk, P.k_pool, 128, rows, 128, 128, kBS) &&
+                                    pa_make_tmap_2d_u8(&tv, P.v_pool, 128, rows, 128, 128, kBS);
+    if (!maps) return PA_ERR_CUDA;
     dim3 grid(P.max_parts, P.n_kv_heads, n_seqs);
-    return pa_launch_pdl(kern, grid, dim3(mma::kNW * 32), mma::kSmem, stream, P, tk, tv);
+    return pa_launch_pdl(kern, grid, dim3(mma::kNW * 32), kSmem, stream, P, tk, tv);
 }
 
 constexpr int kDefaultPartitionTokens = 512;
@@ -1024,16 +1133,26 @@ int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int st;
-    // groups of 8 heads at head_dim 128 (bf16) run on the tensor cores, unless
-    // the pool has too many rows for a TMA coordinate; pa_decode_tc asks for
-    // the tensor-core kernel at every group size
-    const bool tensor = force_tc || (eb == 2 && head_dim == 128 && G == 8 && tc_rows_ok);
+    // At head_dim 128, groups of 8 heads and every E4M3 cache run on the tensor
+    // cores (the CUDA-core kernel is bound by its instructions there, not by
+    // HBM), unless the pool has too many rows for a TMA coordinate;
+    // pa_decode_tc asks for the tensor-core kernel at every group size
+    const bool tensor = force_tc || (head_dim == 128 && tc_rows_ok && (G == 8 || eb == 1));
     if (tensor) {
-        switch (G) {
-            case 1: st = launch_partition_mma<1>(P, n_seqs, s); break;
-            case 2: st = launch_partition_mma<2>(P, n_seqs, s); break;
-            case 4: st = launch_partition_mma<4>(P, n_seqs, s); break;
-            default: st = launch_partition_mma<8>(P, n_seqs, s); break;
+        if (eb == 2) {
+            switch (G) {
+                case 1: st = launch_partition_mma<1, 2>(P, n_seqs, s); break;
+                case 2: st = launch_partition_mma<2, 2>(P, n_seqs, s); break;
+                case 4: st = launch_partition_mma<4, 2>(P, n_seqs, s); break;
+                default: st = launch_partition_mma<8, 2>(P, n_seqs, s); break;
+            }
+        } else {
+            switch (G) {
+                case 1: st = launch_partition_mma<1, 1>(P, n_seqs, s); break;
+                case 2: st = launch_partition_mma<2, 1>(P, n_seqs, s); break;
+                case 4: st = launch_partition_mma<4, 1>(P, n_seqs, s); break;
+                default: st = launch_partition_mma<8, 1>(P, n_seqs, s); break;
+            }
         }
     } else if (eb == 1)
         st = head_dim == 128 ? dispatch_group<128, 1>(G, P, n_seqs, s) : dispatch_group<64, 1>(G, P, n_seqs, s);

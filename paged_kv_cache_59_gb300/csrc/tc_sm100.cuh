@@ -169,6 +169,9 @@ __host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t chunk
 // Returns false if the driver entry point is unavailable or rejects it.
 bool pa_make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                           uint64_t row_stride_bytes, uint32_t box_x, uint32_t box_y);
+// The same for a 2-D tensor of bytes (E4M3 codes), box_x bytes (128) wide.
+bool pa_make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                        uint64_t row_stride_bytes, uint32_t box_x, uint32_t box_y);
 
 namespace tc {
 // D[tmem] (+)= A[tmem] x B[smem]^T, K = 16, A read from tensor memory: row i
