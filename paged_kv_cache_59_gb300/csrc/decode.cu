@@ -507,17 +507,19 @@ pa_decode_partition_kernel(const DecodeParams P) {
 namespace mma {
 
 constexpr int kNW = 4;  // warps per CTA
-constexpr int kS = 2;   // stages per warp
-// Per warp, bf16 cache: kS stages of K 4 KiB + V 4 KiB (each two 2 KiB boxes,
-// 16 rows x 64 dims). E4M3 cache: kS stages of K 2 KiB + V 2 KiB (one box of
+constexpr int kS = 2;   // stages per warp (bf16 cache)
+// Per warp, bf16 cache: 2 stages of K 4 KiB + V 4 KiB (each two 2 KiB boxes,
+// 16 rows x 64 dims). E4M3 cache: 3 stages of K 2 KiB + V 2 KiB (one box of
 // 16 rows x 128 codes each) and one 4 KiB fp16 tile the V codes are widened
-// into (K's codes are widened in registers, straight from the stage).
+// into (K's codes are widened in registers, straight from the stage). Both
+// come to 64 KiB per CTA, three CTAs per SM.
 template <int EB>
 struct Lay {
     static constexpr int kStage = EB == 2 ? 8192 : 4096;
     static constexpr int kConv = EB == 2 ? 0 : 4096;
-    static constexpr int kWarp = kS * kStage + kConv;
-    static constexpr int kSmem = kNW * kWarp + kNW * kS * 8;
+    static constexpr int kStages = EB == 2 ? kS : 3;
+    static constexpr int kWarp = kStages * kStage + kConv;
+    static constexpr int kSmem = kNW * kWarp + kNW * kStages * 8;
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -582,7 +584,7 @@ __global__ void __launch_bounds__(mma::kNW * 32, 3)
 pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
     using namespace mma;
-    constexpr int D = 128, NW = kNW, S = kS;
+    constexpr int D = 128, NW = kNW, S = Lay<EB>::kStages;
     constexpr int kStage = Lay<EB>::kStage, kWarp = Lay<EB>::kWarp;
     static_assert(G <= 8, "query heads of a group fill the first G of 16 MMA rows");
     extern __shared__ __align__(1024) unsigned char smem_mma[];
