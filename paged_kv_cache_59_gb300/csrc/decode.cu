@@ -493,13 +493,14 @@ pa_decode_partition_kernel(const DecodeParams P) {
 // (head_dim 128, bf16 cache). With G = 8 query heads per KV head the CUDA-core
 // kernel above needs 255 registers, runs 8 warps per SM and is bound by its
 // FMA work, not by HBM. Here each tile's two products are warp-level
-// mma.sync tensor-core instructions (M = 16 rows, of which the G query heads
-// are the first G; N = 8; K = 16): a tile costs 16 + 32 of them instead of
-// ~1,000 FMA and shuffle instructions. tcgen05 needs M >= 64, which would
+// mma.sync tensor-core instructions (m16n8k16): a tile costs 16 (QK^T, the
+// G query heads in the first G of 16 rows) + 16 (PV, two P terms x 8 m-tiles
+// of 16 dims) of them instead of ~1,000 FMA and shuffle instructions. tcgen05 needs M >= 64, which would
 // waste 7/8 of every instruction on padding rows for this shape.
 //   S[16 x 16 tokens] = Q[16 x 128] . K^T   (A = q in registers, B = K via ldmatrix)
-//   O[16 x 128]      += P . V               (A = P, reused from S's accumulator
-//                                            layout; B = V via ldmatrix.trans)
+//   O^T[128 x 8]     += V^T . P^T           (A = V^T via ldmatrix.trans; B = P^T,
+//                                            which is S's accumulator layout as it
+//                                            stands; the 8 head rows fill N = 8)
 // P enters as two bf16 terms (P_hi = p truncated, P_lo = the rounded
 // remainder), as in the prefill, so the weights keep ~16 significant bits.
 // K and V tiles arrive by 2-D TMA in 128B-swizzled layout (16 rows x 64 dims
@@ -543,6 +544,12 @@ template <int EB>
 __device__ __forceinline__ void mma_t(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
     if constexpr (EB == 2) mma16816(c, a0, 0u, a2, 0u, b0, b1);
     else mma16816_f16(c, a0, 0u, a2, 0u, b0, b1);
+}
+template <int EB>
+__device__ __forceinline__ void mma_full(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    if constexpr (EB == 2) mma16816(c, a0, a1, a2, a3, b0, b1);
+    else mma16816_f16(c, a0, a1, a2, a3, b0, b1);
 }
 __device__ __forceinline__ uint32_t f2_to_h2(float a, float b) {  // fp16x2, a in the low half
     uint32_t r;
@@ -686,9 +693,11 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
             }
         }
     }
-    float o[16][4];  // O fragments: rows g (head g) and g+8 (padding), dims 8n + 2t, +1
+    // O^T fragments: m-tile mt holds dims 16mt + g (c0, c1) and 16mt + g + 8 (c2, c3)
+    // of heads 2t (c0, c2) and 2t + 1 (c1, c3)
+    float o[8][4];
 #pragma unroll
-    for (int n = 0; n < 16; ++n)
+    for (int n = 0; n < 8; ++n)
 #pragma unroll
         for (int k = 0; k < 4; ++k) o[n][k] = 0.f;
     float m_used = -INFINITY, l_run = 0.f;  // row g, base-2 units; l over this lane's columns
@@ -772,15 +781,21 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
             float tmax = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
             tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
             tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
+            float alpha = 1.f;
             if (tmax > m_used + 8.f) {  // lazy rescale: p <= 2^8 un-normalised
-                const float alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
+                alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
                 l_run *= alpha;
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    o[n][0] *= alpha;
-                    o[n][1] *= alpha;
-                }
                 m_used = tmax;
+            }
+            if (__any_sync(kFull, alpha != 1.f)) {  // O^T columns are heads: head h's factor from lane 4h
+                const float a0 = __shfl_sync(kFull, alpha, 8 * t), a1 = __shfl_sync(kFull, alpha, 8 * t + 4);
+#pragma unroll
+                for (int n = 0; n < 8; ++n) {
+                    o[n][0] *= a0;
+                    o[n][1] *= a1;
+                    o[n][2] *= a0;
+                    o[n][3] *= a1;
+                }
             }
             const float mref = m_used == -INFINITY ? 0.f : m_used;  // a row with no visible key yet
             float pv[4];
@@ -816,17 +831,16 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
                 tc::fence_async_smem();  // before the stage's next TMA fill
                 __syncwarp();
             }
-            // ---- O += P V: 16 n-tiles of 8 dims, k = the tile's 16 tokens
+            // ---- O^T += V^T P^T: 8 m-tiles of 16 dims, k = the tile's 16 tokens, n = the 8 head
+            // rows; P's accumulator layout is already the B operand (tokens 2t.. and 2t+8.. of head g)
             {
-                const int m = lane >> 3, row = 8 * (m & 1) + (lane & 7), dh = m >> 1;  // matrix: (token half, dim half)
+                const int m = lane >> 3, row = 8 * (m >> 1) + (lane & 7), dh = m & 1;  // matrix: (token half, dim half)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t b0a, b1a, b0b, b1b;
-                    ldsm_x4_t(vb + sw_off(row, 2 * j + dh), b0a, b1a, b0b, b1b);
-                    mma_t<EB>(o[2 * j], ph[0], ph[1], b0a, b1a);
-                    mma_t<EB>(o[2 * j], pl[0], pl[1], b0a, b1a);
-                    mma_t<EB>(o[2 * j + 1], ph[0], ph[1], b0b, b1b);
-                    mma_t<EB>(o[2 * j + 1], pl[0], pl[1], b0b, b1b);
+                for (int mt = 0; mt < 8; ++mt) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(vb + sw_off(row, 2 * mt + dh), a0, a1, a2, a3);
+                    mma_full<EB>(o[mt], a0, a1, a2, a3, ph[0], ph[1]);
+                    mma_full<EB>(o[mt], a0, a1, a2, a3, pl[0], pl[1]);
                 }
             }
         }
@@ -845,14 +859,21 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
     float* mo = reinterpret_cast<float*>(stages);  // [NW][G][D]
     float* mm = mo + NW * G * D;                   // [NW][G] max
     float* ml = mm + NW * G;                       // [NW][G] sum
-    if (g < G) {
-        float* dst = mo + ((size_t)warp * G + g) * D + 2 * t;
 #pragma unroll
-        for (int n = 0; n < 16; ++n) *reinterpret_cast<float2*>(dst + 8 * n) = make_float2(o[n][0], o[n][1]);
-        if (t == 0) {
-            mm[warp * G + g] = m_used;
-            ml[warp * G + g] = l_run;
+    for (int k = 0; k < 2; ++k) {  // heads 2t and 2t + 1
+        const int h = 2 * t + k;
+        if (h < G) {
+            float* dst = mo + ((size_t)warp * G + h) * D + g;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                dst[16 * mt] = o[mt][k];
+                dst[16 * mt + 8] = o[mt][2 + k];
+            }
         }
+    }
+    if (g < G && t == 0) {
+        mm[warp * G + g] = m_used;
+        ml[warp * G + g] = l_run;
     }
     __syncthreads();
 
