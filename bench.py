@@ -249,7 +249,8 @@ def run_ours(args):
     # algorithmic KV bytes: the distinct cached tokens the batch attends to (a
     # block shared by several tables, like a common prompt prefix, counts once)
     uniq_tok = unique_kv_tokens(wl.dec_tables, wl.dec_ctx, window)
-    tc_path = H // Hk == 8 and D == 128 and wl.meta.get("kv_dtype") != "fp8_e4m3"  # pa_decode's choice
+    # pa_decode's kernel choice: tensor cores at head_dim 128 for groups of 8 and E4M3 caches
+    tc_path = D == 128 and (H // Hk == 8 or wl.meta.get("kv_dtype") == "fp8_e4m3")
     if window is not None:   # tokens each query attends to: ctx-1-W .. ctx-1
         sum_ctx = int(sum(min(int(c), window + 1) for c in wl.dec_ctx))
     else:
@@ -424,7 +425,7 @@ def run_ours(args):
         "hbm_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {
             "bound": "hbm",
-            "kernel": (("pa_decode_mma_kernel (warp-level tensor-core MMAs; group of 8)" if tc_path else
+            "kernel": (("pa_decode_mma_kernel (warp-level tensor-core MMAs)" if tc_path else
                         "pa_decode_partition_kernel") + " + pa_decode_merge_kernel (one decode call)"),
             "achieved": round(achieved, 1),
             "peak": peak,
