@@ -121,10 +121,11 @@ size_t pa_decode_workspace_bytes(int n_seqs, int n_heads, int head_dim,
  * exponent with scale*log2(e) folded into q), fp32 split-K merge, bf16 output
  * rounded to nearest even.
  * Kernels: groups of up to 4 query heads per KV head use warp-shuffle fp32 dot
- * products on the CUDA cores. A group of 8 at head_dim 128 (bf16) would make
- * that kernel bound by its FMA work, far below HBM speed, so it runs its two
+ * products on the CUDA cores. A group of 8 at head_dim 128 would make that
+ * kernel bound by its FMA work, far below HBM speed, so it runs its two
  * products as warp-level tensor-core MMAs (see pa_decode_tc), unless the pool
- * has more than 2^31 - 16 rows of 16 tokens x KV heads.
+ * has more than 2^31 - 16 rows of 16 tokens x KV heads. pa_decode_fp8 does the
+ * same for every group at head_dim 128.
  */
 int pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
               const int32_t* block_tables, const int32_t* context_lens, float scale,
@@ -299,6 +300,10 @@ int pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool, void* v
  * q and out are bf16 as in pa_decode; the workspace is sized by
  * pa_decode_workspace_bytes (the same formula); partition_tokens as in
  * pa_decode_ex. Pools must be 16-byte aligned.
+ * At head_dim 128 the products run on the tensor-core kernel (fp16 MMAs with
+ * fp32 accumulate: every E4M3 value is an fp16 value, q is converted to fp16
+ * once, exact for |q| within the fp16 range, and P enters as two fp16 terms);
+ * at head_dim 64 on the CUDA-core kernel (fp32 dot products).
  */
 int pa_decode_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
