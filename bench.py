@@ -414,7 +414,7 @@ def run_ours(args):
                      if window is not None else
                      "pa_reshape_and_cache (1 new token/seq) + pa_decode (partition kernel + split-K merge)"),
             "l2": f"no flush: the KV stream ({kv_bytes / 1e6:.0f} MB/step) exceeds the 129 MB L2",
-            "partition_tokens": pt or 512,
+            "partition_tokens": pt or (1024 if tc_path else 512),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "tokens_per_s": round(world * B / (ms_per_step / 1e3), 1),

@@ -91,7 +91,9 @@ enum pa_device_error {
  * holds fp32 split-K partials: running max m and sum l per (seq, q-head,
  * partition) and the unnormalised output per (seq, q-head, partition, dim).
  * partition_tokens: tokens per context partition, a multiple of 64 in
- * [64, 2048]; 0 selects the library default.
+ * [64, 2048]; 0 selects the library default: 512 tokens, which also sizes
+ * the workspace for the tensor-core kernel's default of 1024 (fewer, larger
+ * partitions fit in the same bytes).
  */
 size_t pa_decode_workspace_bytes(int n_seqs, int n_heads, int head_dim,
                                  int max_context_len, int partition_tokens);

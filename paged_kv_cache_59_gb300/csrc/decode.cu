@@ -1107,7 +1107,16 @@ int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void
     const bool tc_rows_ok = (long long)num_blocks * n_kv_heads * kBS + kBS <= 0x7fffffffLL;  // TMA coordinates
     if (force_tc && (eb != 2 || head_dim != 128 || !tc_rows_ok)) return PA_ERR_UNSUPPORTED;
     if ((long long)max_blocks_per_seq * kBS < (long long)max_context_len) return PA_ERR_INVALID_ARG;
-    const int pt = resolve_partition_tokens(partition_tokens);
+    // At head_dim 128, groups of 8 heads and every E4M3 cache run on the tensor
+    // cores (the CUDA-core kernel is bound by its instructions there, not by
+    // HBM), unless the pool has too many rows for a TMA coordinate;
+    // pa_decode_tc asks for the tensor-core kernel at every group size
+    const bool tensor = force_tc || (head_dim == 128 && tc_rows_ok && (G == 8 || eb == 1));
+    // default partitions: 512 tokens on the CUDA-core kernel, 1024 on the
+    // tensor-core kernel, whose shorter blocks amortise a CTA's fixed cost
+    // over more of them (measured 3-5% faster); the workspace for 512 covers it
+    const int pt = partition_tokens == 0 && tensor ? 2 * kDefaultPartitionTokens
+                                                  : resolve_partition_tokens(partition_tokens);
     if (pt < 0) return PA_ERR_INVALID_ARG;
     if (pt / kBS > 32 * kNW) return PA_ERR_INVALID_ARG;  // one table entry per lane
     if (n_seqs == 0) return PA_OK;
@@ -1156,11 +1165,6 @@ int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int st;
-    // At head_dim 128, groups of 8 heads and every E4M3 cache run on the tensor
-    // cores (the CUDA-core kernel is bound by its instructions there, not by
-    // HBM), unless the pool has too many rows for a TMA coordinate;
-    // pa_decode_tc asks for the tensor-core kernel at every group size
-    const bool tensor = force_tc || (head_dim == 128 && tc_rows_ok && (G == 8 || eb == 1));
     if (tensor) {
         if (eb == 2) {
             switch (G) {

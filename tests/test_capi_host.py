@@ -104,8 +104,10 @@ def test_fp8_argument_errors_need_no_device(capi):
     assert capi.pa_decode_fp8(p, C.c_void_p(8192), p, p, p, p, p, p, *bad_g) == -2
     empty = list(tail); empty[5] = 0
     assert capi.pa_decode_fp8(p, C.c_void_p(8192), p, p, p, p, p, p, *empty) == 0
-    # a batch that needs split-K scratch and gets none
-    assert capi.pa_decode_fp8(p, C.c_void_p(8192), p, p, p, p, p, p, *tail) == -3
+    # a batch that needs split-K scratch and gets none (contexts up to 2048 tokens: two of the
+    # tensor-core kernel's default 1024-token partitions)
+    big = list(tail); big[6], big[7] = 128, 2048
+    assert capi.pa_decode_fp8(p, C.c_void_p(8192), p, p, p, p, p, p, *big) == -3
 
 
 # ----------------------------------------------------------- block manager --
