@@ -34,6 +34,10 @@
 //    one partition the CTA writes the bf16 output directly; otherwise it
 //    writes (max, sum, unnormalised output) to the workspace and a second
 //    kernel merges the partitions (split-K).
+//  * Groups of 8 query heads and E4M3 caches (head_dim 128) make the dot
+//    products above bound by their instructions, not by HBM. Those run the
+//    tensor-core variant further down: the same decomposition, with each
+//    block's two products as warp-level MMAs over TMA-staged, swizzled tiles.
 #include <cuda_bf16.h>
 #include <math.h>
 
