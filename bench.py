@@ -465,7 +465,9 @@ def run_ours(args):
                                 dist if world > 1 else None,
                                 (ks, vs) if fp8 else None)
         if rank == 0:
-            result["cpu_baseline"] = run_cpu_baseline(args.workload, args.cpu_seconds)
+            # an oracle process holds its own host copy of the pools plus numpy's working arrays
+            child_bytes = int(1.2 * 2 * kp.numel() * kp.element_size()) + (256 << 20)
+            result["cpu_baseline"] = run_cpu_baseline(args.workload, args.cpu_seconds, child_bytes)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -621,34 +623,37 @@ def prepare(b, h):
         slot = np.array([idx * 16 + off], dtype=np.int64)
     return kp, vp, table, slot
 kv_tok = 2 * wl.head_dim * (1 if fp8 else 2)   # K + V bytes of one token of one KV head
+def run_unit(b, h, kp, vp, table, slot):
+    if fp8:
+        ks, vs = wl.meta["k_scale"][h:h + 1], wl.meta["v_scale"][h:h + 1]
+        if slot is not None:
+            kp, vp = ofp8.reshape_and_cache_fp8(wl.new_k[b:b + 1, h:h + 1], wl.new_v[b:b + 1, h:h + 1],
+                                                kp, vp, slot, ks, vs)
+        ofp8.paged_decode_fp8(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1],
+                              wl.scale, ks, vs)
+    else:
+        if slot is not None:
+            kp, vp = reshape_and_cache(wl.new_k[b:b + 1, h:h + 1], wl.new_v[b:b + 1, h:h + 1], kp, vp,
+                                       slot)
+        if W is not None:
+            paged_decode_window(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1],
+                                wl.scale, W)
+        else:
+            paged_decode(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1], wl.scale)
 done_tok = 0
 n_units = 0
-u = 0
+u = {start} % len(units)
 dt = 0.0
 while True:
     sel = [units[(u + i) % len(units)] for i in range(per_step)]
     u = (u + per_step) % len(units)
     prep = [prepare(b, h) for b, h in sel]
     t0 = time.perf_counter()
-    for (b, h), (kp, vp, table, slot) in zip(sel, prep):
-        if fp8:
-            ks, vs = wl.meta["k_scale"][h:h + 1], wl.meta["v_scale"][h:h + 1]
-            if slot is not None:
-                kp, vp = ofp8.reshape_and_cache_fp8(wl.new_k[b:b + 1, h:h + 1], wl.new_v[b:b + 1, h:h + 1],
-                                                    kp, vp, slot, ks, vs)
-            ofp8.paged_decode_fp8(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1],
-                                  wl.scale, ks, vs)
-        else:
-            if slot is not None:
-                kp, vp = reshape_and_cache(wl.new_k[b:b + 1, h:h + 1], wl.new_v[b:b + 1, h:h + 1], kp, vp,
-                                           slot)
-            if W is not None:
-                paged_decode_window(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1],
-                                    wl.scale, W)
-            else:
-                paged_decode(wl.q[b:b + 1, h * G:(h + 1) * G], kp, vp, table, wl.dec_ctx[b:b + 1], wl.scale)
-        done_tok += int(wl.dec_ctx[b]) if W is None else min(int(wl.dec_ctx[b]), W + 1)
+    for (b, h), args in zip(sel, prep):
+        run_unit(b, h, *args)
     dt += time.perf_counter() - t0
+    for b, h in sel:
+        done_tok += int(wl.dec_ctx[b]) if W is None else min(int(wl.dec_ctx[b]), W + 1)
     n_units += len(sel)
     if {fixed_steps} and n_units >= {fixed_steps} * per_step:
         break
@@ -658,21 +663,25 @@ print(json.dumps({{"seconds": dt, "tokens": done_tok, "units": n_units, "kv_byte
 """
 
 
-def _oracle_child(workload, seconds, per_step, fixed_steps=0):
+def _oracle_cmd(workload, seconds, per_step, fixed_steps=0, start=0):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     code = _CPU_CHILD.format(root=ROOT, workload=workload, seconds=seconds, per_step=per_step,
-                             fixed_steps=fixed_steps)
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
-                       timeout=3600)
+                             fixed_steps=fixed_steps, start=start)
+    return [sys.executable, "-c", code], env
+
+
+def _oracle_child(workload, seconds, per_step, fixed_steps=0):
+    cmd, env = _oracle_cmd(workload, seconds, per_step, fixed_steps)
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=3600)
     if r.returncode != 0:
         raise RuntimeError(f"oracle child failed:\n{r.stderr[-2000:]}")
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def run_cpu_baseline(workload, seconds):
+def run_cpu_baseline(workload, seconds, bytes_per_child):
     try:
         res = _oracle_child(workload, seconds, per_step=1)
     except Exception as e:  # report, do not hide
@@ -683,7 +692,43 @@ def run_cpu_baseline(workload, seconds):
                       f"order; {res['tokens']} context tokens, each unit's cache write and decode) "
                       f"through the fp64 numpy oracle in {res['seconds']:.1f} s on 1 host thread "
                       f"(BLAS pinned to 1 thread)",
-            "host_logical_cores": os.cpu_count()}
+            "host_logical_cores": os.cpu_count(),
+            "all_cores": run_cpu_all_cores(workload, seconds, bytes_per_child)}
+
+
+def run_cpu_all_cores(workload, seconds, bytes_per_child):
+    """The same oracle in one single-threaded process per host core, run at
+    the same time, each starting at its own place in the unit list; the
+    reported rate is the sum of the processes' rates. The process count is
+    capped so that their copies of the workload take at most half of the
+    host's free memory."""
+    cores = os.cpu_count() or 1
+    try:
+        free = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError):
+        free = 0
+    n = max(1, min(cores, int(free // 2 // max(bytes_per_child, 1)))) if free else 1
+    procs = []
+    try:
+        for i in range(n):
+            cmd, env = _oracle_cmd(workload, seconds, per_step=1, start=i * 997)
+            procs.append(subprocess.Popen(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                          text=True))
+        outs = [p.communicate(timeout=3600) for p in procs]
+        if any(p.returncode != 0 for p in procs):
+            err = next(e for p, (_, e) in zip(procs, outs) if p.returncode != 0)
+            raise RuntimeError(f"oracle child failed:\n{err[-2000:]}")
+        res = [json.loads(o.strip().splitlines()[-1]) for o, _ in outs]
+    except Exception as e:  # report, do not hide
+        for p in procs:
+            if p.poll() is None:
+                p.kill()
+        return {"value": None, "cores": n, "error": str(e)[-300:]}
+    rate = sum(r["kv_bytes"] / r["seconds"] for r in res) / 1e9
+    return {"value": round(rate, 4), "unit": "GB/s", "cores": n,
+            "sample": f"{n} single-threaded oracle processes at once, each timing about {seconds:.0f} s "
+                      f"of units ({sum(r['units'] for r in res)} units, {sum(r['tokens'] for r in res)} "
+                      f"context tokens in all); the rate is the sum of theirs"}
 
 
 # --------------------------------------------------------- reference arm ----
