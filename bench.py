@@ -313,9 +313,10 @@ def run_ours(args):
                                 partition_tokens=pt)
         else:
             pk.pa_decode(out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, workspace=ws, partition_tokens=pt)
-    launches_per_step = ((1 if n_dec_new else 0) + (1 if has_pf else 0) + 1
-                         + (1 if pk.pa_decode_workspace_bytes(B, H, D, max_ctx, pt) else 0)
-                         + (1 if has_pf and ws_pf is not None else 0))
+    # cache write, prefill (plan + main + merge of the cut pairs in balanced mode), decode
+    # (partition kernel, plus the split-K merge kernel when some context spans partitions)
+    launches_per_step = ((1 if n_dec_new else 0) + ((3 if ws_pf is not None else 1) if has_pf else 0)
+                         + 1 + (1 if pk.pa_decode_workspace_bytes(B, H, D, max_ctx, pt) else 0))
 
     def step(ev_pair=None, pf_pair=None):
         if n_dec_new:
