@@ -454,14 +454,14 @@ def run_ours(args):
                                               if ws_pf is not None else 1)
         result["prefill_roofline"] = {
             "bound": "tensor",
-            "kernel": "pa_prefill_plan_kernel + pa_prefill_tc_kernel (one CTA per SM) + pa_prefill_merge_kernel",
+            "kernel": "pa_prefill_plan_kernel + pa_prefill_tc_kernel (one CTA per SM) + pa_prefill_merge_cut_kernel",
             "achieved": round(pf_flops / (pf_avg / 1e3) / 1e12, 1), "peak": tpk,
             "peak_source": tpk_kind, "unit": "TFLOP/s",
             "frac": round(pf_flops / (pf_avg / 1e3) / 1e12 / tpk, 4),
             "launch_ms_avg": round(pf_avg, 4),
             "launch_ms_median": round(sorted(pf_ms)[len(pf_ms) // 2], 4),
             "note": "algorithmic FLOPs 4*D*H*sum(positions attended); the kernel also runs the "
-                    "P_lo correction MMA (1.5x the PV FLOPs) and the masked diagonal tiles"}
+                    "masked halves of the diagonal tiles"}
 
     if not args.skip_baselines:
         result["e2e"] = run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world,

@@ -79,8 +79,12 @@ enum pa_device_error {
     PA_DEVERR_CONTEXT = 16, /* a context length beyond 16*max_blocks_per_seq or
                                max_context_len (the excess is not attended), or a
                                prefill chunk longer than its context */
-    PA_DEVERR_LAYOUT = 32   /* the shared-memory base was not 1024-byte aligned
+    PA_DEVERR_LAYOUT = 32,  /* the shared-memory base was not 1024-byte aligned
                                (prefill; nothing computed) */
+    PA_DEVERR_RANGE = 64    /* a prefill output (or split partial) was not finite:
+                               a V element beyond +-65504*2^8 in a key tile the
+                               chunk reads (the P.V product stages V in fp16), or
+                               non-finite inputs */
 };
 
 /* ------------------------------------------------------------------ decode */
@@ -330,8 +334,13 @@ int pa_decode_fp8(void* out, const void* q, const void* k_pool, const void* v_po
  *  context_lens  int32 [n_seqs], >= L_s
  *  max_chunk_len upper bound of L_s
  * head_dim must be 128 and the group n_heads/n_kv_heads 1, 2, 4 or 8.
- * QK^T and PV run on the tcgen05 tensor cores (bf16 in, fp32 accumulate in
- * tensor memory); softmax in fp32.
+ * QK^T and PV run on the tcgen05 tensor cores with fp32 accumulation in
+ * tensor memory; softmax in fp32. QK^T takes bf16 q and K. PV takes P rounded
+ * to fp16 (within 2^-12 of p) and V staged in fp16 as v * 2^-8, which holds
+ * every bf16 significand for 2^-6 <= |v| <= 65504 * 2^8. The P rounding adds
+ * at most 2^-12 * max|v| to an output. Smaller |v| lose bits, at an absolute
+ * error of at most 2^-17. Larger |v| in a key tile the chunk reads make the
+ * output non-finite and set PA_DEVERR_RANGE.
  */
 int pa_prefill_paged(void* out, const void* q, const void* k_pool, const void* v_pool,
                      const int32_t* block_tables, const int32_t* context_lens,

@@ -27,6 +27,7 @@ PA_DEVERR_TIMEOUT = 4
 PA_DEVERR_PAIR = 8
 PA_DEVERR_CONTEXT = 16
 PA_DEVERR_LAYOUT = 32
+PA_DEVERR_RANGE = 64
 
 vp = C.c_void_p
 i32 = C.c_int

@@ -15,29 +15,35 @@
 // the same (sequence, KV head): both use every K/V tile it loads, and the
 // tensor core alternates between them so that one tile's MMAs run while the
 // other tile's softmax works. Per key tile j of 128 keys (8 blocks of 16),
-// four roles, each waiting only on mbarriers:
+// five roles, each waiting only on mbarriers:
 //   - a producer warp moves the 8 K and 8 V blocks with 2-D TMA loads into
 //     128B-swizzled shared memory: three K stages and two V stages, each
 //     refilled as soon as the tensor core is done with it (blocks past the
 //     end of the sequence load out of bounds and arrive as zeros);
+//   - two converter warps rewrite each landed V tile in place as fp16
+//     values of v * 2^-8 (rows past the context, which hold whatever the
+//     pool has there, become zeros);
 //   - an MMA warp issues, per query tile X, S_X = Q_X K_j^T (tcgen05.mma
 //     kind::f16, bf16 in, fp32 accumulator in tensor memory, M = N = 128)
-//     and, once X's softmax has written P, O_X += P V_j (P read from tensor
-//     memory, V as an MN-major shared-memory operand). The MMAs of one
-//     thread execute in issue order, so S_X(j+1) is issued right behind the
-//     PV MMA that still reads P(j) out of the same columns;
+//     and, once X's softmax has written P, O_X += P V_j (fp16 in: P read
+//     from tensor memory, V as an MN-major shared-memory operand). The MMAs
+//     of one thread execute in issue order, so S_X(j+1) is issued right
+//     behind the PV MMA that still reads P(j) out of the same columns;
 //   - one softmax warpgroup per query tile (thread = row) reads S_X from
 //     tensor memory twice, a quarter of 32 columns at a time (row maximum,
 //     then exponentials), applies the scale, the causal mask (diagonal tiles
 //     only) and an online softmax in fp32 (base 2) with a lazily updated
 //     maximum (O_X is rescaled in tensor memory only when a row's maximum
 //     grows by more than 8, so un-normalised p <= 2^8), and writes P back
-//     into S_X's columns as two bf16 terms, P = P_hi + P_lo (P_hi = p
-//     truncated, P_lo = the remainder rounded), consumed by two MMAs. A
-//     single bf16 P costs up to ~2^-9 relative per weight, which on short
-//     causal rows with cancelling values exceeds an absolute error of 2e-3;
-//     the two-term P is accurate to ~2^-16.
-// The normalised output O / l is written once at the end.
+//     into S_X's columns as fp16 (rounded to nearest: within 2^-12 of p
+//     relative). A bf16 P (within 2^-9) would exceed an absolute error of
+//     2e-3 on short causal rows with cancelling values; the tensor core
+//     takes A and B of one type, hence V in fp16 too. Every bf16 value is
+//     an fp16 value inside fp16's exponent range; the factor 2^-8 moves
+//     that range up to |v| <= 65504 * 2^8 (larger values become infinite
+//     and the output non-finite, which is flagged), at an absolute error of
+//     at most 2^-17 for |v| < 2^-6, where the scaled value is subnormal.
+// The normalised output 2^8 O / l is written once at the end.
 //
 // Scheduling. Per-pair mode: one CTA per (pair, KV head, sequence), or per
 // piece of its key range. Balanced mode: one CTA per SM takes entries of a
@@ -112,6 +118,22 @@ __host__ __device__ inline void piece_range(int n_kt, int sp, int splits, int& k
     kt1 = (int)((long long)(sp + 1) * n_kt / splits);
 }
 
+// fp32 -> fp16 round to nearest even; a in the low half, b in the high half
+// (beyond the fp16 range: infinity).
+__device__ __forceinline__ uint32_t float2_to_f16x2(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with fp16 A and B (the
+// kind takes one type for both operands) and an fp32 accumulator; fields as
+// in tc::idesc_bf16_f32 with the A and B format fields 0 (fp16).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // max of three floats in one instruction (sm_100 family)
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float r;
@@ -141,7 +163,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigne
 }
 
 template <int G>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
 pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
     constexpr int QT = kRows / G;  // chunk tokens per query tile
@@ -149,13 +171,14 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
     uint64_t* k_full = bars;        // [kKS] K tile landed
     uint64_t* k_free = bars + 3;    // [kKS] both QKs that read the K stage are done
-    uint64_t* v_full = bars + 6;    // [kVS] V tile landed
+    uint64_t* v_full = bars + 6;    // [kVS] V tile landed (bf16)
     uint64_t* v_free = bars + 8;    // [kVS] PV_B, the last reader of the V stage, is done
     uint64_t* s_full = bars + 10;   // [2] per query tile
     uint64_t* p_full = bars + 12;   // [2] per query tile, 4 arrivals (one per warp)
     uint64_t* pv_done = bars + 14;  // [2] per query tile
     uint64_t* drain = bars + 16;
-    constexpr int kNumBars = 17;
+    uint64_t* v_conv = bars + 17;   // [kVS] V tile rewritten as fp16, 2 arrivals (one per converter warp)
+    constexpr int kNumBars = 19;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
 
@@ -237,6 +260,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             for (int i = 0; i < kVS; ++i) {
                 pa::mbar_init(&v_full[i], 1);
                 pa::mbar_init(&v_free[i], 1);
+                pa::mbar_init(&v_conv[i], 2);
             }
             for (int x = 0; x < 2; ++x) {
                 pa::mbar_init(&s_full[x], 1);
@@ -269,7 +293,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         have_tmem = true;
 
         constexpr uint32_t ID_QK = tc::idesc_bf16_f32(128, 128, 0, 0);
-        constexpr uint32_t ID_PV = tc::idesc_bf16_f32(128, 128, 0, 1);
+        constexpr uint32_t ID_PV = idesc_f16_f32(128, 128, 0, 1);
 
         if (warp == 9) {
             // ------------------------------------------------------- TMA producer
@@ -352,16 +376,14 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 }
                 __syncwarp();
             };
-            auto issue_pv = [&](int x, int j) {  // O_x += P_hi V_j + P_lo V_j, P in S_x's columns
+            auto issue_pv = [&](int x, int j) {  // O_x += P V_j (fp16), P in S_x's columns
                 if (lane == 0) {
                     const uint32_t vo = (j % kVS) * (32768 >> 4);
                     const uint32_t pcol = tbase + x * 256, dst = pcol + 128;
 #pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks)
-                            tc::mma_bf16_ts(dst, pcol + (ks >> 1) * 32 + part * 16 + (ks & 1) * 8, at(dv, vo + ks * (2048 >> 4)),
-                                            ID_PV, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16_ts(dst, pcol + (ks >> 1) * 32 + (ks & 1) * 8, at(dv, vo + ks * (2048 >> 4)),
+                                        ID_PV, (j > 0 || ks > 0) ? 1u : 0u);  // fp16 operands per ID_PV
                     tc::mma_commit(&pv_done[x]);
                     if (x == 1) tc::mma_commit(&v_free[j % kVS]);  // the stage's last reader
                 }
@@ -379,7 +401,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             for (int j = 0; j < n_kt && ok; ++j) {
                 const uint32_t par = (uint32_t)(j & 1);
                 ok = wait_bar(&p_full[0], par, P.err, abort_flag);
-                if (ok) ok = wait_bar(&v_full[j % kVS], (uint32_t)((j / kVS) & 1), P.err, abort_flag);
+                if (ok) ok = wait_bar(&v_conv[j % kVS], (uint32_t)((j / kVS) & 1), P.err, abort_flag);
                 if (!ok) break;
                 tc::fence_after_sync();
                 issue_pv(0, j);
@@ -405,6 +427,41 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 for (int t = max(0, n_kt - kVS); t < n_kt; ++t)
                     pa::mbar_wait(&v_free[t % kVS], (uint32_t)((t / kVS) & 1), nullptr, 10000000ull);
             }
+        } else if (warp >= 10) {
+            // ------------------------------------------------------ V converters
+            // Thread t of 64 rewrites the 16-byte chunks t, t + 64, ... of the
+            // landed tile (consecutive threads, consecutive chunks). A chunk holds
+            // 8 consecutive values of one key row: row (chunk % 1024) / 8 of
+            // either 64-dim half, wherever the swizzle put the chunk in the row.
+            const int t = threadIdx.x - 320;
+            const float2 k2 = make_float2(0.00390625f, 0.00390625f);  // 2^-8
+            auto cvt = [&](uint32_t u) {  // bf16 pair -> fp16 pair of v * 2^-8
+                const float2 f = __fmul2_rn(make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)), k2);
+                return float2_to_f16x2(f.x, f.y);
+            };
+            bool ok = true;
+            for (int j = 0; j < n_kt && ok; ++j) {
+                ok = wait_bar(&v_full[j % kVS], (uint32_t)((j / kVS) & 1), P.err, abort_flag);
+                ok = __all_sync(kFull, ok);
+                if (!ok) break;
+                const int kb = (kt0 + j) * kKT;
+                uint4* vs = reinterpret_cast<uint4*>(sm + kV0 + (j % kVS) * 32768);
+                const int valid = ctx - kb;  // key rows of this tile inside the context (may exceed 128)
+#pragma unroll 4
+                for (int c = 0; c < 32; ++c) {
+                    const int e = t + 64 * c;
+                    uint4 w = vs[e];
+                    if (((e & 1023) >> 3) >= valid) w = make_uint4(0, 0, 0, 0);
+                    w.x = cvt(w.x);
+                    w.y = cvt(w.y);
+                    w.z = cvt(w.z);
+                    w.w = cvt(w.w);
+                    vs[e] = w;
+                }
+                tc::fence_async_smem();  // generic-proxy writes, read next by the tensor core
+                __syncwarp();
+                if (lane == 0) pa::mbar_arrive(&v_conv[j % kVS]);
+            }
         } else {
             // --------------------------------------- softmax warpgroup of tile x
             // warp w serves TMEM lanes 32*(w%4) .. +31 (rows). After a failed wait
@@ -424,21 +481,6 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 ok = __all_sync(kFull, ok);
                 tc::fence_after_sync();
                 const int kb = (kt0 + j) * kKT;
-                // V rows of the sequence's last, partial block hold whatever the pool
-                // has there: zero them so that p = 0 never meets a NaN (tile A's
-                // warpgroup, once V_j has landed and before PV_A(j), the first PV
-                // reading it)
-                if (x == 0 && (ctx & (kBS - 1)) && ctx > kb && ctx < kb + kKT) {
-                    if (ok) ok = wait_bar(&v_full[j % kVS], (uint32_t)((j / kVS) & 1), P.err, abort_flag);
-                    ok = __all_sync(kFull, ok);
-                    const int z0 = ctx - kb, z1 = min(((ctx + kBS - 1) & ~(kBS - 1)) - kb, kKT);
-                    unsigned char* vs = sm + kV0 + (j % kVS) * 32768;
-                    for (int e = r; e < (z1 - z0) * 16; e += 128) {
-                        const int row = z0 + (e >> 4), g = (e >> 3) & 1, c = e & 7;
-                        *reinterpret_cast<uint4*>(vs + g * 16384 + tc::sw128_offset(row, c)) = make_uint4(0, 0, 0, 0);
-                    }
-                    tc::fence_async_smem();
-                }
                 // Keys beyond a row's position are masked. Only the tiles on the
                 // diagonal have such keys; a warp takes the masking code only when
                 // one of its rows needs it (a warp-uniform branch), so the other
@@ -481,24 +523,21 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                     alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
                     m_used = tmax;
                 }
-                // pass 2, per quarter of 32 keys: p = 2^(s*scale - m) as P_hi + P_lo.
-                // Quarter q's scores sit in columns 32q..32q+31; P_hi of its keys
-                // 2w, 2w+1 goes to column 32q + w and P_lo to 32q + 16 + w, so a
-                // quarter only overwrites columns it has already read. P_hi is p
-                // truncated to bf16 (a byte permute), P_lo the remainder rounded to
-                // bf16: together within 2^-16 of p. Both passes loop over quarters
-                // without unrolling: the smaller body keeps the softmax warps out of
+                // pass 2, per quarter of 32 keys: p = 2^(s*scale - m) in fp16.
+                // Quarter q's scores sit in columns 32q..32q+31; P of its keys 2w,
+                // 2w+1 goes to column 32q + w, so a quarter only overwrites columns
+                // it has already read. Both passes loop over quarters without
+                // unrolling: the smaller body keeps the softmax warps out of
                 // instruction-fetch stalls.
                 float2 psum2 = make_float2(0.f, 0.f);
                 const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_used, -m_used);
-                const float2 neg1 = make_float2(-1.f, -1.f);
                 auto pass2 = [&](auto masked) {
 #pragma unroll 1
                     for (int qd = 0; qd < 4; ++qd) {
                         uint32_t raw[32];
                         tc::tmem_ld32(tS + 32 * qd, raw);
                         tc::tmem_wait_ld();
-                        uint32_t hi[16], lo[16];
+                        uint32_t ph[16];
 #pragma unroll
                         for (int w = 0; w < 16; ++w) {
                             float2 e = __ffma2_rn(make_float2(__uint_as_float(raw[2 * w]), __uint_as_float(raw[2 * w + 1])),
@@ -511,14 +550,9 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                             e.x = pa::fast_exp2(e.x);
                             e.y = pa::fast_exp2(e.y);
                             psum2 = __fadd2_rn(psum2, e);
-                            const uint32_t bx = __float_as_uint(e.x), by = __float_as_uint(e.y);
-                            hi[w] = __byte_perm(bx, by, 0x7632);
-                            const float2 rr = __ffma2_rn(
-                                make_float2(__uint_as_float(bx & 0xffff0000u), __uint_as_float(by & 0xffff0000u)), neg1, e);
-                            lo[w] = pa::float2_to_bf16x2(rr.x, rr.y);
+                            ph[w] = float2_to_f16x2(e.x, e.y);
                         }
-                        tc::tmem_st16(tS + 32 * qd, hi);
-                        tc::tmem_st16(tS + 32 * qd + 16, lo);
+                        tc::tmem_st16(tS + 32 * qd, ph);
                     }
                 };
                 if (mask_warp) pass2(std::true_type{});
@@ -552,6 +586,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 // a piece: keep O, m and l for the merge
                 tc::fence_after_sync();
                 float* dst = part_base + ((size_t)x * 128 + r) * kPartStride;
+                bool finite = true;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t raw[32];
@@ -559,23 +594,32 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                     tc::tmem_wait_ld();
                     if (i < L) {
 #pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            raw[k] = __float_as_uint(__uint_as_float(raw[k]) * 256.f);  // undo V's 2^-8
+                            finite &= (raw[k] & 0x7f800000u) != 0x7f800000u;
+                        }
+#pragma unroll
                         for (int k = 0; k < 32; k += 4)
                             *reinterpret_cast<float4*>(dst + c * 32 + k) =
                                 make_float4(__uint_as_float(raw[k]), __uint_as_float(raw[k + 1]),
                                             __uint_as_float(raw[k + 2]), __uint_as_float(raw[k + 3]));
                     }
                 }
+                if (!finite) pa::set_error(P.err, PA_DEVERR_RANGE);
                 if (i < L) *reinterpret_cast<float2*>(dst + 128) = make_float2(m_used, l);
             } else if (ok) {
                 tc::fence_after_sync();
-                const float inv = 1.f / l;
+                const float inv = 256.f / l;  // with V's 2^-8 undone
                 uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
+                bool finite = true;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t raw[32];
                     tc::tmem_ld32(tO + c * 32, raw);
                     tc::tmem_wait_ld();
                     if (i < L) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) finite &= (raw[k] & 0x7f800000u) != 0x7f800000u;
 #pragma unroll
                         for (int k = 0; k < 32; k += 8) {
                             uint4 w;
@@ -587,6 +631,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                         }
                     }
                 }
+                if (!finite) pa::set_error(P.err, PA_DEVERR_RANGE);
             }
         }
         tc::fence_before_sync();
@@ -819,10 +864,10 @@ int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtenso
     const int n_qp = (max_chunk_len + 2 * QT - 1) / (2 * QT);
     if (Pp.work) {  // balanced mode: plan, then one CTA per SM taking work-list entries
         pa_prefill_plan_kernel<G><<<1, 1024, 0, stream>>>(Pp);
-        kern<<<Pp.n_cta, 320, kSmemBytes, stream>>>(Pp, tk, tv);
+        kern<<<Pp.n_cta, 384, kSmemBytes, stream>>>(Pp, tk, tv);
     } else {
         dim3 grid(n_qp * Pp.splits, Pp.n_kv_heads, n_seqs);
-        kern<<<grid, 320, kSmemBytes, stream>>>(Pp, tk, tv);
+        kern<<<grid, 384, kSmemBytes, stream>>>(Pp, tk, tv);
     }
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (Pp.work)  // the cut pairs (fewer than one per CTA): 256 rows each

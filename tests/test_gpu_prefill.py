@@ -168,3 +168,59 @@ def test_prefill_bad_block_id_is_flagged_not_faulted(pk, splits):
     for r, h in rows:
         assert_attention_close(got[r, h], ref[r, h], f"row {(r, h)}")
     check_device_error(1)                               # PA_DEVERR_BLOCK_ID
+
+
+def _scale_bf16(bits, factor):
+    """bf16 bits times a power of two (exact; NaN stays NaN)."""
+    f = (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32) * np.float32(factor)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("splits", [None, 0])
+def test_prefill_small_v(pk, splits):
+    """P.V stages V as fp16 values of v * 2^-8: V of magnitude ~2^-12 (subnormal
+    after the scaling) still matches the oracle within the tolerance."""
+    wl = make_prefill_case(951, [300, 129], [37, 129], [], 32, 8, 128)
+    wl.v_pool = _scale_bf16(wl.v_pool, 2.0 ** -12)
+    wl.new_v = _scale_bf16(wl.new_v, 2.0 ** -12)
+    got = _run(pk, wl, splits)
+    ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
+    assert_attention_close(got, ref, "V x 2^-12")
+    check_device_error(0)
+
+
+@pytest.mark.parametrize("splits", [None, 0])
+def test_prefill_large_v_scales_exactly(pk, splits):
+    """Attention is linear in V. P.V stages V as fp16 values of v * 2^-8, which
+    holds every bf16 significand exactly while v * 2^-8 is a normal fp16 value
+    (2^-14 .. 65504). Here the nonzero |v| span 2^-20.3 .. 5, so V x 2^15 and
+    V x 2^21 (values up to ~2^23, far beyond the plain fp16 range) both stage
+    exactly, and the outputs differ by exactly 2^6: the bf16 output bits
+    differ by 6 in the exponent field only."""
+    wl = make_prefill_case(953, [300, 129], [37, 129], [], 32, 8, 128)
+    mags = []
+    for a in (wl.v_pool, wl.new_v):
+        f = np.abs((a.astype(np.uint32) << 16).view(np.float32))
+        mags.append(f[np.isfinite(f) & (f > 0)])
+    mags = np.concatenate(mags)
+    assert mags.min() * 2.0 ** (15 - 8) >= 2.0 ** -14 and mags.max() * 2.0 ** (21 - 8) <= 65504
+    v_pool, new_v = wl.v_pool, wl.new_v
+    outs = []
+    for c in (15, 21):
+        wl.v_pool, wl.new_v = _scale_bf16(v_pool, 2.0 ** c), _scale_bf16(new_v, 2.0 ** c)
+        outs.append(_run(pk, wl, splits))
+        check_device_error(0)
+    assert np.array_equal(outs[1], _scale_bf16(outs[0], 2.0 ** 6))
+
+
+@pytest.mark.parametrize("splits", [None, 0])
+def test_prefill_v_beyond_fp16_staging_is_flagged(pk, splits):
+    """One V element of 2^25 (> 65504 * 2^8) in a key tile the chunk reads:
+    the affected outputs are not finite and PA_DEVERR_RANGE is set."""
+    wl = make_prefill_case(952, [300], [37], [], 32, 8, 128)
+    wl.new_v = wl.new_v.copy()
+    wl.new_v[0, 0, 5] = 0x4C00                          # bf16 2^25 at the chunk's first token
+    got = _run(pk, wl, splits)
+    assert not np.isfinite((got.astype(np.uint32) << 16).view(np.float32)).all()
+    check_device_error(64)                              # PA_DEVERR_RANGE
