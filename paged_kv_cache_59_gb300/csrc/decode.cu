@@ -506,7 +506,9 @@ pa_decode_partition_kernel(const DecodeParams P) {
 //                                            which is S's accumulator layout as it
 //                                            stands; the 8 head rows fill N = 8)
 // P enters as two bf16 terms (P_hi = p truncated, P_lo = the rounded
-// remainder), as in the prefill, so the weights keep ~16 significant bits.
+// remainder), so the weights keep ~16 significant bits. (A single fp16 P,
+// as the prefill uses, would need V widened to fp16 element by element in
+// registers here, which costs more instructions than the P_lo MMAs save.)
 // K and V tiles arrive by 2-D TMA in 128B-swizzled layout (16 rows x 64 dims
 // per box), so the ldmatrix row reads are free of bank conflicts.
 namespace mma {
