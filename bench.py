@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--skip-baselines", action="store_true",
                     help="skip the CPU oracle and end-to-end legs (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="host time the reference arm (the oracle) aims to spend on warmup + steps")
     return ap.parse_args()
 
 
@@ -777,7 +779,7 @@ def run_reference(args):
     # size the per-step sample so that warmup + steps stay within ~2 minutes
     calib = _oracle_child(args.workload, 2.0, per_step=1)
     sec_per_unit = calib["seconds"] / max(calib["units"], 1)
-    budget = 120.0
+    budget = args.ref_seconds
     total_steps = args.steps + args.warmup
     per_step = max(1, int(budget / total_steps / sec_per_unit))
     per_step = min(per_step, 512)
