@@ -331,3 +331,27 @@ def test_decode_tc_unsupported_shapes_need_no_device(capi):
     assert capi.pa_decode_tc(*args, 8, 8, 64, 16, 2, 4, 64, 16, 0, None, 0, None) == -2
     assert capi.pa_decode_tc(*args, 8, 8, 128, 16, 2, 4, 64, 20000000, 0, None, 0, None) == -2
     assert capi.pa_decode_tc(*args, 8, 8, 128, 16, 0, 4, 64, 16, 0, None, 0, None) == 0   # no sequences
+
+
+def test_binding_refuses_host_tensors(capi):
+    """No CPU fallback: every compute entry point of the binding rejects host
+    tensors before anything reaches the library."""
+    import torch
+    import paged_kv_cache_59_gb300 as pk
+    n, H, Hk, D, nb = 2, 8, 2, 64, 4
+    q = torch.zeros(n, H, D, dtype=torch.bfloat16)
+    out = torch.zeros_like(q)
+    kp = torch.zeros(nb, Hk, 16, D, dtype=torch.bfloat16)
+    vp = torch.zeros_like(kp)
+    tabs = torch.zeros(n, 2, dtype=torch.int32)
+    ctx = torch.ones(n, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pk.pa_decode(out, q, kp, vp, tabs, ctx, 0.125, 1)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pk.pa_decode_window(out, q, kp, vp, tabs, ctx, 0.125, 1, 4)
+    k_new = torch.zeros(n, Hk, D, dtype=torch.bfloat16)
+    slots = torch.zeros(n, dtype=torch.int64)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pk.pa_reshape_and_cache(k_new, k_new, kp, vp, slots)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pk.pa_copy_blocks(kp, vp, torch.zeros(1, 2, dtype=torch.int64))
