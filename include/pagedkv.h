@@ -308,7 +308,8 @@ int pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_pool, void* v
  * pa_decode_ex. Pools must be 16-byte aligned.
  * At head_dim 128 the products run on the tensor-core kernel (fp16 MMAs with
  * fp32 accumulate: every E4M3 value is an fp16 value, q is converted to fp16
- * once, exact for |q| within the fp16 range, and P enters as two fp16 terms);
+ * once, exact for |q| within the fp16 range, and P enters as one fp16 term,
+ * within 2^-12 of p, which adds at most 2^-12 * max|v| to an output);
  * at head_dim 64 on the CUDA-core kernel (fp32 dot products).
  */
 int pa_decode_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,

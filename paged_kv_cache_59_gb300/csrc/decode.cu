@@ -505,10 +505,12 @@ pa_decode_partition_kernel(const DecodeParams P) {
 //   O^T[128 x 8]     += V^T . P^T           (A = V^T via ldmatrix.trans; B = P^T,
 //                                            which is S's accumulator layout as it
 //                                            stands; the 8 head rows fill N = 8)
-// P enters as two bf16 terms (P_hi = p truncated, P_lo = the rounded
-// remainder), so the weights keep ~16 significant bits. (A single fp16 P,
-// as the prefill uses, would need V widened to fp16 element by element in
-// registers here, which costs more instructions than the P_lo MMAs save.)
+// With a bf16 cache P enters as two bf16 terms (P_hi = p truncated, P_lo =
+// the rounded remainder), so the weights keep ~16 significant bits. (A single
+// fp16 P, as the prefill uses, would need V widened to fp16 element by element
+// in registers here, which costs more instructions than the P_lo MMAs save.)
+// With an E4M3 cache, whose V codes are widened to fp16 anyway, P enters as
+// one fp16 term, rounded to nearest (within 2^-12 of p).
 // K and V tiles arrive by 2-D TMA in 128B-swizzled layout (16 rows x 64 dims
 // per box), so the ldmatrix row reads are free of bank conflicts.
 namespace mma {
@@ -810,7 +812,10 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
                 pv[k] = pa::fast_exp2(sv[k] - mref);
                 l_run += pv[k];
             }
-            // P as the A operand (rows g; rows g+8 zero): P_hi truncated, P_lo the rounded rest
+            // P as the B operand (tokens of head g). bf16: P_hi truncated and P_lo the
+            // rounded rest, two MMAs (a single bf16 term, within 2^-9 of p, can miss an
+            // absolute 2e-3 on short rows). fp16: one term rounded to nearest, within
+            // 2^-12 of p, one MMA.
             uint32_t ph[2], pl[2];
 #pragma unroll
             for (int n = 0; n < 2; ++n) {
@@ -819,10 +824,9 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
                     ph[n] = __byte_perm(bx, by, 0x7632);
                     pl[n] = pa::float2_to_bf16x2(pv[2 * n] - __uint_as_float(bx & 0xffff0000u),
                                                  pv[2 * n + 1] - __uint_as_float(by & 0xffff0000u));
-                } else {  // fp16 terms: P_hi rounded, P_lo the rounded remainder
+                } else {
                     ph[n] = f2_to_h2(pv[2 * n], pv[2 * n + 1]);
-                    const float2 hf = h2_to_f2(ph[n]);
-                    pl[n] = f2_to_h2(pv[2 * n] - hf.x, pv[2 * n + 1] - hf.y);
+                    pl[n] = 0u;
                 }
             }
             if constexpr (EB == 1) __syncwarp();  // the widened V tile is complete
@@ -846,7 +850,7 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_t(vb + sw_off(row, 2 * mt + dh), a0, a1, a2, a3);
                     mma_full<EB>(o[mt], a0, a1, a2, a3, ph[0], ph[1]);
-                    mma_full<EB>(o[mt], a0, a1, a2, a3, pl[0], pl[1]);
+                    if constexpr (EB == 2) mma_full<EB>(o[mt], a0, a1, a2, a3, pl[0], pl[1]);
                 }
             }
         }
