@@ -100,7 +100,6 @@ struct PrefillParams {
     // of the last partial wave, which are cut into sched[2] equal key ranges
     // (piece-major); CTAs take entries in order from the counter sched[0].
     int4* work;      // entries (item, first key tile, end key tile, partial slot or -1); sched[1] of them
-    int* item_slot;  // [n_items] first partial slot of a cut item, -1 otherwise
     int* sched;      // counter, entries, pieces per cut item, cut items
     int n_items;
     int n_qp;
@@ -717,13 +716,9 @@ __global__ void __launch_bounds__(1024) pa_prefill_plan_kernel(const PrefillPara
     int rank = incl - mine + (wid > 0 ? wsum[wid - 1] : 0);
     for (int it = b0; it < b1; ++it) {
         const int nk = item_tiles<G>(P, it);
-        if (nk <= 0) {
-            P.item_slot[it] = -1;
-            continue;
-        }
+        if (nk <= 0) continue;
         if (rank < whole) {
             P.work[rank] = make_int4(it, 0, nk, -1);
-            P.item_slot[it] = -1;
         } else {
             const int ti = rank - whole;
             for (int sp = 0; sp < S; ++sp) {
@@ -731,7 +726,6 @@ __global__ void __launch_bounds__(1024) pa_prefill_plan_kernel(const PrefillPara
                 piece_range(nk, sp, S, a, b);
                 P.work[whole + sp * R + ti] = make_int4(it, a, b, ti * S + sp);
             }
-            P.item_slot[it] = ti * S;
         }
         ++rank;
     }
@@ -903,17 +897,16 @@ size_t part_bytes(long long n_items, int splits) {
 }
 
 // Balanced mode (splits = 0): partial slots for the cut items (at most 4
-// per CTA), the work list (n_items + 4 * n_cta entries), the item slots and
-// the counters, each part 16-byte aligned.
+// per CTA), the work list (n_items + 4 * n_cta entries) and the counters,
+// each part 16-byte aligned.
 struct BalancedLayout {
-    size_t part, work, item_slot, sched, total;
+    size_t part, work, sched, total;
 };
 BalancedLayout balanced_layout(long long n_items, int n_cta) {
     BalancedLayout b;
     b.part = 0;
     b.work = (size_t)4 * n_cta * 2 * 128 * kPartStride * sizeof(float);
-    b.item_slot = b.work + (size_t)(n_items + 4LL * n_cta) * sizeof(int4);
-    b.sched = b.item_slot + (((size_t)n_items * sizeof(int) + 15) & ~(size_t)15);
+    b.sched = b.work + (size_t)(n_items + 4LL * n_cta) * sizeof(int4);
     b.total = b.sched + 16;
     return b;
 }
@@ -968,13 +961,11 @@ int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_poo
     Pp.splits = splits > 0 ? splits : 1;
     Pp.part = need ? static_cast<float*>(workspace) : nullptr;
     Pp.work = nullptr;
-    Pp.item_slot = nullptr;
     Pp.sched = nullptr;
     if (splits == 0) {
         const BalancedLayout bl = balanced_layout(n_items, n_cta);
         char* w = static_cast<char*>(workspace);
         Pp.work = reinterpret_cast<int4*>(w + bl.work);
-        Pp.item_slot = reinterpret_cast<int*>(w + bl.item_slot);
         Pp.sched = reinterpret_cast<int*>(w + bl.sched);
     }
     Pp.n_items = (int)n_items;

@@ -298,12 +298,12 @@ def test_prefill_workspace_formula_and_errors(capi):
     assert capi.pa_prefill_workspace_bytes(4, 32, 6, 512, 2) == 0   # group 32/6: not supported
     assert capi.pa_prefill_workspace_bytes(0, 32, 8, 512, 2) == 0
     assert capi.pa_prefill_workspace_bytes(4, 32, 8, 512, 65) == 0
-    # balanced (splits 0): 4 partial slots per SM, the work list (items + 4 per SM, 16 bytes each),
-    # the items' slots (rounded to 16 bytes) and 16 bytes of counters; 0 with no device
+    # balanced (splits 0): 4 partial slots per SM, the work list (items + 4 per SM, 16 bytes each)
+    # and 16 bytes of counters; 0 with no device
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 0
     items = pairs * 8 * 4
-    want = (4 * sms * 2 * 128 * 132 * 4 + (items + 4 * sms) * 16 + (items * 4 + 15) // 16 * 16 + 16) if sms else 0
+    want = (4 * sms * 2 * 128 * 132 * 4 + (items + 4 * sms) * 16 + 16) if sms else 0
     assert capi.pa_prefill_workspace_bytes(4, 32, 8, 512, 0) == want
     p = C.c_void_p(4096)
     args = [C.c_void_p(8192), p, p, p, p, p, p, C.c_float(0.1), 32, 8, 128, 16, 2, 4, 512, 16]
