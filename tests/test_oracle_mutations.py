@@ -40,6 +40,12 @@ MUTANTS = [
     ("block_manager.py", "test_oracle_block_manager.py",
      "self.ref[b] -= 1\n        if self.ref[b] == 0:", "self.ref[b] -= 1\n        if self.ref[b] <= 1:",
      "block freed while still referenced"),
+    ("attention.py", "test_oracle_window.py", "lo = max(0, n - 1 - int(window))",
+     "lo = max(0, n - int(window))", "window one position short"),
+    ("cache_ops.py", "test_oracle_cache_and_sizes.py", "kp[blk, :, off, :] = k_new[t]",
+     "kp[blk, :, off, :] = v_new[t]", "V written into the K pool"),
+    ("cache_ops.py", "test_oracle_cache_and_sizes.py", "kp[int(dst)] = kp[int(src)]",
+     "kp[int(src)] = kp[int(dst)]", "block copied the wrong way"),
     ("block_manager.py", "test_oracle_block_manager.py", "if self.ref[last] > 1:", "if self.ref[last] > 2:",
      "write into a block shared by two tables"),
 ]
