@@ -50,8 +50,10 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["tiny_mha", "mha_7b", "gqa_8b", "gqa_70b_cow", "mixed", "gqa_8b_fp8",
                              "swa_mistral", "swap_8b", "prefix_cache"])
-    ap.add_argument("--partition-tokens", type=int, default=0,
-                    help="decode context partition size (0 = library default)")
+    ap.add_argument("--partition-tokens", type=int, default=int(os.environ.get("PA_PARTITION_TOKENS", "0")),
+                    help="decode context partition size (0 = library default; env PA_PARTITION_TOKENS)")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="mark the warm-up and timed regions and every step with NVTX ranges")
     ap.add_argument("--skip-baselines", action="store_true",
                     help="skip the CPU oracle and end-to-end legs (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -320,7 +322,7 @@ def run_ours(args):
     launches_per_step = ((1 if n_dec_new else 0) + ((3 if ws_pf is not None else 1) if has_pf else 0)
                          + 1 + (1 if pk.pa_decode_workspace_bytes(B, H, D, max_ctx, pt) else 0))
 
-    def step(ev_pair=None, pf_pair=None):
+    def step_body(ev_pair=None, pf_pair=None):
         if n_dec_new:
             write_cache()
         if has_pf:
@@ -336,8 +338,21 @@ def run_ours(args):
         if ev_pair is not None:
             ev_pair[1].record(stream)
 
+    nvtx = torch.cuda.nvtx if args.nvtx else None
+
+    def step(ev_pair=None, pf_pair=None):
+        if nvtx is not None:
+            nvtx.range_push("step")
+        step_body(ev_pair, pf_pair)
+        if nvtx is not None:
+            nvtx.range_pop()
+
+    if nvtx is not None:
+        nvtx.range_push("warmup")
     for _ in range(max(args.warmup, 3)):
         step()
+    if nvtx is not None:
+        nvtx.range_pop()
     torch.cuda.synchronize()
     assert pk.pa_get_device_error() == 0
 
@@ -351,10 +366,14 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
         sampler.mark("begin")
+        if nvtx is not None:
+            nvtx.range_push("timed")
         t_start.record(stream)
         for i in range(args.steps):
             step(evs[i], pfe[i])
         t_end.record(stream)
+        if nvtx is not None:
+            nvtx.range_pop()
         torch.cuda.synchronize()
         sampler.mark("end")
         if world > 1:
