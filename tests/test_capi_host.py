@@ -355,3 +355,31 @@ def test_binding_refuses_host_tensors(capi):
         pk.pa_reshape_and_cache(k_new, k_new, kp, vp, slots)
     with pytest.raises(ValueError, match="CUDA tensor"):
         pk.pa_copy_blocks(kp, vp, torch.zeros(1, 2, dtype=torch.int64))
+
+
+@pytest.mark.parametrize("H,Hk,D", [(32, 8, 128), (64, 8, 128), (8, 8, 64), (16, 2, 64), (8, 1, 128)])
+@pytest.mark.parametrize("max_ctx", [513, 1025, 4096, 20000])
+def test_default_workspace_covers_every_decode_path(capi, H, Hk, D, max_ctx):
+    """pa_decode_workspace_bytes(..., 0) is enough for every entry point at its
+    default partition size (512 tokens on the CUDA-core kernel, 1024 on the
+    tensor-core one): with that many bytes each call passes every host check
+    and only then fails for want of a device (PA_ERR_CUDA); the CUDA-core
+    path needs all of it (16 bytes fewer is PA_ERR_WORKSPACE)."""
+    B = 8
+    wsb = capi.pa_decode_workspace_bytes(B, H, D, max_ctx, 0)
+    assert wsb > 0
+    p, q, ws = C.c_void_p(4096), C.c_void_p(1 << 16), C.c_void_p(1 << 24)
+    maxb = (max_ctx + 15) // 16
+
+    def common(n):
+        return (C.c_float(0.1), H, Hk, D, 16, B, maxb, max_ctx, 100000, 0, ws, n, None)
+
+    assert capi.pa_decode_ex(p, q, p, p, p, p, *common(wsb)) == -4
+    assert capi.pa_decode_fp8(p, q, p, p, p, p, p, p, *common(wsb)) == -4
+    assert capi.pa_decode_window(p, q, p, p, p, p, C.c_float(0.1), H, Hk, D, 16, B, maxb, max_ctx, 100000,
+                                 max_ctx, 0, ws, wsb, None) == -4
+    if D == 128:
+        assert capi.pa_decode_tc(p, q, p, p, p, p, *common(wsb)) == -4
+    tensor_default = D == 128 and H // Hk == 8
+    if not tensor_default:  # pa_decode_ex runs the CUDA-core kernel: 512-token partitions, all bytes used
+        assert capi.pa_decode_ex(p, q, p, p, p, p, *common(wsb - 16)) == -3
