@@ -1,0 +1,91 @@
+"""Static check of the device code's waits.
+
+Every wait in a kernel must end: a kernel that spins on a barrier nothing
+completes would hang the GPU. The device code keeps all of its spinning in
+two helpers that give up after a time limit (pa::mbar_wait, with a
+%globaltimer limit, and the prefill's wait_bar, with a 1 s limit and an
+abort flag). This test reads the native sources and checks that:
+
+- the raw mbarrier polls (mbar_try_wait, mbar_try_wait_sleep) are called only
+  inside those two helpers;
+- every loop without a condition is one of the reviewed ones below, each of
+  which ends for the reason given;
+- every call of those helpers in a kernel is made with a result or a limit
+  that is used (mbar_wait calls pass an error word or a limit).
+
+A new unbounded loop or a raw poll elsewhere fails here, on the CPU, before
+it can run on a GPU.
+"""
+import os
+import re
+
+from tests.conftest import ROOT
+
+CSRC = os.path.join(ROOT, "paged_kv_cache_59_gb300", "csrc")
+
+# (file, loop text) -> why it ends
+REVIEWED_UNCONDITIONAL_LOOPS = {
+    ("pa_common.cuh", "for (uint32_t it = 1;; ++it) {"): "mbar_wait: returns once the %globaltimer limit passes",
+    ("prefill.cu", "for (uint32_t it = 1;; ++it) {"): "wait_bar: returns after 1 s or once another role aborted",
+    ("prefill.cu", "for (int seg = 0;; ++seg) {"): "segment loop: breaks when the work-list counter passes its "
+                                                   "end (balanced) or after one segment (per pair)",
+}
+
+
+def _sources():
+    out = {}
+    for f in sorted(os.listdir(CSRC)):
+        if f.endswith((".cu", ".cuh", ".cpp")):
+            src = open(os.path.join(CSRC, f)).read()
+            out[f] = re.sub(r"//[^\n]*", "", src)  # comments removed, lines kept
+    return out
+
+
+def _enclosing_function(src, pos):
+    """Name of the function whose body contains offset pos (by brace depth)."""
+    depth, i = 0, pos
+    while i > 0:
+        i -= 1
+        c = src[i]
+        if c == "}":
+            depth += 1
+        elif c == "{":
+            if depth == 0:
+                head = src[max(0, i - 400):i]
+                m = re.findall(r"([A-Za-z_]\w*)\s*\([^;{}]*\)\s*(?:const\s*)?$", head.rstrip())
+                if m:
+                    return m[-1]
+            else:
+                depth -= 1
+    return None
+
+
+def test_raw_polls_only_inside_the_bounded_helpers():
+    allowed = {("pa_common.cuh", "mbar_wait"), ("prefill.cu", "wait_bar")}
+    for f, src in _sources().items():
+        for m in re.finditer(r"\bmbar_try_wait(?:_sleep)?\s*\(", src):
+            line_start = src.rfind("\n", 0, m.start()) + 1
+            if re.match(r"\s*__device__", src[line_start:m.start()]):  # the poll's own definition
+                continue
+            fn = _enclosing_function(src, m.start())
+            assert (f, fn) in allowed, f"{f}: raw mbarrier poll in {fn}"
+
+
+def test_unconditional_loops_are_reviewed():
+    found = set()
+    for f, src in _sources().items():
+        for m in re.finditer(r"for\s*\([^;)]*;\s*;[^)]*\)\s*\{|while\s*\(\s*(?:true|1)\s*\)\s*\{", src):
+            found.add((f, re.sub(r"\s+", " ", m.group(0)).strip()))
+    assert found == set(REVIEWED_UNCONDITIONAL_LOOPS), found ^ set(REVIEWED_UNCONDITIONAL_LOOPS)
+
+
+def test_helpers_give_up():
+    src = _sources()
+    common = src["pa_common.cuh"]
+    body = common[common.index("bool mbar_wait("):]
+    body = body[:body.index("\n}\n")]
+    assert "globaltimer_ns()" in body and "limit_ns" in body and "return false" in body
+    pf = src["prefill.cu"]
+    body = pf[pf.index("bool wait_bar("):]
+    body = body[:body.index("\n}\n")]
+    assert "PA_WAIT_LIMIT_NS" in body and "abort_flag" in body and "return false" in body
