@@ -184,6 +184,9 @@ int pa_decode_tc(void* out, const void* q, const void* k_pool, const void* v_poo
  *    overlap on the GPU race on it.
  *  - The first call on a device (with that device current) looks up the
  *    array's device address; make that first call before any stream capture.
+ *    The lookup is cached per device and per context, and is thread-safe;
+ *    after a device reset the first call in the new context looks the
+ *    address up again (and the array's contents start over).
  */
 int pa_decode_noalloc(void* out, const void* q, const void* k_pool, const void* v_pool,
                       const int32_t* block_tables, const int32_t* context_lens, float scale,
@@ -214,10 +217,22 @@ int pa_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_poo
  * Bit copy. Destinations must be distinct and must not be sources of other
  * pairs. A pair outside [0, num_blocks) sets PA_DEVERR_PAIR and is skipped.
  *  block_mapping int64 [n_pairs][2] (src, dst), device memory
+ * The pools are bf16 (2-byte elements); an fp8 pool takes pa_copy_blocks_ex.
  */
 int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs,
                    int n_kv_heads, int head_dim, int block_size, int num_blocks,
                    pa_stream_t stream);
+
+/*
+ * pa_copy_blocks for a pool of either element size: elem_bytes 2 for a bf16
+ * pool (the same as pa_copy_blocks), 1 for an fp8 (E4M3) pool, whose blocks
+ * hold n_kv_heads * 16 * head_dim bytes. Any other elem_bytes returns
+ * PA_ERR_INVALID_ARG. Pools 16-byte aligned. The copy-on-write pairs the
+ * block manager emits do not depend on the cache's element type.
+ */
+int pa_copy_blocks_ex(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs,
+                      int n_kv_heads, int head_dim, int block_size, int elem_bytes, int num_blocks,
+                      pa_stream_t stream);
 
 /* ----------------------------------------------------- swap (preemption) */
 

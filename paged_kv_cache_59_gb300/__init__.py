@@ -267,15 +267,22 @@ def pa_decode_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, contex
 
 
 def pa_copy_blocks(k_pool, v_pool, block_mapping, stream=None) -> None:
-    """block_mapping int64 [n][2] (src, dst) on the device: dst block := src block."""
+    """block_mapping int64 [n][2] (src, dst) on the device: dst block := src block.
+    The pools may be bf16 or fp8 (uint8 E4M3 codes); the element size is read
+    from k_pool."""
     torch = _torch()
     num_blocks, n_kv_heads, block_size, head_dim = k_pool.shape
     n_pairs = block_mapping.shape[0] if block_mapping.numel() else 0
-    st = load().pa_copy_blocks(
-        _ptr(k_pool, "k_pool", bf16=True), _ptr(v_pool, "v_pool", bf16=True),
-        _ptr(block_mapping, "block_mapping", dtype=torch.int64) if n_pairs else C.c_void_p(None),
-        n_pairs, n_kv_heads, head_dim, block_size, num_blocks, _stream(stream))
-    check("pa_copy_blocks", st)
+    if k_pool.dtype == torch.uint8:
+        kp, vp_, eb = _fp8_pool(k_pool, "k_pool"), _fp8_pool(v_pool, "v_pool"), 1
+    else:
+        kp, vp_, eb = _ptr(k_pool, "k_pool", bf16=True), _ptr(v_pool, "v_pool", bf16=True), 2
+    if v_pool.dtype != k_pool.dtype or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("k_pool and v_pool must have the same shape and dtype")
+    st = load().pa_copy_blocks_ex(
+        kp, vp_, _ptr(block_mapping, "block_mapping", dtype=torch.int64) if n_pairs else C.c_void_p(None),
+        n_pairs, n_kv_heads, head_dim, block_size, eb, num_blocks, _stream(stream))
+    check("pa_copy_blocks_ex", st)
 
 
 def pa_prefill_paged(out, q, k_pool, v_pool, block_tables, context_lens, q_start_loc,

@@ -48,6 +48,7 @@ SIGNATURES = {
                                 i32, vp]),
     "pa_reshape_and_cache": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     "pa_copy_blocks": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp]),
+    "pa_copy_blocks_ex": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
     "pa_decode_window": (i32, [vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32, i32,
                                i32, i32, vp, C.c_size_t, vp]),
     "pa_swap_out_blocks": (i32, [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp]),

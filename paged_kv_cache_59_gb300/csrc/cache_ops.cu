@@ -251,10 +251,11 @@ extern "C" int pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_po
                          cph, (long long)num_blocks * kBS, err);
 }
 
-extern "C" int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs,
-                              int n_kv_heads, int head_dim, int block_size, int num_blocks,
-                              pa_stream_t stream) {
+namespace {
+int copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs, int n_kv_heads,
+                int head_dim, int block_size, int elem_bytes, int num_blocks, pa_stream_t stream) {
     if (n_pairs < 0 || n_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (elem_bytes != 1 && elem_bytes != 2) return PA_ERR_INVALID_ARG;
     if (block_size != kBS) return PA_ERR_UNSUPPORTED;
     if (head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
     if (n_pairs == 0) return PA_OK;
@@ -265,7 +266,9 @@ extern "C" int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_m
         return PA_ERR_INVALID_ARG;
     unsigned int* err = pa_device_error_ptr();
     if (!err) return PA_ERR_CUDA;
-    const long long chunks = (long long)n_kv_heads * kBS * head_dim / 8;
+    // 16-byte chunks per block: n_kv_heads * 16 tokens * head_dim * elem_bytes
+    // (a multiple of 16 for every head_dim that is a multiple of 8)
+    const long long chunks = (long long)n_kv_heads * kBS * head_dim * elem_bytes / 16;
     if (chunks > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     const int threads = 256;
     int slices = (int)((chunks + threads - 1) / threads);
@@ -275,4 +278,19 @@ extern "C" int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_m
         static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), block_mapping, (int)chunks, num_blocks,
         err);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" int pa_copy_blocks(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs,
+                              int n_kv_heads, int head_dim, int block_size, int num_blocks,
+                              pa_stream_t stream) {
+    return copy_blocks(k_pool, v_pool, block_mapping, n_pairs, n_kv_heads, head_dim, block_size, 2, num_blocks,
+                       stream);
+}
+
+extern "C" int pa_copy_blocks_ex(void* k_pool, void* v_pool, const int64_t* block_mapping, int n_pairs,
+                                 int n_kv_heads, int head_dim, int block_size, int elem_bytes, int num_blocks,
+                                 pa_stream_t stream) {
+    return copy_blocks(k_pool, v_pool, block_mapping, n_pairs, n_kv_heads, head_dim, block_size, elem_bytes,
+                       num_blocks, stream);
 }

@@ -84,6 +84,12 @@ def test_cache_ops_argument_errors(capi):
     assert capi.pa_copy_blocks(p, p, p, 3, 2, 64, 4, 16, None) == -2
     assert capi.pa_copy_blocks(p, p, p, 0, 2, 64, 16, 16, None) == 0
     assert capi.pa_copy_blocks(p, p, C.c_void_p(12), 3, 2, 64, 16, 16, None) == -1
+    # element size: 1 (fp8) and 2 (bf16) only
+    for eb in (0, 3, 4, -1):
+        assert capi.pa_copy_blocks_ex(p, p, p, 3, 2, 64, 16, eb, 16, None) == -1
+    assert capi.pa_copy_blocks_ex(p, p, p, 0, 2, 64, 16, 1, 16, None) == 0
+    assert capi.pa_copy_blocks_ex(p, p, p, 3, 2, 64, 4, 1, 16, None) == -2
+    assert capi.pa_copy_blocks_ex(C.c_void_p(72), p, p, 3, 2, 64, 16, 1, 16, None) == -1
 
 
 def test_fp8_argument_errors_need_no_device(capi):

@@ -80,3 +80,41 @@ def test_copy_blocks_flags_bad_pair(pk):
     ek, _ = o_copy(kpool, kpool, pairs[:1])
     assert np.array_equal(host_bits(kp), ek)
     check_device_error(8)                        # PA_DEVERR_PAIR
+
+
+@pytest.mark.parametrize("D,Hk", [(64, 8), (128, 8), (128, 2)])
+def test_copy_blocks_fp8_pool_bit_exact(pk, D, Hk):
+    """Copy-on-write in an E4M3 pool (1-byte elements): the block size in
+    bytes is half the bf16 one, so a copy sized for bf16 would move the wrong
+    bytes and, for a destination in the upper half of the pool, write past its
+    end. Destinations here sit in the upper half and at the last block."""
+    torch = torch_cuda()
+    rng = np.random.default_rng(700 + D + Hk)
+    nb = 48
+    kpool = rng.integers(0, 256, size=(nb, Hk, 16, D), dtype=np.uint8)
+    vpool = rng.integers(0, 256, size=(nb, Hk, 16, D), dtype=np.uint8)
+    pairs = np.array([[3, 30], [3, 47], [7, 40], [39, 0], [12, 25]], dtype=np.int64)
+    # guard bytes after each pool catch a copy that runs past the end
+    guard = 4096
+    kbuf = torch.full((nb * Hk * 16 * D + guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    vbuf = torch.full((nb * Hk * 16 * D + guard,), 0x5A, dtype=torch.uint8, device="cuda")
+    kp = kbuf[: nb * Hk * 16 * D].view(nb, Hk, 16, D)
+    vp = vbuf[: nb * Hk * 16 * D].view(nb, Hk, 16, D)
+    kp.copy_(torch.from_numpy(kpool))
+    vp.copy_(torch.from_numpy(vpool))
+    pk.pa_copy_blocks(kp, vp, dev(pairs))
+    ek, ev = o_copy(kpool, vpool, pairs)
+    assert np.array_equal(kp.cpu().numpy(), ek)
+    assert np.array_equal(vp.cpu().numpy(), ev)
+    assert bool((kbuf[nb * Hk * 16 * D:] == 0xA5).all()) and bool((vbuf[nb * Hk * 16 * D:] == 0x5A).all())
+    check_device_error(0)
+
+
+def test_copy_blocks_fp8_flags_bad_pair(pk):
+    kpool = (np.arange(8 * 2 * 16 * 64) % 251).astype(np.uint8).reshape(8, 2, 16, 64)
+    pairs = np.array([[1, 2], [5, 8], [-1, 3]], dtype=np.int64)
+    kp, vp = dev(kpool), dev(kpool.copy())
+    pk.pa_copy_blocks(kp, vp, dev(pairs))
+    ek, _ = o_copy(kpool, kpool, pairs[:1])
+    assert np.array_equal(kp.cpu().numpy(), ek)
+    check_device_error(8)                        # PA_DEVERR_PAIR
