@@ -1285,29 +1285,26 @@ extern "C" int pa_decode(void* out, const void* q, const void* k_pool, const voi
 //
 // Host code cannot use the array's name as a device address (on the host it
 // only names a stand-in). The first call on each device, with that device
-// current, resolves the real address with cudaGetSymbolAddress and caches
-// it; make that first call before any stream capture on that device.
+// current, resolves the real address with cudaGetSymbolAddress and caches it
+// (thread-safe, per device and per context: after a device reset the new
+// context's address is looked up again on its first call); make that first
+// call before any stream capture on that device.
 static constexpr size_t kNoAllocScratchBytes = 32ull << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-static void* g_noalloc_scratch_addr[64] = {nullptr};
 
 extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_pool, const void* v_pool,
                                  const int32_t* block_tables, const int32_t* context_lens, float scale,
                                  int n_heads, int n_kv_heads, int head_dim, int block_size, int n_seqs,
                                  int max_blocks_per_seq, int max_context_len, int num_blocks,
                                  pa_stream_t stream) {
+    static PaSymbolCache* cache = pa_symbol_cache_new();
     if (n_seqs < 0 || n_heads <= 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
     if (n_seqs > 0 && max_context_len > 0 &&
         pa_decode_workspace_bytes(n_seqs, n_heads, head_dim, max_context_len, 0) > kNoAllocScratchBytes)
         return PA_ERR_WORKSPACE;  // this batch needs more scratch than the fixed array holds
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
-    if (!g_noalloc_scratch_addr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return PA_ERR_CUDA;
-        g_noalloc_scratch_addr[dev] = ptr;
-    }
+    void* scratch = pa_symbol_address(cache, &g_noalloc_scratch);
+    if (!scratch) return PA_ERR_CUDA;
     return pa_decode_ex(out, q, k_pool, v_pool, block_tables, context_lens, scale, n_heads, n_kv_heads,
                         head_dim, block_size, n_seqs, max_blocks_per_seq, max_context_len, num_blocks, 0,
-                        g_noalloc_scratch_addr[dev], kNoAllocScratchBytes, stream);
+                        scratch, kNoAllocScratchBytes, stream);
 }

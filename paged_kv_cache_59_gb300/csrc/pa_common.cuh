@@ -16,6 +16,15 @@
 // word lives in status.cu). Returns nullptr if the runtime call fails.
 unsigned int* pa_device_error_ptr();
 
+// Host: device address of a file-scope __device__ variable on the current
+// device (host code cannot use the variable's name as a device address).
+// The address is looked up with cudaGetSymbolAddress once per device and
+// context and cached in *cache; a new context on the device (after a device
+// reset) is looked up again. Thread-safe. nullptr if a runtime call fails.
+struct PaSymbolCache;
+PaSymbolCache* pa_symbol_cache_new();
+void* pa_symbol_address(PaSymbolCache* cache, const void* symbol);
+
 // Host-side helpers shared by the entry points.
 static inline bool pa_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -4,7 +4,10 @@
 // slot outside the pool, a bulk-copy wait that timed out) set a bit in this
 // word and skip the work instead of trapping, so the CUDA context stays
 // usable. The host reads and clears it with pa_get_device_error().
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "pa_common.cuh"
 
@@ -12,18 +15,64 @@ __device__ unsigned int g_pa_device_error = 0;
 
 namespace {
 constexpr int kMaxDevices = 64;
-unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+std::once_flag g_ctx_fns_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Driver entry points resolved through the runtime (the library does not
+// link libcuda directly).
+void resolve_ctx_fns() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
+}
+
+// Unique id of the calling thread's current context; 0 if there is none yet
+// (or the driver cannot tell).
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_fns_once, resolve_ctx_fns);
+    CUcontext c = nullptr;
+    if (!g_ctx_get_current || g_ctx_get_current(&c) != CUDA_SUCCESS || !c) return 0;
+    unsigned long long id = 0;
+    if (!g_ctx_get_id || g_ctx_get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+}  // namespace
+
+struct PaSymbolCache {
+    std::mutex mu;
+    unsigned long long ctx_id[kMaxDevices] = {};
+    void* addr[kMaxDevices] = {};
+};
+
+PaSymbolCache* pa_symbol_cache_new() { return new PaSymbolCache(); }  // lives until the process exits
+
+void* pa_symbol_address(PaSymbolCache* cache, const void* symbol) {
+    int dev = 0;
+    if (!cache || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    const unsigned long long id = current_context_id();
+    std::lock_guard<std::mutex> lock(cache->mu);
+    if (id != 0 && cache->ctx_id[dev] == id && cache->addr[dev]) return cache->addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) return nullptr;
+    // the lookup makes the device's primary context current if none was
+    cache->ctx_id[dev] = id != 0 ? id : current_context_id();
+    cache->addr[dev] = p;
+    return p;
 }
 
 unsigned int* pa_device_error_ptr() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!g_err_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_pa_device_error) != cudaSuccess) return nullptr;
-        g_err_ptr[dev] = static_cast<unsigned int*>(p);
-    }
-    return g_err_ptr[dev];
+    static PaSymbolCache* cache = pa_symbol_cache_new();
+    return static_cast<unsigned int*>(pa_symbol_address(cache, &g_pa_device_error));
 }
 
 extern "C" int pa_get_device_error(int* flags_out) {
