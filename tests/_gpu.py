@@ -39,6 +39,23 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+# Every comparison's error figures, for the session summary printed by
+# tests/conftest.py: per test, the number of outputs compared, the largest
+# absolute error, the largest relative error over |ref| > 1e-2, and the
+# largest ratio of error to the element-wise bound.
+PARITY_STATS = {}
+
+
+def _record(what: str, n: int, max_abs: float, max_rel: float, worst_frac: float) -> None:
+    import os
+    test = os.environ.get("PYTEST_CURRENT_TEST", what).split(" ")[0]
+    s = PARITY_STATS.setdefault(test, {"n": 0, "max_abs": 0.0, "max_rel": 0.0, "bound_frac": 0.0})
+    s["n"] += n
+    s["max_abs"] = max(s["max_abs"], max_abs)
+    s["max_rel"] = max(s["max_rel"], max_rel)
+    s["bound_frac"] = max(s["bound_frac"], worst_frac)
+
+
 def assert_attention_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
     got = bf16_to_f64(gpu_bits)
     assert got.shape == ref.shape, (got.shape, ref.shape)
@@ -51,8 +68,11 @@ def assert_attention_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str = ""
         raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance; worst at {i}: "
                              f"gpu={got[i]!r} ref={ref[i]!r}")
     big = np.abs(ref) > 1e-2
-    return {"max_abs": float(err.max()) if err.size else 0.0,
-            "max_rel": float((err[big] / np.abs(ref[big])).max()) if big.any() else 0.0}
+    stats = {"max_abs": float(err.max()) if err.size else 0.0,
+             "max_rel": float((err[big] / np.abs(ref[big])).max()) if big.any() else 0.0,
+             "bound_frac": float((err / bound).max()) if err.size else 0.0}
+    _record(what, int(err.size), stats["max_abs"], stats["max_rel"], stats["bound_frac"])
+    return stats
 
 
 def check_device_error(expected: int = 0) -> None:

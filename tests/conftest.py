@@ -36,3 +36,23 @@ def capi():
     from paged_kv_cache_59_gb300 import _capi
     _b.build()
     return _capi.load()
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Attention parity figures of the GPU tests (the tolerance is applied per
+    element as |gpu - ref| <= 2e-3 + 1e-2 |ref|; the pair of maxima below is
+    reported besides): outputs compared, max-abs over all of them, max-rel
+    over |ref| > 1e-2, and the worst error as a fraction of its bound."""
+    stats = sys.modules.get("tests._gpu")
+    stats = getattr(stats, "PARITY_STATS", None) if stats else None
+    if not stats:
+        return
+    n = sum(s["n"] for s in stats.values())
+    worst_abs = max(stats.items(), key=lambda kv: kv[1]["max_abs"])
+    worst_rel = max(stats.items(), key=lambda kv: kv[1]["max_rel"])
+    worst_frac = max(stats.items(), key=lambda kv: kv[1]["bound_frac"])
+    tr = terminalreporter
+    tr.write_line(f"attention parity: {n} outputs in {len(stats)} tests; "
+                  f"max-abs {worst_abs[1]['max_abs']:.3e} ({worst_abs[0].split('::')[-1]}); "
+                  f"max-rel(|ref|>1e-2) {worst_rel[1]['max_rel']:.3e} ({worst_rel[0].split('::')[-1]}); "
+                  f"worst err/bound {worst_frac[1]['bound_frac']:.3f} ({worst_frac[0].split('::')[-1]})")

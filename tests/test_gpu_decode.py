@@ -181,11 +181,15 @@ def test_gqa_70b_shared_prefix_and_cow(pk):
     wl = make_workload("gqa_70b_cow")
     before, kp, vp = _step(pk, wl)
     ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    # every query head of 16 sequences: the 10 that diverge below and 6 others
     rng = np.random.default_rng(3)
-    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, 100, 20), rng.integers(0, 64, 20))]
+    others0 = np.setdiff1d(np.arange(100), wl.cow_seqs)
+    seqs = sorted(set(int(b) for b in wl.cow_seqs) | set(int(b) for b in rng.choice(others0, 6, replace=False)))
+    assert len(seqs) >= 16
+    rows = [(b, h) for b in seqs for h in range(64)]
     ref = paged_decode_rows(wl.q, ek, ev, wl.dec_tables, wl.dec_ctx, wl.scale, rows)
-    for (b, h), r in ref.items():
-        assert_attention_close(before[b, h], r, f"shared-prefix row {(b, h)}")
+    assert_attention_close(np.stack([before[b, h] for b, h in rows]), np.stack([ref[r] for r in rows]),
+                           "shared-prefix rows (16 sequences x 64 heads)")
     # copy-on-write of the last shared block for 10 sequences, then a divergent write
     pk.pa_copy_blocks(kp, vp, dev(wl.copy_pairs))
     ek2, ev2 = o_copy(ek, ev, wl.copy_pairs)
@@ -197,11 +201,12 @@ def test_gqa_70b_shared_prefix_and_cow(pk):
     after = gpu_decode(pk, wl.q, kp, vp, wl.dec_tables_after_cow, wl.dec_ctx, wl.scale, 4096)
     others = np.setdiff1d(np.arange(100), wl.cow_seqs)
     assert np.array_equal(after[others], before[others])
-    rows = [(int(b), h) for b in wl.cow_seqs for h in (0, 17, 63)]
+    rows = [(int(b), h) for b in wl.cow_seqs for h in range(64)]
     ref2 = paged_decode_rows(wl.q, ek2, ev2, wl.dec_tables_after_cow, wl.dec_ctx, wl.scale, rows)
-    for (b, h), r in ref2.items():
-        assert_attention_close(after[b, h], r, f"diverged row {(b, h)}")
-        assert not np.array_equal(after[b, h], before[b, h])
+    assert_attention_close(np.stack([after[b, h] for b, h in rows]), np.stack([ref2[r] for r in rows]),
+                           "diverged rows (10 sequences x 64 heads)")
+    for b in wl.cow_seqs:   # the divergent token moves every diverged sequence's outputs
+        assert not np.array_equal(after[b], before[b]), f"diverged sequence {int(b)} unchanged"
     check_device_error(0)
 
 

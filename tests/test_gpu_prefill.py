@@ -73,6 +73,33 @@ def test_prefill_hot_logits(pk):
     check_device_error(0)
 
 
+def _group_rows(wl, ek, ev, s, kh, tokens):
+    """Oracle outputs of every query head of KV head kh's group for chunk
+    tokens `tokens` of sequence s: [len(tokens)][G][D]. The oracle gets one KV
+    head's pools and its group's query heads (the head map h // G is then
+    the identity onto that one KV head)."""
+    G = wl.n_heads // wl.n_kv_heads
+    r0 = int(wl.q_start_loc[s])
+    rows = [(r0 + t, g) for t in tokens for g in range(G)]
+    ref = paged_prefill(wl.q_pf[:, kh * G:(kh + 1) * G], ek[:, kh:kh + 1], ev[:, kh:kh + 1], wl.pf_tables,
+                        wl.pf_ctx, wl.q_start_loc, wl.scale, rows=rows)
+    return np.stack([ref[r0 + t] for t in tokens])
+
+
+def _check_group(got, wl, ek, ev, s, kh, tokens, what):
+    G = wl.n_heads // wl.n_kv_heads
+    r0 = int(wl.q_start_loc[s])
+    ref = _group_rows(wl, ek, ev, s, kh, tokens)
+    sel = got[[r0 + t for t in tokens]][:, kh * G:(kh + 1) * G]
+    assert_attention_close(sel, ref, what)
+
+
+def _query_tile(G, which):
+    """Chunk tokens of one complete 128-row query tile (128 / G tokens x G heads)."""
+    qt = 128 // G
+    return list(range(which * qt, (which + 1) * qt))
+
+
 def test_prefill_mixed_workload_sampled_rows(pk):
     wl = make_workload("mixed")
     got = _run(pk, wl)
@@ -84,6 +111,12 @@ def test_prefill_mixed_workload_sampled_rows(pk):
     ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale, rows=rows)
     for r, h in rows:
         assert_attention_close(got[r, h], ref[r, h], f"mixed prefill row {(r, h)}")
+    # complete query tiles: the chunk start of the first sequence, the chunk end of the last
+    G = wl.n_heads // wl.n_kv_heads
+    L = int(wl.q_start_loc[1] - wl.q_start_loc[0])
+    _check_group(got, wl, ek, ev, 0, 1, _query_tile(G, 0), "mixed prefill: chunk-start tile")
+    _check_group(got, wl, ek, ev, len(wl.pf_ctx) - 1, 6, _query_tile(G, L * G // 128 - 1),
+                 "mixed prefill: chunk-end tile")
     check_device_error(0)
 
 
@@ -105,14 +138,51 @@ def test_prefill_split_pieces_match_oracle(pk, case, splits):
     check_device_error(0)
 
 
-def test_prefill_mixed_workload_auto_split_sampled_rows(pk):
+def _balanced_cut(n_pairs, n_cta):
+    """The balanced work list's rule for where whole pairs end: with P
+    non-empty pairs and C CTAs, the last R = P mod C pairs are cut into S key
+    ranges, S in 1..8 with R*S <= 4C minimising ceil(R*S/C)/S + 0.03 S (no
+    cut when S = 1). Returns (first cut pair, S)."""
+    R = n_pairs % n_cta
+    best, S = 2.0, 1
+    for c in range(1, 9):
+        if R * c > 4 * n_cta:
+            break
+        cost = -(-R * c // n_cta) / c + 0.03 * c
+        if cost < best:
+            best, S = cost, c
+    return (n_pairs - R if S > 1 else n_pairs), S
+
+
+def test_prefill_mixed_workload_auto_split_tiles(pk):
+    """Balanced mode on the full mixed batch: every query head of a complete
+    query tile at the chunk start and at the chunk end of every long
+    sequence, both query tiles of the last pair that runs whole and of the
+    first pair cut into key-range pieces, and random rows."""
+    torch = torch_cuda()
     wl = make_workload("mixed")
     got = _run(pk, wl, 0)
     ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    G = wl.n_heads // wl.n_kv_heads
+    Hk = wl.n_kv_heads
+    L = int(wl.q_start_loc[1] - wl.q_start_loc[0])
+    assert all(int(wl.q_start_loc[i + 1] - wl.q_start_loc[i]) == L for i in range(len(wl.pf_ctx)))
+    for s in range(len(wl.pf_ctx)):
+        _check_group(got, wl, ek, ev, s, (2 * s) % Hk, _query_tile(G, 0), f"seq {s}: chunk-start tile")
+        _check_group(got, wl, ek, ev, s, (2 * s + 1) % Hk, _query_tile(G, L * G // 128 - 1),
+                     f"seq {s}: chunk-end tile")
+    # pair items in work-list order: (sequence * Hk + kv head) * pairs_per_seq + pair
+    n_qp = L * G // 256
+    n_items = len(wl.pf_ctx) * Hk * n_qp
+    first_cut, S = _balanced_cut(n_items, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert S > 1 and 0 < first_cut < n_items, "the mixed batch's last partial wave is expected to be cut"
+    for it, what in ((first_cut - 1, "last whole pair"), (first_cut, f"first pair cut into {S} pieces")):
+        s, kh, qp = it // (Hk * n_qp), (it // n_qp) % Hk, it % n_qp
+        toks = list(range(qp * 256 // G, (qp + 1) * 256 // G))
+        _check_group(got, wl, ek, ev, s, kh, toks, f"{what} (seq {s}, kv head {kh}, pair {qp})")
     rng = np.random.default_rng(6)
     n_rows = int(wl.q_start_loc[-1])
     rows = [(int(r), int(h)) for r, h in zip(rng.integers(0, n_rows, 24), rng.integers(0, 32, 24))]
-    rows += [(0, 0), (511, 31), (512, 5), (n_rows - 1, 7)]
     ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale, rows=rows)
     for r, h in rows:
         assert_attention_close(got[r, h], ref[r, h], f"mixed split prefill row {(r, h)}")
