@@ -38,7 +38,14 @@ FALLBACK_HBM_GBS = 6800.0
 DEFAULT_WORKLOAD = "gqa_8b"
 WORKLOAD_LAYERS = {"tiny_mha": 1, "mha_7b": 32, "gqa_8b": 32, "gqa_70b_cow": 80, "mixed": 32,
                    "gqa_8b_fp8": 32, "swa_mistral": 32}
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_decode_partition_gqa8b.md")
+# ncu DRAM bytes per launch of the decode partition kernel, per workload,
+# each tagged with the hash of the kernel sources it was taken on (written
+# from an ncu CSV by `bench.py --record-traffic CSV --workload W`)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+TRAFFIC_KERNELS = ("pa_decode_partition_kernel", "pa_decode_mma_kernel")
+TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none "
+                   "-k regex:'pa_decode_(partition|mma)' -s 5 -c 2 --csv --log-file dram_{w}.csv "
+                   "python bench.py --workload {w} --steps 20 --warmup 3 --skip-baselines")
 
 
 def parse_args():
@@ -59,6 +66,11 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="host time the reference arm (the oracle) aims to spend on warmup + steps")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="store the decode kernel's ncu DRAM bytes per launch from CSV for --workload "
+                         "in profiles/traffic.json, then exit")
+    ap.add_argument("--no-prefill-leg", action="store_true",
+                    help="skip the tensor-core prefill leg of the default run")
     return ap.parse_args()
 
 
@@ -98,13 +110,16 @@ def measured_peaks():
 
 
 def measured_tensor_peak():
-    """Sustained dense bf16 TFLOP/s (a kernel timed inside a long step)."""
+    """Dense bf16 TFLOP/s measured as a burst: the prefill is timed over tens
+    of milliseconds, not a seconds-long loop under the power cap (fp16, which
+    its P.V product uses, has the same dense rate)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d.get("bf16_tflops_sustained", 1700.0)), "measured sustained bf16 TFLOP/s"
-    return 1700.0, "fallback sustained bf16 TFLOP/s"
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured bf16 dense TFLOP/s, burst (MEASURED_PEAKS.json bf16_tflops)"
+    return 1900.0, "fallback bf16 dense TFLOP/s, burst"
 
 
 def unique_kv_tokens(tables, ctx, window=None) -> int:
@@ -122,34 +137,67 @@ def unique_kv_tokens(tables, ctx, window=None) -> int:
     return int(np.unique(np.concatenate(ids)).size) if ids else 0
 
 
+TRAFFIC_SOURCES = ("decode.cu", "pa_common.cuh", "tc_sm100.cuh")
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cu", "pa_common.cuh", "tc_sm100.cuh"):
+    for f in TRAFFIC_SOURCES:
         with open(os.path.join(ROOT, "paged_kv_cache_59_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload: str = None):
-    """DRAM bytes per launch of the partition kernel from the committed ncu
-    summary (the default workload's line, or the line tagged with the
-    workload), if it was taken on the current kernel source (else None)."""
-    if not os.path.exists(PROFILE_SUMMARY):
+    """DRAM bytes (read + write) per launch of the decode partition kernel
+    for this workload from the committed ncu figures, if they were taken on
+    the current kernel sources (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
         return None
-    tag = "bench_traffic:" if workload in (None, DEFAULT_WORKLOAD) else f"bench_traffic[{workload}]:"
-    vals = {}
-    with open(PROFILE_SUMMARY) as f:
-        for line in f:
-            if line.startswith(tag):
-                for kv in line.split(":", 1)[1].split():
-                    k, _, v = kv.partition("=")
-                    vals[k] = v
-    if vals.get("source_sha") != kernel_source_sha():
+    with open(TRAFFIC_FILE) as f:
+        entry = json.load(f).get("entries", {}).get(workload or DEFAULT_WORKLOAD)
+    if not entry or entry.get("source_sha") != kernel_source_sha():
         return None
-    try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    return float(entry["dram_bytes_per_launch"])
+
+
+def record_traffic(csv_path: str, workload: str) -> dict:
+    """Reads an ncu CSV (dram__bytes_read.sum and dram__bytes_write.sum of
+    the decode partition kernel's launches) and stores the mean bytes per
+    launch for `workload` in the traffic file, tagged with the current kernel
+    source hash."""
+    import csv
+    per_launch = {}
+    names = {}
+    with open(csv_path) as f:
+        rows = [ln for ln in f if ln.startswith('"')]
+    for row in csv.DictReader(rows):
+        name = row.get("Kernel Name", "")
+        if not any(k in name for k in TRAFFIC_KERNELS):
+            continue
+        if row.get("Metric Name") not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}[row.get("Metric Unit", "byte")]
+        val = float(row["Metric Value"].replace(",", "")) * scale
+        per_launch[row["ID"]] = per_launch.get(row["ID"], 0.0) + val
+        names[row["ID"]] = name
+    if not per_launch:
+        raise SystemExit(f"{csv_path}: no DRAM figures of {TRAFFIC_KERNELS}")
+    data = {"entries": {}}
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
+    data["source_files"] = ["paged_kv_cache_59_gb300/csrc/" + f for f in TRAFFIC_SOURCES]
+    entry = {"kernel": sorted(set(n.split("(")[0] for n in names.values())),
+             "launches": len(per_launch),
+             "dram_bytes_per_launch": round(sum(per_launch.values()) / len(per_launch)),
+             "source_sha": kernel_source_sha(),
+             "command": TRAFFIC_COMMAND.format(w=workload)}
+    data.setdefault("entries", {})[workload] = entry
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return entry
 
 
 class ClockSampler:
@@ -399,6 +447,7 @@ def run_ours(args):
     t_max = reduce_max_ms(total_ms, dist if world > 1 else None, dev)
     ms_per_step = t_max / args.steps
     graph = graph_replay(torch, step, args.steps, kv_bytes)
+    clocks = merge_clocks(clocks, clock_leg(torch, graph_replay.replay or step, sampler.gpu))
     value = whole_job_gbps(kv_bytes, args.steps, world, t_max)
 
     # roofline of the decode call (partition kernel + merge kernel)
@@ -467,24 +516,12 @@ def run_ours(args):
         "graph_replay": graph,
     }
     if has_pf:
-        pf_ms = timed_region.pf_ms
-        pf_avg = sum(pf_ms) / len(pf_ms)
-        tpk, tpk_kind = measured_tensor_peak()
         result["config"]["step"] = ("pa_reshape_and_cache (decode tokens + chunk tokens) + "
                                     "pa_prefill_paged_ex (tcgen05, balanced) + pa_decode")
         result["config"]["prefill_flop_per_step"] = pf_flops
         result["config"]["prefill_splits"] = ("balanced (0): %d bytes of workspace" % ws_pf.numel()
                                               if ws_pf is not None else 1)
-        result["prefill_roofline"] = {
-            "bound": "tensor",
-            "kernel": "pa_prefill_plan_kernel + pa_prefill_tc_kernel (one CTA per SM) + pa_prefill_merge_cut_kernel",
-            "achieved": round(pf_flops / (pf_avg / 1e3) / 1e12, 1), "peak": tpk,
-            "peak_source": tpk_kind, "unit": "TFLOP/s",
-            "frac": round(pf_flops / (pf_avg / 1e3) / 1e12 / tpk, 4),
-            "launch_ms_avg": round(pf_avg, 4),
-            "launch_ms_median": round(sorted(pf_ms)[len(pf_ms) // 2], 4),
-            "note": "algorithmic FLOPs 4*D*H*sum(positions attended); the kernel also runs the "
-                    "masked halves of the diagonal tiles"}
+        result["prefill_roofline"] = prefill_roofline(pf_flops, timed_region.pf_ms, ws_pf)
 
     if not args.skip_baselines:
         result["e2e"] = run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world,
@@ -494,6 +531,17 @@ def run_ours(args):
             # an oracle process holds its own host copy of the pools plus numpy's working arrays
             child_bytes = int(1.2 * 2 * kp.numel() * kp.element_size()) + (256 << 20)
             result["cpu_baseline"] = run_cpu_baseline(args.workload, args.cpu_seconds, child_bytes)
+            if has_pf:
+                result["prefill_roofline"]["cpu_baseline"] = run_cpu_prefill_baseline(args.cpu_seconds,
+                                                                                      child_bytes)
+    if not has_pf and args.workload == DEFAULT_WORKLOAD and not args.no_prefill_leg:
+        # the tensor-core row of the path, after the decode legs; the decode
+        # batch's pools are freed first (the prefill leg brings its own)
+        del kp, vp
+        torch.cuda.empty_cache()
+        result["prefill_roofline"] = prefill_leg(args, pk, torch, dev, sampler.gpu)
+        result["gpu_launches_prefill_leg"] = result["prefill_roofline"]["calls_timed"] * \
+            result["prefill_roofline"]["launches_per_call"]
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -525,10 +573,132 @@ def graph_replay(torch, step, n, kv_bytes):
         b.record()
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / n
+        graph_replay.replay = g.replay
         return {"ms_per_step": round(ms, 5), "value": round(kv_bytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s",
                 "how": f"the step captured once as a CUDA graph, {n} replays back to back"}
     except Exception as e:  # report, do not hide
+        graph_replay.replay = None
         return {"error": str(e)[-200:]}
+
+
+def clock_leg(torch, fn, gpu, seconds=1.2):
+    """SM clock under load: fn (one step, or one graph replay) run back to back
+    for at least `seconds` while nvidia-smi samples the clocks. Not part of
+    the timed region; it only shows the clock the kernels run at."""
+    sampler = ClockSampler(gpu)
+    sampler.start()
+    torch.cuda.synchronize()
+    sampler.mark("begin")
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        for _ in range(64):
+            fn()
+        calls += 64
+        torch.cuda.synchronize()
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    sampler.mark("end")
+    c = sampler.stop()
+    return {"sm_mhz": c["sm_mhz"], "sm_max_mhz": c["sm_max_mhz"], "reasons": c["reasons"],
+            "samples": c.get("samples_in_region", 0), "seconds": round(dt, 3), "calls": calls}
+
+
+def merge_clocks(region, leg):
+    """The timed region's clock record, with the load leg's median SM clock
+    standing in when the region was too short for the 50 ms sampler."""
+    out = dict(region)
+    out["load_leg"] = leg
+    if leg and leg.get("sm_mhz") is not None and region.get("samples_in_region", 0) < 3:
+        out["sm_mhz"] = leg["sm_mhz"]
+        out["sm_mhz_source"] = (f"load leg: {leg['samples']} samples over {leg['seconds']} s of back-to-back "
+                                "steps (the timed region is shorter than a few sample periods)")
+        out["reasons"] = sorted(set(region.get("reasons", [])) | set(leg.get("reasons", [])))
+    else:
+        out["sm_mhz_source"] = "timed region"
+    return out
+
+
+def prefill_leg(args, pk, torch, dev, gpu):
+    """The tensor-core contraction of the path, timed in the default run
+    beside the decode step: the mixed workload's chunked prefill (4 sequences
+    x a 512-token causal chunk at 32,768 context, 32 q / 8 KV heads, head_dim
+    128, bf16 cache), one pa_prefill_paged_ex call (balanced: plan, tcgen05
+    main kernel, merge of the cut pairs) per iteration, CUDA events around
+    every call, then a clock leg of >= 1 s of calls."""
+    import numpy as np
+    from workloads import make_workload
+
+    wl = make_workload("mixed", fill="zero", keep_logical=False)
+    H, Hk, D = wl.n_heads, wl.n_kv_heads, wl.head_dim
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    kp, vp = to_dev(wl.k_pool), to_dev(wl.v_pool)
+    del wl.k_pool, wl.v_pool
+    pk.pa_reshape_and_cache(to_dev(wl.new_k), to_dev(wl.new_v), kp, vp, to_dev(wl.slot_mapping))
+    q_pf, tabs, ctx, qsl = to_dev(wl.q_pf), to_dev(wl.pf_tables), to_dev(wl.pf_ctx), to_dev(wl.q_start_loc)
+    out = torch.empty_like(q_pf)
+    max_chunk = int(np.max(np.diff(wl.q_start_loc)))
+    ws = pk.prefill_workspace(q_pf, len(wl.pf_ctx), Hk, max_chunk, 0)
+    flops = 0
+    for si in range(len(wl.pf_ctx)):
+        L = int(wl.q_start_loc[si + 1] - wl.q_start_loc[si]); c = int(wl.pf_ctx[si])
+        flops += 4 * D * H * sum(c - L + i + 1 for i in range(L))
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pk.pa_prefill_paged_ex(out, q_pf, kp, vp, tabs, ctx, qsl, wl.scale, max_chunk, splits=0, workspace=ws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    assert pk.pa_get_device_error() == 0
+    n = max(20, min(args.steps, 100))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    sampler = ClockSampler(gpu)
+    sampler.start()
+    torch.cuda.synchronize()
+    sampler.mark("begin")
+    for a, b in evs:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("end")
+    clocks = merge_clocks(sampler.stop(), clock_leg(torch, call, gpu))
+    assert pk.pa_get_device_error() == 0
+    ms = sorted(a.elapsed_time(b) for a, b in evs)
+    res = prefill_roofline(flops, ms, ws)
+    res.update({"workload": "mixed: 4 x 512-token causal chunk at 32,768 context, 32 q / 8 KV heads, d 128",
+                "calls_timed": n, "launches_per_call": 3 if ws is not None else 1, "clocks": clocks})
+    del kp, vp, q_pf, out, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def prefill_roofline(flops, ms, ws):
+    avg = sum(ms) / len(ms)
+    tpk, tpk_kind = measured_tensor_peak()
+    ms = sorted(ms)
+    return {
+        "bound": "tensor",
+        "kernel": ("pa_prefill_plan_kernel + pa_prefill_tc_kernel (one CTA per SM) + pa_prefill_merge_cut_kernel"
+                   if ws is not None else "pa_prefill_tc_kernel"),
+        "achieved": round(flops / (avg / 1e3) / 1e12, 1), "peak": tpk,
+        "peak_source": tpk_kind, "unit": "TFLOP/s",
+        "frac": round(flops / (avg / 1e3) / 1e12 / tpk, 4),
+        "flop_per_call": flops,
+        "launch_ms_avg": round(avg, 4),
+        "launch_ms_median": round(ms[len(ms) // 2], 4),
+        "launch_ms_p10_p90": [round(ms[len(ms) // 10], 4), round(ms[(9 * len(ms)) // 10], 4)],
+        "note": "algorithmic FLOPs 4*D*H*sum(positions attended); the kernel also runs the "
+                "masked halves of the diagonal tiles; CUDA events around each call"}
 
 
 def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dist, fp8_scales=None):
@@ -719,14 +889,108 @@ print(json.dumps({{"seconds": dt, "tokens": done_tok, "units": n_units, "kv_byte
 """
 
 
-def _oracle_cmd(workload, seconds, per_step, fixed_steps=0, start=0):
+_CPU_PREFILL_CHILD = r"""
+import json, sys, time
+import numpy as np
+sys.path.insert(0, {root!r})
+from workloads import make_workload
+from oracle.attention import paged_prefill
+from oracle.cache_ops import reshape_and_cache
+wl = make_workload("mixed", fill="zero", keep_logical=False)
+H, Hk, D = wl.n_heads, wl.n_kv_heads, wl.head_dim
+G = H // Hk
+budget = {seconds}
+# The unit of work is one chunk row of one KV head's group: its G query heads
+# attend causally over positions 0..p of the sequence through the unchanged
+# oracle, given that KV head's pools (so its gather reads one head). Units
+# cycle over (sequence, KV head, row), rows spread over the chunk. The cache
+# write of the chunk tokens runs once, outside the timed region.
+n_seq = len(wl.pf_ctx)
+n_dec = len(wl.dec_ctx)
+kp, vp = reshape_and_cache(wl.new_k[n_dec:], wl.new_v[n_dec:], wl.k_pool, wl.v_pool,
+                           wl.slot_mapping[n_dec:])
+units = []
+for i in range(0, 512, 37):
+    for s in range(n_seq):
+        for kh in range(Hk):
+            units.append((s, kh, i))
+u = {start} % len(units)
+dt, flops, n_units = 0.0, 0, 0
+while dt < budget:
+    s, kh, i = units[u]
+    u = (u + 1) % len(units)
+    r = int(wl.q_start_loc[s]) + i
+    L = int(wl.q_start_loc[s + 1] - wl.q_start_loc[s])
+    p = int(wl.pf_ctx[s]) - L + i
+    rows = [(r, g) for g in range(G)]
+    t0 = time.perf_counter()
+    paged_prefill(wl.q_pf[:, kh * G:(kh + 1) * G], kp[:, kh:kh + 1], vp[:, kh:kh + 1], wl.pf_tables,
+                  wl.pf_ctx, wl.q_start_loc, wl.scale, rows=rows)
+    dt += time.perf_counter() - t0
+    flops += 4 * D * G * (p + 1)
+    n_units += 1
+print(json.dumps({{"seconds": dt, "flops": flops, "units": n_units}}))
+"""
+
+
+def _oracle_cmd(workload, seconds, per_step, fixed_steps=0, start=0, mode="decode"):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    code = _CPU_CHILD.format(root=ROOT, workload=workload, seconds=seconds, per_step=per_step,
-                             fixed_steps=fixed_steps, start=start)
+    if mode == "prefill":
+        code = _CPU_PREFILL_CHILD.format(root=ROOT, seconds=seconds, start=start)
+    else:
+        code = _CPU_CHILD.format(root=ROOT, workload=workload, seconds=seconds, per_step=per_step,
+                                 fixed_steps=fixed_steps, start=start)
     return [sys.executable, "-c", code], env
+
+
+def run_cpu_prefill_baseline(seconds, bytes_per_child):
+    """The fp64 oracle on sampled chunk rows of the mixed workload's prefill
+    (1 thread, then one single-threaded process per host core), in TFLOP/s of
+    the same algorithmic FLOPs as the GPU figure."""
+    def one(start):
+        return _oracle_cmd("mixed", seconds, 1, start=start, mode="prefill")
+    try:
+        cmd, env = one(0)
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=3600)
+        if r.returncode != 0:
+            raise RuntimeError(r.stderr[-2000:])
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # report, do not hide
+        return {"value": None, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "error": str(e)[-300:]}
+    out = {"value": round(res["flops"] / res["seconds"] / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+           "kind": "oracle",
+           "sample": f"{res['units']} chunk rows x {4} query heads of one KV head (cycled over the 4 "
+                     f"sequences, 8 KV heads and every 37th chunk row) through the fp64 numpy oracle's "
+                     f"causal prefill in {res['seconds']:.1f} s on 1 host thread (BLAS pinned to 1)",
+           "host_logical_cores": os.cpu_count()}
+    cores = os.cpu_count() or 1
+    try:
+        free = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError):
+        free = 0
+    n = max(1, min(cores, int(free // 2 // max(bytes_per_child, 1)))) if free else 1
+    procs = []
+    try:
+        for i in range(n):
+            cmd, env = one(i * 31)
+            procs.append(subprocess.Popen(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True))
+        outs = [p.communicate(timeout=3600) for p in procs]
+        if any(p.returncode != 0 for p in procs):
+            raise RuntimeError(next(e for p, (_, e) in zip(procs, outs) if p.returncode != 0)[-2000:])
+        rs = [json.loads(o.strip().splitlines()[-1]) for o, _ in outs]
+        out["all_cores"] = {"value": round(sum(x["flops"] / x["seconds"] for x in rs) / 1e12, 6),
+                            "unit": "TFLOP/s", "cores": n,
+                            "sample": f"{n} single-threaded oracle processes at once, each timing about "
+                                      f"{seconds:.0f} s of chunk rows; the rate is the sum of theirs"}
+    except Exception as e:  # report, do not hide
+        for p in procs:
+            if p.poll() is None:
+                p.kill()
+        out["all_cores"] = {"value": None, "cores": n, "error": str(e)[-300:]}
+    return out
 
 
 def _oracle_child(workload, seconds, per_step, fixed_steps=0):
@@ -1007,7 +1271,9 @@ def run_prefix_cache(args):
 
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.workload)))
+    elif args.impl == "reference":
         run_reference(args)
     elif args.workload == "swap_8b":
         run_swap(args)
