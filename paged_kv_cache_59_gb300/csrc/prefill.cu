@@ -15,34 +15,38 @@
 // the same (sequence, KV head): both use every K/V tile it loads, and the
 // tensor core alternates between them so that one tile's MMAs run while the
 // other tile's softmax works. Per key tile j of 128 keys (8 blocks of 16),
-// five roles, each waiting only on mbarriers:
+// five roles in 14 warps, each waiting only on mbarriers or, for the
+// hand-over of P, on a named barrier:
 //   - a producer warp moves the 8 K and 8 V blocks with 2-D TMA loads into
-//     128B-swizzled shared memory: three K stages and two V stages, each
+//     128B-swizzled shared memory: two K stages and three V stages, each
 //     refilled as soon as the tensor core is done with it (blocks past the
 //     end of the sequence load out of bounds and arrive as zeros);
-//   - two converter warps rewrite each landed V tile in place as fp16
-//     values of v * 2^-8 (rows past the context, which hold whatever the
-//     pool has there, become zeros);
-//   - an MMA warp issues, per query tile X, S_X = Q_X K_j^T (tcgen05.mma
-//     kind::f16, bf16 in, fp32 accumulator in tensor memory, M = N = 128)
-//     and, once X's softmax has written P, O_X += P V_j (fp16 in: P read
-//     from tensor memory, V as an MN-major shared-memory operand). The MMAs
-//     of one thread execute in issue order, so S_X(j+1) is issued right
-//     behind the PV MMA that still reads P(j) out of the same columns;
+//   - four converter warps (one per scheduler) rewrite each landed V tile in
+//     place as fp16 values of v * 2^-8 (rows past the context, which hold
+//     whatever the pool has there, become zeros);
+//   - one thread of an MMA warp issues, per query tile X, S_X = Q_X K_j^T
+//     (tcgen05.mma kind::f16, bf16 in, fp32 accumulator in tensor memory,
+//     M = N = 128) and, once X's softmax has written P, O_X += P V_j (fp16
+//     in: P read from tensor memory, V as an MN-major shared-memory operand)
+//     with S_X(j+1) right behind it. The MMAs of one thread execute in issue
+//     order, so S_X(j+1) may follow the PV MMA that still reads P(j) out of
+//     the same columns, and the completion of S_X(j+1) covers that PV MMA;
 //   - one softmax warpgroup per query tile (thread = row) reads S_X from
-//     tensor memory twice, a quarter of 32 columns at a time (row maximum,
-//     then exponentials), applies the scale, the causal mask (diagonal tiles
-//     only) and an online softmax in fp32 (base 2) with a lazily updated
-//     maximum (O_X is rescaled in tensor memory only when a row's maximum
-//     grows by more than 8, so un-normalised p <= 2^8), and writes P back
-//     into S_X's columns as fp16 (rounded to nearest: within 2^-12 of p
-//     relative). A bf16 P (within 2^-9) would exceed an absolute error of
-//     2e-3 on short causal rows with cancelling values; the tensor core
-//     takes A and B of one type, hence V in fp16 too. Every bf16 value is
-//     an fp16 value inside fp16's exponent range; the factor 2^-8 moves
-//     that range up to |v| <= 65504 * 2^8 (larger values become infinite
-//     and the output non-finite, which is flagged), at an absolute error of
-//     at most 2^-17 for |v| < 2^-6, where the scaled value is subnormal.
+//     tensor memory once, a quarter of 32 columns at a time, applies the
+//     scale, the causal mask (diagonal tiles only) and an online softmax in
+//     fp32 (base 2) against the row's integer reference maximum m (changed
+//     only on a row's first visible keys or before any p = 2^(s*scale - m)
+//     could leave the fp16 range, so every rescale of O, l and the tile's
+//     earlier P is an exact power of two), and writes P back into S_X's
+//     columns as fp16 (rounded to nearest: within 2^-12 of p relative).
+//     A bf16 P (within 2^-9) would exceed an absolute error of 2e-3 on short
+//     causal rows with cancelling values; the tensor core takes A and B of
+//     one type, hence V in fp16 too. Every bf16 value is an fp16 value
+//     inside fp16's exponent range; the factor 2^-8 moves that range up to
+//     |v| <= 65504 * 2^8 (larger values become infinite and the output
+//     non-finite, which is flagged), at an absolute error of at most 2^-17
+//     for |v| < 2^-6, where the scaled value is subnormal. The four warps
+//     hand P over to the MMA warp through a named barrier (arrive/sync).
 // The normalised output 2^8 O / l is written once at the end.
 //
 // Scheduling. Per-pair mode: one CTA per (pair, KV head, sequence), or per
@@ -52,6 +56,7 @@
 // its barriers between entries; pieces leave partials for a merge kernel.
 #include <type_traits>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "tc_sm100.cuh"
@@ -64,10 +69,10 @@ constexpr int kKT = 128;         // keys per key tile
 constexpr int kBPT = kKT / kBS;  // blocks per key tile
 constexpr int kRows = 128;       // MMA M
 constexpr unsigned kFull = 0xffffffffu;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-constexpr int kKS = 3;  // K tile stages
-constexpr int kVS = 2;  // V tile stages
+constexpr int kKS = 2;  // K tile stages
+constexpr int kVS = 3;  // V tile stages
+constexpr int kThreads = 448;  // 8 softmax warps, MMA warp (8), producer (9), 4 converter warps (10..13)
 // shared memory map; the dynamic shared memory base must be 1024-byte
 // aligned (swizzle atoms of TMA and of the matrix descriptors): checked
 constexpr uint32_t kQ = 0;                      // Q_A, Q_B: 2 x 32 KiB
@@ -133,20 +138,13 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_majo
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// max of three floats in one instruction (sm_100 family)
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
 // Bounded wait (1 s) that also gives up once another role has aborted. A
 // waiting thread sleeps inside try_wait (up to 20 us per try, woken when the
 // phase completes), so idle roles take no issue slots from busy ones.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigned int* err,
                                          volatile int* abort_flag) {
-    if (*abort_flag) return false;
     if (pa::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
     const uint64_t t0 = pa::globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (pa::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
@@ -162,22 +160,22 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigne
 }
 
 template <int G>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
     constexpr int QT = kRows / G;  // chunk tokens per query tile
     extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-    uint64_t* k_full = bars;        // [kKS] K tile landed
-    uint64_t* k_free = bars + 3;    // [kKS] both QKs that read the K stage are done
-    uint64_t* v_full = bars + 6;    // [kVS] V tile landed (bf16)
-    uint64_t* v_free = bars + 8;    // [kVS] PV_B, the last reader of the V stage, is done
-    uint64_t* s_full = bars + 10;   // [2] per query tile
-    uint64_t* p_full = bars + 12;   // [2] per query tile, 4 arrivals (one per warp)
-    uint64_t* pv_done = bars + 14;  // [2] per query tile
-    uint64_t* drain = bars + 16;
-    uint64_t* v_conv = bars + 17;   // [kVS] V tile rewritten as fp16, 2 arrivals (one per converter warp)
-    constexpr int kNumBars = 19;
+    uint64_t* k_full = bars;          // [kKS] K tile landed
+    uint64_t* k_free = k_full + kKS;  // [kKS] QK_B, the last reader of the K stage, is done
+    uint64_t* v_full = k_free + kKS;  // [kVS] V tile landed (bf16)
+    uint64_t* v_free = v_full + kVS;  // [kVS] PV_B, the last reader of the V stage, is done
+    uint64_t* s_full = v_free + kVS;  // [2] per query tile: S_X(j) and every earlier MMA done
+    uint64_t* pv_done = s_full + 2;   // [2] per query tile
+    uint64_t* drain = pv_done + 2;    // every MMA issued in the segment is done
+    uint64_t* v_conv = drain + 1;     // [kVS] V tile rewritten as fp16, 4 arrivals (one per converter warp)
+    constexpr int kNumBars = 2 * kKS + 3 * kVS + 5;
+    static_assert(kNumBars * 8 <= 256, "barrier area");
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
 
@@ -259,11 +257,10 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             for (int i = 0; i < kVS; ++i) {
                 pa::mbar_init(&v_full[i], 1);
                 pa::mbar_init(&v_free[i], 1);
-                pa::mbar_init(&v_conv[i], 2);
+                pa::mbar_init(&v_conv[i], 4);
             }
             for (int x = 0; x < 2; ++x) {
                 pa::mbar_init(&s_full[x], 1);
-                pa::mbar_init(&p_full[x], 4);
                 pa::mbar_init(&pv_done[x], 1);
             }
             pa::mbar_init(drain, 1);
@@ -296,9 +293,9 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
 
         if (warp == 9) {
             // ------------------------------------------------------- TMA producer
-            // K(j) goes to K stage j%3 once both QKs of K(j-3) are done (k_free);
-            // V(j) to V stage j%2 once PV_B(j-2), the last reader of V(j-2), is
-            // done. K(j+1) is issued before V(j): its stage frees first.
+            // K(j) goes to K stage j%2 once both QKs of K(j-2) are done (k_free);
+            // V(j) to V stage j%3 once PV_B(j-3), the last reader of V(j-3), is
+            // done. K(j) is issued before V(j), and V(j) before K(j+1).
             const int32_t* trow = P.tables + (size_t)s * P.max_blocks;
             struct Ids { int ids = -1, group = -1; };  // block ids of key tiles 4g..4g+3, one per lane
             Ids idk, idv;
@@ -334,11 +331,11 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             for (; nk < kKS && nk < n_kt; ++nk) issue_k(nk);
             for (; nv < kVS && nv < n_kt; ++nv) issue_v(nv);
             while (ok && (nk < n_kt || nv < n_kt)) {
-                if (nk < n_kt && nk <= nv + 1) {  // K(nk) replaces K(nk-3)
+                if (nk < n_kt && nk <= nv) {  // K(nk) replaces K(nk-2)
                     ok = wait_bar(&k_free[nk % kKS], (uint32_t)(((nk - kKS) / kKS) & 1), P.err, abort_flag);
                     if (!ok) break;
                     issue_k(nk++);
-                } else {  // V(nv) replaces V(nv-2)
+                } else {  // V(nv) replaces V(nv-3)
                     ok = wait_bar(&v_free[nv % kVS], (uint32_t)(((nv - kVS) / kVS) & 1), P.err, abort_flag);
                     if (!ok) break;
                     issue_v(nv++);
@@ -352,87 +349,99 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 pa::mbar_wait(&v_full[t % kVS], (uint32_t)((t / kVS) & 1), nullptr, 5000000ull);
         } else if (warp == 8) {
             // ---------------------------------------------------------- MMA issuer
+            // One thread issues every MMA. Its waits for data that is normally
+            // ready long before (the V tile's conversion, the next K tile) come
+            // before its wait for a tile's P, so that P.V and the next Q.K^T of a
+            // tile are issued back to back once the softmax hands P over.
             // Matrix descriptors differ only in the start-address field (bits
             // 0-13, byte address / 16); every operand lies inside the shared
             // allocation, so offsets added to the low word never leave the field.
+            // The hand-over of each tile's P is a named barrier (ids 1 and 2, the
+            // four softmax warps arrive, this warp syncs): every segment has
+            // exactly n_kt arrivals of each softmax warpgroup and n_kt syncs here,
+            // also after a failed wait, so neither side can be left waiting.
             const uint64_t dq = tc::smem_desc(pa::smem_u32(sm + kQ), 16, 1024);
             const uint64_t dk = tc::smem_desc(pa::smem_u32(sm + kK0), 16, 1024);
             const uint64_t dv = tc::smem_desc(pa::smem_u32(sm + kV0), 16384, 1024);
             auto at = [](uint64_t d, uint32_t off16) {
                 return ((uint64_t)(uint32_t)(d >> 32) << 32) | (uint32_t)((uint32_t)d + off16);
             };
-            auto issue_qk = [&](int x, int j) {  // S_x = Q_x K_j^T
-                if (lane == 0) {
-                    const uint32_t qo = x * (32768 >> 4), ko = (j % kKS) * (32768 >> 4);
-                    const uint32_t dst = tbase + x * 256;
+            auto issue_qk = [&](int x, int kst) {  // S_x = Q_x K^T, K in stage kst (one thread)
+                const uint32_t qo = x * (32768 >> 4), ko = kst * (32768 >> 4);
+                const uint32_t dst = tbase + x * 256;
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                        tc::mma_bf16(dst, at(dq, qo + o), at(dk, ko + o), ID_QK, ks > 0 ? 1u : 0u);
-                    }
-                    tc::mma_commit(&s_full[x]);
-                    if (x == 1) tc::mma_commit(&k_free[j % kKS]);  // the stage's last reader
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                    tc::mma_bf16(dst, at(dq, qo + o), at(dk, ko + o), ID_QK, ks > 0 ? 1u : 0u);
                 }
-                __syncwarp();
+                if (x == 1) tc::mma_commit(&k_free[kst]);  // the stage's last reader
+                tc::mma_commit(&s_full[x]);
             };
-            auto issue_pv = [&](int x, int j) {  // O_x += P V_j (fp16), P in S_x's columns
-                if (lane == 0) {
-                    const uint32_t vo = (j % kVS) * (32768 >> 4);
-                    const uint32_t pcol = tbase + x * 256, dst = pcol + 128;
+            auto issue_pv = [&](int x, int vst, bool first) {  // O_x += P V (fp16), V in stage vst (one thread)
+                const uint32_t vo = vst * (32768 >> 4);
+                const uint32_t pcol = tbase + x * 256, dst = pcol + 128;
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_bf16_ts(dst, pcol + (ks >> 1) * 32 + (ks & 1) * 8, at(dv, vo + ks * (2048 >> 4)),
-                                        ID_PV, (j > 0 || ks > 0) ? 1u : 0u);  // fp16 operands per ID_PV
-                    tc::mma_commit(&pv_done[x]);
-                    if (x == 1) tc::mma_commit(&v_free[j % kVS]);  // the stage's last reader
-                }
-                __syncwarp();
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16_ts(dst, pcol + (ks >> 1) * 32 + (ks & 1) * 8, at(dv, vo + ks * (2048 >> 4)),
+                                    ID_PV, (!first || ks > 0) ? 1u : 0u);  // fp16 operands per ID_PV
+                if (x == 1) tc::mma_commit(&v_free[vst]);  // the stage's last reader
+                tc::mma_commit(&pv_done[x]);
             };
             // The tensor core runs the MMAs of this thread in issue order, so
             // QK_x(j+1) may follow PV_x(j) (which reads P out of S_x's columns)
             // without a wait.
             bool ok = wait_bar(&k_full[0], 0, P.err, abort_flag);
-            if (ok) {
+            ok = __all_sync(kFull, ok);
+            if (ok && lane == 0) {
                 tc::fence_after_sync();
                 issue_qk(0, 0);
                 issue_qk(1, 0);
             }
-            for (int j = 0; j < n_kt && ok; ++j) {
-                const uint32_t par = (uint32_t)(j & 1);
-                ok = wait_bar(&p_full[0], par, P.err, abort_flag);
-                if (ok) ok = wait_bar(&v_conv[j % kVS], (uint32_t)((j / kVS) & 1), P.err, abort_flag);
-                if (!ok) break;
-                tc::fence_after_sync();
-                issue_pv(0, j);
-                if (j + 1 < n_kt) {
-                    ok = wait_bar(&k_full[(j + 1) % kKS], (uint32_t)(((j + 1) / kKS) & 1), P.err, abort_flag);
-                    if (!ok) break;
-                    issue_qk(0, j + 1);
+            __syncwarp();
+            int kst = 1, kph = 0;  // stage and phase parity of K(j+1)
+            int vst = 0, vph = 0;  // stage and phase parity of V(j)
+            for (int j = 0; j < n_kt; ++j) {
+                const bool more = j + 1 < n_kt;
+                if (ok) ok = wait_bar(&v_conv[vst], (uint32_t)vph, P.err, abort_flag);
+                if (ok && more) ok = wait_bar(&k_full[kst], (uint32_t)kph, P.err, abort_flag);
+                ok = __all_sync(kFull, ok);
+                asm volatile("bar.sync 1, 160;" ::: "memory");  // tile A's P is in tensor memory
+                if (ok && lane == 0) {
+                    tc::fence_after_sync();
+                    issue_pv(0, vst, j == 0);
+                    if (more) issue_qk(0, kst);
                 }
-                ok = wait_bar(&p_full[1], par, P.err, abort_flag);
-                if (!ok) break;
-                tc::fence_after_sync();
-                issue_pv(1, j);
-                if (j + 1 < n_kt) issue_qk(1, j + 1);
+                __syncwarp();
+                asm volatile("bar.sync 2, 160;" ::: "memory");  // tile B's P
+                if (ok && lane == 0) {
+                    tc::fence_after_sync();
+                    issue_pv(1, vst, j == 0);
+                    if (more) issue_qk(1, kst);
+                }
+                __syncwarp();
+                if (++vst == kVS) { vst = 0; vph ^= 1; }
+                if (++kst == kKS) { kst = 0; kph ^= 1; }
             }
             // drain: every issued MMA has completed before the CTA can release its
             // shared and tensor memory (bounded wait)
             if (lane == 0) tc::mma_commit(drain);
             __syncwarp();
             pa::mbar_wait(drain, 0, nullptr, 10000000ull);
-            if (ok) {  // the stages' last frees (never waited for) land before the barriers are reused
+            if (ok && lane == 0) {  // the stages' last frees (never waited for) land before the barriers are reused
                 for (int t = max(0, n_kt - kKS); t < n_kt; ++t)
                     pa::mbar_wait(&k_free[t % kKS], (uint32_t)((t / kKS) & 1), nullptr, 10000000ull);
                 for (int t = max(0, n_kt - kVS); t < n_kt; ++t)
                     pa::mbar_wait(&v_free[t % kVS], (uint32_t)((t / kVS) & 1), nullptr, 10000000ull);
             }
+            __syncwarp();
         } else if (warp >= 10) {
             // ------------------------------------------------------ V converters
-            // Thread t of 64 rewrites the 16-byte chunks t, t + 64, ... of the
-            // landed tile (consecutive threads, consecutive chunks). A chunk holds
+            // Thread t of 128 (four warps, one per scheduler) rewrites the 16-byte
+            // chunks t, t + 128, ... of the landed tile (consecutive threads,
+            // consecutive chunks). A chunk holds
             // 8 consecutive values of one key row: row (chunk % 1024) / 8 of
             // either 64-dim half, wherever the swizzle put the chunk in the row.
-            const int t = threadIdx.x - 320;
+            const int t = threadIdx.x - 320;  // 0..127
             const float2 k2 = make_float2(0.00390625f, 0.00390625f);  // 2^-8
             auto cvt = [&](uint32_t u) {  // bf16 pair -> fp16 pair of v * 2^-8
                 const float2 f = __fmul2_rn(make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)), k2);
@@ -447,8 +456,8 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 uint4* vs = reinterpret_cast<uint4*>(sm + kV0 + (j % kVS) * 32768);
                 const int valid = ctx - kb;  // key rows of this tile inside the context (may exceed 128)
 #pragma unroll 4
-                for (int c = 0; c < 32; ++c) {
-                    const int e = t + 64 * c;
+                for (int c = 0; c < 16; ++c) {
+                    const int e = t + 128 * c;
                     uint4 w = vs[e];
                     if (((e & 1023) >> 3) >= valid) w = make_uint4(0, 0, 0, 0);
                     w.x = cvt(w.x);
@@ -465,6 +474,17 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
             // --------------------------------------- softmax warpgroup of tile x
             // warp w serves TMEM lanes 32*(w%4) .. +31 (rows). After a failed wait
             // (timeout) the warps keep iterating without waiting.
+            //
+            // One pass over S per key tile, a quarter of 32 columns at a time:
+            // p = 2^(s*scale - m) against the row's current reference m, which is
+            // an integer (or -inf before the row has seen a key), so every change
+            // of m rescales by an exact power of two. m changes only when a
+            // quarter's sum of p exceeds 2^15, i.e. before any p could leave the
+            // fp16 range (65504), and on a row's first visible quarter (m = -inf
+            // gives p = inf): the quarter is then recomputed against
+            // m = ceil(max s*scale of the quarter) (its p <= 1), and the P of the
+            // tile's earlier quarters, already in tensor memory, is rescaled in
+            // place (fp16 times a power of two: exact down to the subnormals).
             const int x = warp >> 2;
             const int r = threadIdx.x & 127;  // matrix row = TMEM lane
             const int i = i0 + x * QT + r / G;
@@ -483,83 +503,93 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 // Keys beyond a row's position are masked. Only the tiles on the
                 // diagonal have such keys; a warp takes the masking code only when
                 // one of its rows needs it (a warp-uniform branch), so the other
-                // tiles run the plain loops.
+                // tiles run the plain loop.
                 const bool mask_warp = __any_sync(kFull, kb + kKT - 1 > pos);
                 const int lim0 = pos - kb;  // keys k > lim0 of the tile are not visible
-                // pass 1: row maximum over the 128 scores, a quarter at a time
-                float tmax = -INFINITY;
-                auto pass1 = [&](auto masked) {
-#pragma unroll 1
-                    for (int qd = 0; qd < 4; ++qd) {
-                        uint32_t sr[32];
-                        tc::tmem_ld32(tS + 32 * qd, sr);
-                        tc::tmem_wait_ld();
-                        if constexpr (decltype(masked)::value) {
-                            const int lim = lim0 - 32 * qd;
+                float2 psum2 = make_float2(0.f, 0.f);  // this tile's sum of p against m_used
+                float alpha = 1.f;                     // this tile's rescale of l and O
+                const float2 sc2 = make_float2(sc, sc);
+                // p of one quarter (raw scores in columns 32q..32q+31) -> fp16 pairs;
+                // P of keys 2w, 2w+1 goes to column 32q + w, so a quarter only
+                // overwrites columns it has already read.
+                auto exps = [&](auto masked, const uint32_t (&raw)[32], int qd, uint32_t (&ph)[16]) {
+                    const float2 nm2 = make_float2(-m_used, -m_used);
+                    float2 qs = make_float2(0.f, 0.f);
 #pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                if (k > lim) sr[k] = __float_as_uint(-INFINITY);
+                    for (int w = 0; w < 16; ++w) {
+                        float2 e = __ffma2_rn(make_float2(__uint_as_float(raw[2 * w]), __uint_as_float(raw[2 * w + 1])),
+                                              sc2, nm2);
+                        if constexpr (decltype(masked)::value) {  // masked keys give p = 0 (also for a zero scale)
+                            const int k = 32 * qd + 2 * w;
+                            if (k > lim0) e.x = -INFINITY;
+                            if (k + 1 > lim0) e.y = -INFINITY;
                         }
-                        float mx[4];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) mx[c] = __uint_as_float(sr[c]);
-#pragma unroll
-                        for (int k = 4; k + 8 <= 32; k += 8)
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                mx[c] = max3f(mx[c], __uint_as_float(sr[k + 2 * c]), __uint_as_float(sr[k + 2 * c + 1]));
-                        tmax = max3f(tmax, max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])),
-                                     max3f(__uint_as_float(sr[28]), __uint_as_float(sr[29]),
-                                           fmaxf(__uint_as_float(sr[30]), __uint_as_float(sr[31]))));
+                        e.x = pa::fast_exp2(e.x);
+                        e.y = pa::fast_exp2(e.y);
+                        qs = __fadd2_rn(qs, e);
+                        ph[w] = float2_to_f16x2(e.x, e.y);
                     }
+                    return qs.x + qs.y;
                 };
-                if (mask_warp) pass1(std::true_type{});
-                else pass1(std::false_type{});
-                tmax *= sc;
-                const bool rescale = tmax > m_used + kRescaleThreshold;
-                float alpha = 1.f;
-                if (rescale) {
-                    alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
-                    m_used = tmax;
-                }
-                // pass 2, per quarter of 32 keys: p = 2^(s*scale - m) in fp16.
-                // Quarter q's scores sit in columns 32q..32q+31; P of its keys 2w,
-                // 2w+1 goes to column 32q + w, so a quarter only overwrites columns
-                // it has already read. Both passes loop over quarters without
-                // unrolling: the smaller body keeps the softmax warps out of
-                // instruction-fetch stalls.
-                float2 psum2 = make_float2(0.f, 0.f);
-                const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_used, -m_used);
-                auto pass2 = [&](auto masked) {
+                auto sweep = [&](auto masked) {
 #pragma unroll 1
                     for (int qd = 0; qd < 4; ++qd) {
                         uint32_t raw[32];
                         tc::tmem_ld32(tS + 32 * qd, raw);
                         tc::tmem_wait_ld();
                         uint32_t ph[16];
+                        float qs = exps(masked, raw, qd, ph);
+                        const bool big = !(qs <= 32768.f);  // also inf (no reference yet) and NaN
+                        if (__any_sync(kFull, big)) {
+                            // rare: a new reference for the rows that need one
+                            float a = 1.f;
+                            if (big) {
+                                float qmax = -INFINITY;
 #pragma unroll
-                        for (int w = 0; w < 16; ++w) {
-                            float2 e = __ffma2_rn(make_float2(__uint_as_float(raw[2 * w]), __uint_as_float(raw[2 * w + 1])),
-                                                  sc2, nm2);
-                            if constexpr (decltype(masked)::value) {  // masked keys give p = 0 (also for a zero scale)
-                                const int k = 32 * qd + 2 * w;
-                                if (k > lim0) e.x = -INFINITY;
-                                if (k + 1 > lim0) e.y = -INFINITY;
+                                for (int k = 0; k < 32; ++k) {
+                                    const bool vis = !decltype(masked)::value || 32 * qd + k <= lim0;
+                                    if (vis) qmax = fmaxf(qmax, __uint_as_float(raw[k]));
+                                }
+                                const float mq = ceilf(qmax * sc);
+                                if (mq > m_used) {
+                                    // 2^(m_used - mq) built from its exponent bits (0 below 2^-126)
+                                    const float d = m_used - mq;
+                                    a = d < -126.f ? 0.f : __int_as_float(((int)d + 127) << 23);
+                                    m_used = mq;
+                                    qs = exps(masked, raw, qd, ph);
+                                }
                             }
-                            e.x = pa::fast_exp2(e.x);
-                            e.y = pa::fast_exp2(e.y);
-                            psum2 = __fadd2_rn(psum2, e);
-                            ph[w] = float2_to_f16x2(e.x, e.y);
+                            psum2.x *= a;
+                            psum2.y *= a;
+                            alpha *= a;
+                            if (qd > 0) {  // P of the earlier quarters, in place (warp-collective)
+                                tc::tmem_wait_st();
+                                // in fp32: the factor itself may lie below fp16's range
+                                // (2^-25 would round to 0 as a half) while the products
+                                // (P <= 2^15) do not
+#pragma unroll 1
+                                for (int q2 = 0; q2 < qd; ++q2) {
+                                    uint32_t pp[16];
+                                    tc::tmem_ld16(tS + 32 * q2, pp);
+                                    tc::tmem_wait_ld();
+#pragma unroll
+                                    for (int w = 0; w < 16; ++w) {
+                                        const float2 f = __half22float2(*reinterpret_cast<__half2*>(&pp[w]));
+                                        pp[w] = float2_to_f16x2(f.x * a, f.y * a);
+                                    }
+                                    tc::tmem_st16(tS + 32 * q2, pp);
+                                }
+                            }
                         }
+                        psum2.x += qs;
                         tc::tmem_st16(tS + 32 * qd, ph);
                     }
                 };
-                if (mask_warp) pass2(std::true_type{});
-                else pass2(std::false_type{});
-                const float psum = psum2.x + psum2.y;
-                l = l * alpha + psum;
-                // a larger maximum rescales O_x: PV_x(j-1) must have landed first
-                if (j > 0 && __any_sync(kFull, rescale)) {
+                if (mask_warp) sweep(std::true_type{});
+                else sweep(std::false_type{});
+                l = l * alpha + (psum2.x + psum2.y);
+                // a new reference rescales O_x: PV_x(j-1) must have landed first
+                if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
                     if (ok) ok = wait_bar(&pv_done[x], (uint32_t)((j - 1) & 1), P.err, abort_flag);
                     ok = __all_sync(kFull, ok);
                     tc::fence_after_sync();
@@ -576,7 +606,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) pa::mbar_arrive(&p_full[x]);
+                asm volatile("bar.arrive %0, 160;" ::"r"(1 + x) : "memory");  // P handed to the MMA warp
             }
             tc::tmem_wait_st();  // no store may be pending when the columns are released
             if (ok) ok = wait_bar(&pv_done[x], (uint32_t)((n_kt - 1) & 1), P.err, abort_flag);
@@ -858,10 +888,10 @@ int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtenso
     const int n_qp = (max_chunk_len + 2 * QT - 1) / (2 * QT);
     if (Pp.work) {  // balanced mode: plan, then one CTA per SM taking work-list entries
         pa_prefill_plan_kernel<G><<<1, 1024, 0, stream>>>(Pp);
-        kern<<<Pp.n_cta, 384, kSmemBytes, stream>>>(Pp, tk, tv);
+        kern<<<Pp.n_cta, kThreads, kSmemBytes, stream>>>(Pp, tk, tv);
     } else {
         dim3 grid(n_qp * Pp.splits, Pp.n_kv_heads, n_seqs);
-        kern<<<grid, 384, kSmemBytes, stream>>>(Pp, tk, tv);
+        kern<<<grid, kThreads, kSmemBytes, stream>>>(Pp, tk, tv);
     }
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (Pp.work)  // the cut pairs (fewer than one per CTA): 256 rows each

@@ -294,3 +294,46 @@ def test_prefill_v_beyond_fp16_staging_is_flagged(pk, splits):
     got = _run(pk, wl, splits)
     assert not np.isfinite((got.astype(np.uint32) << 16).view(np.float32)).all()
     check_device_error(64)                              # PA_DEVERR_RANGE
+
+
+def _bf16(x):
+    f = np.asarray(x, np.float32)
+    return ((f.view(np.uint32) + 0x7FFF + ((f.view(np.uint32) >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("splits", [None, 0])
+def test_prefill_row_maximum_jump_keeps_earlier_keys(pk, splits):
+    """One row whose scores jump twice inside one key tile: a key 15 binades
+    (log2 units after the scale) above the reference of the first tile, then
+    one 25.5 binades above it. The second jump rescales the tile's earlier P
+    by about 2^-25, a factor below fp16's range although the rescaled P
+    (about 2^-10) is not: the key 15 binades up keeps its weight of about
+    2^-10.5, which carries the whole output (its V is 8, every other V is 0)."""
+    torch = torch_cuda()
+    H = Hk = 4
+    D, ctx = 128, 300
+    wl = make_prefill_case(960, [ctx], [1], [], H, Hk, D)
+    sc = wl.scale / np.log(2.0)                      # scores -> log2 units
+    base = 20.0 / sc                                 # first tile's maximum at 20 binades
+    x = np.full(ctx, -200.0)                         # every other key: far below
+    x[5], x[130], x[230] = base, base + 15.0 / sc, base + 25.5 / sc
+    kpos = np.zeros((ctx, Hk, D), np.float32)
+    kpos[:, :, 0] = x[:, None]
+    vpos = np.zeros((ctx, Hk, D), np.float32)
+    vpos[130] = 8.0
+    K, V = _bf16(kpos), _bf16(vpos)
+    tab = wl.pf_tables[0]
+    for t in range(ctx - 1):                         # the cached tokens; the last one is this step's
+        wl.k_pool[tab[t // 16], :, t % 16] = K[t]
+        wl.v_pool[tab[t // 16], :, t % 16] = V[t]
+    wl.new_k = K[ctx - 1:ctx].copy()
+    wl.new_v = V[ctx - 1:ctx].copy()
+    q = np.zeros((1, H, D), np.float32)
+    q[:, :, 0] = 1.0
+    wl.q_pf = _bf16(q)
+    got = _run(pk, wl, splits)
+    ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+    ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
+    assert ref[0, 0, 0] > 3e-3                       # the moderate key's share is not negligible
+    assert_attention_close(got, ref, "row maximum jump")
+    check_device_error(0)

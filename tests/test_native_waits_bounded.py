@@ -89,3 +89,70 @@ def test_helpers_give_up():
     body = pf[pf.index("bool wait_bar("):]
     body = body[:body.index("\n}\n")]
     assert "PA_WAIT_LIMIT_NS" in body and "abort_flag" in body and "return false" in body
+
+
+def _loop_body(src, start):
+    """Body text of the loop whose header starts at offset `start`."""
+    i = src.index("{", start)
+    depth = 0
+    for k in range(i, len(src)):
+        if src[k] == "{":
+            depth += 1
+        elif src[k] == "}":
+            depth -= 1
+            if depth == 0:
+                return src[i + 1:k]
+    raise AssertionError("unbalanced braces")
+
+
+def _without_lambdas(body):
+    """The text with every lambda's body removed (a return there leaves the
+    lambda, not the loop)."""
+    out, i = [], 0
+    for m in re.finditer(r"\[[&=]?\]\s*\(", body):
+        if m.start() < i:
+            continue
+        k, depth = m.end() - 1, 0          # the parameter list, parentheses balanced
+        while True:
+            depth += {"(": 1, ")": -1}.get(body[k], 0)
+            k += 1
+            if depth == 0:
+                break
+        k = body.index("{", k)
+        out.append(body[i:k])
+        depth = 0                          # the body, braces balanced
+        while True:
+            depth += {"{": 1, "}": -1}.get(body[k], 0)
+            k += 1
+            if depth == 0:
+                break
+        i = k
+    out.append(body[i:])
+    return "".join(out)
+
+
+def test_named_barrier_arrivals_and_syncs_balance():
+    """The prefill hands each tile's P to the MMA warp through a hardware named
+    barrier, which has no time limit. It cannot be left waiting because each
+    side meets it exactly once per key tile: the arrive and the syncs sit in
+    loops `for (int j = 0; j < n_kt; ++j)` with no break, continue or return
+    (a failed mbarrier wait only stops the waiting, not the loop)."""
+    pf = _sources()["prefill.cu"]
+    uses = [m.start() for m in re.finditer(r"bar\.(sync|arrive) ", pf)]
+    assert uses, "no named barrier found"
+    loops = [m.start() for m in re.finditer(r"for \(int j = 0; j < n_kt; \+\+j\) \{", pf)]
+    covered = 0
+    for start in loops:
+        body = _loop_body(pf, start)
+        n_bar = len(re.findall(r"bar\.(?:sync|arrive) ", body))
+        if not n_bar:
+            continue
+        covered += n_bar
+        assert not re.search(r"\b(break|continue|return)\b", _without_lambdas(body)), \
+            "a loop with a named barrier can exit early"
+    assert covered == len(uses), "a named barrier outside the per-key-tile loops"
+    arrives = re.findall(r'bar\.arrive %0, (\d+);', pf)
+    syncs = re.findall(r'bar\.sync (\d), (\d+);', pf)
+    assert len(arrives) == 1 and sorted(i for i, _ in syncs) == ["1", "2"]
+    assert all(c == arrives[0] for _, c in syncs)        # the same thread count on both sides
+    assert int(arrives[0]) == 4 * 32 + 32                # four softmax warps arrive, one warp syncs

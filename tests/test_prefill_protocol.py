@@ -1,18 +1,24 @@
 """A discrete-event model of the prefill kernel's barrier protocol.
 
-The chunked-prefill kernel runs five roles that meet only on mbarriers: a TMA
-producer (K and V tiles into kKS and kVS shared-memory stages), two converter
-warps (each landed V tile rewritten in place), an MMA warp (QK and PV for two
-query tiles A and B, issued in order into one tensor-core pipe), and two
-softmax warpgroups of four warps. This model replays the same waits and
-arrivals with random delays and checks, for every schedule it draws:
+The chunked-prefill kernel runs five roles: a TMA producer (K and V tiles
+into kKS and kVS shared-memory stages), four converter warps (each landed V
+tile rewritten in place), one MMA-issuing thread (QK and PV for two query
+tiles A and B, issued in order into one tensor-core pipe), and two softmax
+warpgroups of four warps. They meet on mbarriers, except for the hand-over
+of a tile's P, where the four softmax warps arrive on a named barrier and
+the MMA warp syncs on it. This model replays the same waits and arrivals
+with random delays and checks, for every schedule it draws:
 
 - every parity wait targets phase c or c + 1 of its barrier, where c phases
   have completed, so the wait's parity names exactly one phase;
 - the run finishes (no deadlock);
 - each QK reads the K tile it names and each PV the V tile it names, and that
   tile has been converted; a converter finishes a tile before the next load
-  lands in its stage.
+  lands in its stage;
+- a softmax warpgroup that rescales O at step j finds P.V of step j-1 done
+  (it waits for no barrier of its own: S(j) is issued after that P.V);
+- no softmax warp arrives on a tile's named barrier for step j+1 before the
+  MMA warp has synced for step j (a hardware barrier has no phases).
 
 The stage counts are read from the kernel source, so the model follows them.
 A mutated protocol (PV_A waiting for the landed V tile instead of the
@@ -52,10 +58,12 @@ def run(n, KS, VS, seed, pv_waits_converter=True):
     k_free = [Bar(f"k_free{i}") for i in range(KS)]
     v_full = [Bar(f"v_full{i}") for i in range(VS)]
     v_free = [Bar(f"v_free{i}") for i in range(VS)]
-    v_conv = [Bar(f"v_conv{i}", 2) for i in range(VS)]
+    v_conv = [Bar(f"v_conv{i}", 4) for i in range(VS)]
     s_full = [Bar("s_full0"), Bar("s_full1")]
-    p_full = [Bar("p_full0", 4), Bar("p_full1", 4)]
+    p_named = [Bar("named0", 4), Bar("named1", 4)]  # four softmax warps arrive; the MMA warp syncs
+    synced = [0, 0]                                   # steps the MMA warp has synced per tile
     pv_done = [Bar("pv_done0"), Bar("pv_done1")]
+    done_ops = set()
     pipe, tma = [], []
     kslot, vslot, vconv_of = {}, {}, {}  # stage -> tile landed / tile converted there
 
@@ -76,7 +84,7 @@ def run(n, KS, VS, seed, pv_waits_converter=True):
         while nv < min(VS, n):
             tma.append(("v", nv, rng.randint(1, 40))); nv += 1
         while nk < n or nv < n:
-            if nk < n and nk <= nv + 1:
+            if nk < n and nk <= nv:
                 yield wait(k_free[nk % KS], (nk - KS) // KS)
                 tma.append(("k", nk, rng.randint(1, 40))); nk += 1
             else:
@@ -99,30 +107,34 @@ def run(n, KS, VS, seed, pv_waits_converter=True):
         pipe.append(([s_full[0]], ("qk", 0, 0)))
         pipe.append(([s_full[1], k_free[0]], ("qk", 1, 0)))
         for j in range(n):
-            yield wait(p_full[0], j)
             if pv_waits_converter:
                 yield wait(v_conv[j % VS], j // VS)
             else:
                 yield wait(v_full[j % VS], j // VS)
-            pipe.append(([pv_done[0]], ("pv", 0, j)))
             if j + 1 < n:
                 yield wait(k_full[(j + 1) % KS], (j + 1) // KS)
-                pipe.append(([s_full[0]], ("qk", 0, j + 1)))
-            yield wait(p_full[1], j)
-            pipe.append(([pv_done[1], v_free[j % VS]], ("pv", 1, j)))
+            yield wait(p_named[0], j)
+            synced[0] = j + 1
+            pipe.append(([pv_done[0]], ("pv", 0, j)))
             if j + 1 < n:
-                pipe.append(([s_full[1], k_free[(j + 1) % KS]], ("qk", 1, j + 1)))
+                pipe.append(([s_full[0]], ("qk", 0, j + 1)))
+            yield wait(p_named[1], j)
+            synced[1] = j + 1
+            pipe.append(([v_free[j % VS], pv_done[1]], ("pv", 1, j)))
+            if j + 1 < n:
+                pipe.append(([k_free[(j + 1) % KS], s_full[1]], ("qk", 1, j + 1)))
 
     def softmax(x):
         for j in range(n):
             yield wait(s_full[x], j)
+            if j > 0:  # an O rescale here would need P.V of step j-1 done
+                assert ("pv", x, j - 1) in done_ops, f"softmax {x} step {j}: PV({j - 1}) not done"
             yield from idle(rng.randint(0, 5))
-            if j > 0 and rng.random() < 0.3:  # a row maximum grew: O is rescaled after PV_x(j-1)
-                yield wait(pv_done[x], j - 1)
-            p_full[x].arrive()
+            assert synced[x] >= j, f"tile {x}: arrival for step {j} before the sync of step {j - 1}"
+            p_named[x].arrive()
         yield wait(pv_done[x], n - 1)
 
-    actors = [producer(), mma(), converter(0), converter(1)] + [softmax(x) for x in (0, 1) for _ in range(4)]
+    actors = [producer(), mma()] + [converter(w) for w in range(4)] + [softmax(x) for x in (0, 1) for _ in range(4)]
     conds = [None] * len(actors)
     done = [False] * len(actors)
     busy = 0
@@ -152,6 +164,7 @@ def run(n, KS, VS, seed, pv_waits_converter=True):
                 else:
                     assert vslot.get(j % VS) == j, f"PV{x}({j}) read the wrong V tile"
                     assert vconv_of.get(j % VS) == j, f"PV{x}({j}) read V before it was converted"
+                done_ops.add((op, x, j))
                 for b in bars:
                     b.arrive()
         order = list(range(len(actors)))
