@@ -95,12 +95,26 @@ enum pa_device_error {
  * holds fp32 split-K partials: running max m and sum l per (seq, q-head,
  * partition) and the unnormalised output per (seq, q-head, partition, dim).
  * partition_tokens: tokens per context partition, a multiple of 64 in
- * [64, 2048]; 0 selects the library default: 512 tokens, which also sizes
- * the workspace for the tensor-core kernel's default of 1024 (fewer, larger
- * partitions fit in the same bytes).
+ * [64, 2048]; 0 selects the library default (pa_decode_partition_tokens),
+ * and sizes the workspace for 512 tokens, which covers every default (fewer,
+ * larger partitions fit in the same bytes).
  */
 size_t pa_decode_workspace_bytes(int n_seqs, int n_heads, int head_dim,
                                  int max_context_len, int partition_tokens);
+
+/*
+ * The partition size (tokens per context partition) pa_decode, pa_decode_fp8
+ * (elem_bytes 1) and pa_decode_window (window >= 0; -1 for none) use when
+ * partition_tokens is 0, for this batch shape on the current device: 1024 on
+ * the tensor-core kernel; on the CUDA-core kernel the multiple of 64 in
+ * [512, 1024] whose grid of n_seqs x n_kv_heads x ceil(context / size) CTAs
+ * (context = max_context_len, or the window's span) fills the last wave of
+ * the device's CTA slots best, the smallest on ties. Every such size needs
+ * no more workspace than pa_decode_workspace_bytes(..., 0) gives. Negative
+ * status for arguments the decode entry points would reject.
+ */
+int pa_decode_partition_tokens(int n_seqs, int n_heads, int n_kv_heads, int head_dim,
+                               int max_context_len, int window, int elem_bytes);
 
 /*
  * PagedAttention decode ([LD] kernel outline; [KE] attention formula):

@@ -20,7 +20,7 @@ from . import _capi
 from ._capi import PagedKVError, check, load  # noqa: F401
 
 __all__ = [
-    "pa_decode", "pa_decode_tc", "pa_decode_workspace_bytes", "decode_workspace", "pa_decode_noalloc", "pa_reshape_and_cache",
+    "pa_decode", "pa_decode_tc", "pa_decode_workspace_bytes", "pa_decode_partition_tokens", "decode_workspace", "pa_decode_noalloc", "pa_reshape_and_cache",
     "pa_copy_blocks", "pa_prefill_paged", "pa_prefill_paged_ex", "pa_prefill_workspace_bytes",
     "prefill_workspace", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_window",
     "pa_swap_out_blocks", "pa_swap_in_blocks", "pa_get_device_error",
@@ -64,6 +64,15 @@ def pa_decode_workspace_bytes(n_seqs: int, n_heads: int, head_dim: int, max_cont
                               partition_tokens: int = 0) -> int:
     return int(load().pa_decode_workspace_bytes(n_seqs, n_heads, head_dim, max_context_len,
                                                 partition_tokens))
+
+
+def pa_decode_partition_tokens(n_seqs: int, n_heads: int, n_kv_heads: int, head_dim: int,
+                               max_context_len: int, window: int = -1, elem_bytes: int = 2) -> int:
+    """The partition size the decode entry points use with partition_tokens=0."""
+    st = int(load().pa_decode_partition_tokens(n_seqs, n_heads, n_kv_heads, head_dim, max_context_len,
+                                               window, elem_bytes))
+    check("pa_decode_partition_tokens", min(st, 0))
+    return st
 
 
 def decode_workspace(q, max_context_len: int, partition_tokens: int = 0):

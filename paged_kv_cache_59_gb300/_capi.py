@@ -38,6 +38,7 @@ p_i64 = C.POINTER(C.c_int64)
 # name -> (restype, argtypes); every symbol declared in include/pagedkv.h
 SIGNATURES = {
     "pa_decode_workspace_bytes": (C.c_size_t, [i32, i32, i32, i32, i32]),
+    "pa_decode_partition_tokens": (i32, [i32, i32, i32, i32, i32, i32, i32]),
     "pa_decode": (i32, [vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32, i32,
                         vp, C.c_size_t, vp]),
     "pa_decode_ex": (i32, [vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32, i32,

@@ -1073,6 +1073,57 @@ int launch_partition_mma(const DecodeParams& P, int n_seqs, cudaStream_t stream)
 
 constexpr int kDefaultPartitionTokens = 512;
 
+// CTAs of the CUDA-core partition kernel resident per SM (its launch bounds).
+int k1_ctas_per_sm(int head_dim, int G, int eb) {
+    if (head_dim == 128) {
+        if (eb == 1 && G == 4) return Launch<128, 4, 1>::MINB;
+        return G == 8 ? Launch<128, 8, 2>::MINB : Launch<128, 4, 2>::MINB;
+    }
+    return G == 8 ? Launch<64, 8, 2>::MINB : Launch<64, 4, 2>::MINB;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;  // every thread that races here writes the same value
+    }
+    return cached[dev];
+}
+
+// Default partition size of the CUDA-core kernel. One CTA streams one
+// partition of one (sequence, KV head); when the grid is a few waves of CTA
+// slots deep, a last wave that fills only part of the slots leaves SMs idle.
+// Among the multiples of 64 tokens in [512, 1024] (each needs no more
+// workspace than 512), take the one whose grid - n_seqs x n_kv_heads x
+// ceil(context / size) CTAs, exact when every context is `context` - fills
+// its last wave best (waves / ceil(waves)), the smallest on ties.
+int wave_partition_tokens(int n_seqs, int n_kv_heads, int context, int slots) {
+    if (slots <= 0 || context <= kDefaultPartitionTokens) return kDefaultPartitionTokens;
+    int best = kDefaultPartitionTokens;
+    double best_fill = -1.0;
+    for (int pt = kDefaultPartitionTokens; pt <= 2 * kDefaultPartitionTokens; pt += 64) {
+        const double ctas = (double)n_seqs * n_kv_heads * ((context + pt - 1) / pt);
+        const double waves = ctas / slots;
+        const double fill = waves / ceil(waves);
+        if (fill > best_fill + 1e-9) {
+            best_fill = fill;
+            best = pt;
+        }
+    }
+    return best;
+}
+
+int default_partition_tokens(bool tensor, int eb, int n_seqs, int n_kv_heads, int G, int head_dim,
+                             int max_context_len, int window) {
+    if (tensor) return 2 * kDefaultPartitionTokens;
+    const int span = window >= 0 && window + 2 * kBS < max_context_len ? window + 2 * kBS : max_context_len;
+    return wave_partition_tokens(n_seqs, n_kv_heads, span, sm_count() * k1_ctas_per_sm(head_dim, G, eb));
+}
+
 int resolve_partition_tokens(int pt) {
     if (pt == 0) return kDefaultPartitionTokens;
     if (pt < 64 || pt > 2048 || pt % 64 != 0) return -1;
@@ -1094,6 +1145,18 @@ extern "C" size_t pa_decode_workspace_bytes(int n_seqs, int n_heads, int head_di
     if (pt < 0 || n_seqs <= 0 || n_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return 0;
     const int max_parts = (max_context_len + pt - 1) / pt;
     return workspace_bytes_for(n_seqs, n_heads, head_dim, max_parts);
+}
+
+extern "C" int pa_decode_partition_tokens(int n_seqs, int n_heads, int n_kv_heads, int head_dim,
+                                          int max_context_len, int window, int elem_bytes) {
+    if (n_seqs < 0 || n_heads <= 0 || n_kv_heads <= 0 || max_context_len < 0 || n_heads % n_kv_heads != 0 ||
+        (elem_bytes != 1 && elem_bytes != 2))
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    const int G = n_heads / n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
+    const bool tensor = head_dim == 128 && (G == 8 || elem_bytes == 1);
+    return default_partition_tokens(tensor, elem_bytes, n_seqs, n_kv_heads, G, head_dim, max_context_len, window);
 }
 
 namespace {
@@ -1122,11 +1185,14 @@ int decode_impl(int eb, void* out, const void* q, const void* k_pool, const void
     // HBM), unless the pool has too many rows for a TMA coordinate;
     // pa_decode_tc asks for the tensor-core kernel at every group size
     const bool tensor = force_tc || (head_dim == 128 && tc_rows_ok && (G == 8 || eb == 1));
-    // default partitions: 512 tokens on the CUDA-core kernel, 1024 on the
-    // tensor-core kernel, whose shorter blocks amortise a CTA's fixed cost
-    // over more of them (measured 3-5% faster); the workspace for 512 covers it
-    const int pt = partition_tokens == 0 && tensor ? 2 * kDefaultPartitionTokens
-                                                  : resolve_partition_tokens(partition_tokens);
+    // default partitions: on the CUDA-core kernel the size in [512, 1024]
+    // whose grid fills its last wave of CTA slots best (wave_partition_tokens);
+    // 1024 tokens on the tensor-core kernel, whose shorter blocks amortise a
+    // CTA's fixed cost over more of them (measured 3-5% faster). The workspace
+    // for 512 covers every one of them.
+    const int pt = partition_tokens == 0
+                       ? default_partition_tokens(tensor, eb, n_seqs, n_kv_heads, G, head_dim, max_context_len, window)
+                       : resolve_partition_tokens(partition_tokens);
     if (pt < 0) return PA_ERR_INVALID_ARG;
     if (pt / kBS > 32 * kNW) return PA_ERR_INVALID_ARG;  // one table entry per lane
     if (n_seqs == 0) return PA_OK;

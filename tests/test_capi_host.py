@@ -389,3 +389,20 @@ def test_default_workspace_covers_every_decode_path(capi, H, Hk, D, max_ctx):
     tensor_default = D == 128 and H // Hk == 8
     if not tensor_default:  # pa_decode_ex runs the CUDA-core kernel: 512-token partitions, all bytes used
         assert capi.pa_decode_ex(p, q, p, p, p, p, *common(wsb - 16)) == -3
+
+
+def test_default_partition_tokens_without_a_device(capi):
+    """Without a visible device the wave rule has no slot count: 512 tokens on
+    the CUDA-core kernel, 1024 on the tensor-core kernel (groups of 8 at
+    head_dim 128, and E4M3 caches at head_dim 128); bad shapes are refused."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is visible: the rule depends on its SM count")
+    assert capi.pa_decode_partition_tokens(64, 32, 8, 128, 4096, -1, 2) == 512
+    assert capi.pa_decode_partition_tokens(8, 32, 32, 128, 2048, -1, 2) == 512
+    assert capi.pa_decode_partition_tokens(100, 64, 8, 128, 4096, -1, 2) == 1024
+    assert capi.pa_decode_partition_tokens(64, 32, 8, 128, 4096, -1, 1) == 1024
+    assert capi.pa_decode_partition_tokens(64, 32, 8, 64, 4096, -1, 1) == 512
+    assert capi.pa_decode_partition_tokens(4, 6, 4, 128, 100, -1, 2) == -1
+    assert capi.pa_decode_partition_tokens(4, 4, 4, 96, 100, -1, 2) == -2
+    assert capi.pa_decode_partition_tokens(4, 4, 4, 128, 100, -1, 3) == -1
