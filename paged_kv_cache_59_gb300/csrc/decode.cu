@@ -501,7 +501,11 @@ pa_decode_partition_kernel(const DecodeParams P) {
 // G query heads in the first G of 16 rows) + 16 (PV, two P terms x 8 m-tiles
 // of 16 dims) of them instead of ~1,000 FMA and shuffle instructions. tcgen05 needs M >= 64, which would
 // waste 7/8 of every instruction on padding rows for this shape.
-//   S[16 x 16 tokens] = Q[16 x 128] . K^T   (A = q in registers, B = K via ldmatrix)
+//   S[16 x 16 tokens] = Q[16 x 128] . K^T   (A = q in registers, B = K via ldmatrix;
+//                                            with an E4M3 cache S^T = K . Q^T instead:
+//                                            the 16 tokens as M, the heads as N, one
+//                                            MMA per k-step, and P^T for the P.V
+//                                            product from two movmatrix transposes)
 //   O^T[128 x 8]     += V^T . P^T           (A = V^T via ldmatrix.trans; B = P^T,
 //                                            which is S's accumulator layout as it
 //                                            stands; the 8 head rows fill N = 8)
@@ -570,6 +574,13 @@ __device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
         : "=f"(a), "=f"(b)
         : "r"(h));
     return make_float2(a, b);
+}
+// transposes an 8 x 8 matrix of 16-bit elements held in the m8n8 fragment
+// layout (lane l: row l / 4, columns 2 (l % 4), +1)
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
 }
 __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t c) {
     uint32_t r;
@@ -709,6 +720,10 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
 #pragma unroll
         for (int k = 0; k < 4; ++k) o[n][k] = 0.f;
     float m_used = -INFINITY, l_run = 0.f;  // row g, base-2 units; l over this lane's columns
+    // E4M3 cache: scores are computed transposed (S^T, tokens x heads), so a
+    // lane holds heads 2t and 2t + 1: their reference maxima and its part of
+    // their sums (the same reference on the 8 lanes of a head)
+    float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.f, 0.f};
     // E4M3 cache: q.(code*s_k) = s_k (q.code), folded into the score scale
     const float sc = EB == 1 ? P.scale_log2 * P.k_scale[kvh] : P.scale_log2;
 
@@ -764,69 +779,127 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
                     mma_t<EB>(s_acc[0], qa[ks][0], qa[ks][1], b00, b01);
                     mma_t<EB>(s_acc[1], qa[ks][0], qa[ks][1], b10, b11);
                 }
-            } else {  // K codes of token row 8nt + g, dims 16ks + 4t .. +3, widened in registers
+            }
+            // E4M3: S^T = K Q^T with the tile's 16 tokens as M and the group's heads as
+            // N: one MMA per k-step of 16 dims; the lane's k = 2t, 2t+1 | 2t+8, 2t+9 are
+            // dims 16ks + 4t, +1 | +2, +3 (four consecutive codes of each of its token
+            // rows g and g + 8, widened in registers); two accumulators (even and odd
+            // k-steps) halve the dependent chain
+            float sT[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (EB == 1) {
                 const unsigned char* rk = my_stages + (size_t)st * kStage;
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int row = 8 * nt + g;
-                        const uint32_t w =
-                            *reinterpret_cast<const uint32_t*>(rk + row * 128 + ((ks ^ (row & 7)) << 4) + 4 * t);
-                        mma_t<EB>(s_acc[nt], qa[ks][0], qa[ks][1], e4m3x2_to_h2((uint16_t)(w & 0xffffu)),
-                                  e4m3x2_to_h2((uint16_t)(w >> 16)));
-                    }
-            }
-            // ---- online softmax of row g over the tile's 16 tokens (this lane: 2t, 2t+1, 8+2t, 9+2t)
-            float sv[4];
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int pos = tok0 + 8 * n + 2 * t + k;
-                    sv[2 * n + k] = (pos < ctx && pos >= first_pos) ? s_acc[n][k] * sc : -INFINITY;
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int off = ((ks ^ (g & 7)) << 4) + 4 * t;  // rows g and g + 8 share the swizzle
+                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(rk + g * 128 + off);
+                    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(rk + (g + 8) * 128 + off);
+                    mma16816_f16(ks & 1 ? sb : sa, e4m3x2_to_h2((uint16_t)(w0 & 0xffffu)),
+                                 e4m3x2_to_h2((uint16_t)(w1 & 0xffffu)), e4m3x2_to_h2((uint16_t)(w0 >> 16)),
+                                 e4m3x2_to_h2((uint16_t)(w1 >> 16)), qa[ks][0], qa[ks][1]);
                 }
-            float tmax = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-            tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
-            tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
-            float alpha = 1.f;
-            if (tmax > m_used + 8.f) {  // lazy rescale: p <= 2^8 un-normalised
-                alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
-                l_run *= alpha;
-                m_used = tmax;
-            }
-            if (__any_sync(kFull, alpha != 1.f)) {  // O^T columns are heads: head h's factor from lane 4h
-                const float a0 = __shfl_sync(kFull, alpha, 8 * t), a1 = __shfl_sync(kFull, alpha, 8 * t + 4);
 #pragma unroll
-                for (int n = 0; n < 8; ++n) {
-                    o[n][0] *= a0;
-                    o[n][1] *= a1;
-                    o[n][2] *= a0;
-                    o[n][3] *= a1;
-                }
+                for (int k = 0; k < 4; ++k) sT[k] = sa[k] + sb[k];
             }
-            const float mref = m_used == -INFINITY ? 0.f : m_used;  // a row with no visible key yet
-            float pv[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                pv[k] = pa::fast_exp2(sv[k] - mref);
-                l_run += pv[k];
-            }
-            // P as the B operand (tokens of head g). bf16: P_hi truncated and P_lo the
-            // rounded rest, two MMAs (a single bf16 term, within 2^-9 of p, can miss an
-            // absolute 2e-3 on short rows). fp16: one term rounded to nearest, within
-            // 2^-12 of p, one MMA.
             uint32_t ph[2], pl[2];
+            if constexpr (EB == 1) {
+                // ---- online softmax per head over the tile's 16 tokens: this lane holds
+                // tokens g, g + 8 (sT[0..1], sT[2..3]) of heads 2t, 2t + 1 (even, odd k).
+                // p = 2^(s*scale - m) against the head's reference m, set to the maximum
+                // so far on the head's first visible keys and whenever a p could leave
+                // fp16's range (the key at the maximum gets p = 1 exactly)
+                float sv[4], pv[4];
 #pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                if constexpr (EB == 2) {
+                for (int u = 0; u < 4; ++u) {
+                    const int pos = tok0 + g + 8 * (u >> 1);
+                    sv[u] = (pos < ctx && pos >= first_pos) ? sT[u] * sc : -INFINITY;
+                }
+                auto exps = [&]() {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) pv[u] = pa::fast_exp2(sv[u] - (m2[u & 1] == -INFINITY ? 0.f : m2[u & 1]));
+                };
+                exps();
+                int need[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    need[k] = !(pv[k] <= 32768.f && pv[2 + k] <= 32768.f) ||
+                              (m2[k] == -INFINITY && (sv[k] != -INFINITY || sv[2 + k] != -INFINITY));
+                if (__any_sync(kFull, need[0] | need[1])) {
+                    // rare: a new reference for the heads that need one (uniform over a head's lanes)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        float hm = fmaxf(sv[k], sv[2 + k]);
+                        int nd = need[k];
+#pragma unroll
+                        for (int o2 = 4; o2 <= 16; o2 <<= 1) {
+                            hm = fmaxf(hm, __shfl_xor_sync(kFull, hm, o2));
+                            nd |= __shfl_xor_sync(kFull, nd, o2);
+                        }
+                        if (nd && hm > m2[k]) {
+                            const float a = pa::fast_exp2(m2[k] - hm);  // 0 on the head's first keys
+                            m2[k] = hm;
+                            l2[k] *= a;
+#pragma unroll
+                            for (int n = 0; n < 8; ++n) {
+                                o[n][k] *= a;
+                                o[n][2 + k] *= a;
+                            }
+                        }
+                    }
+                    exps();
+                }
+                l2[0] += pv[0] + pv[2];
+                l2[1] += pv[1] + pv[3];
+                // P^T as the B operand (tokens 2t, 2t+1 | 2t+8, 2t+9 of head g): the
+                // fp16 pairs (token g; heads 2t, 2t+1) of each 8 x 8 half, transposed
+                ph[0] = movmatrix_t(f2_to_h2(pv[0], pv[1]));
+                ph[1] = movmatrix_t(f2_to_h2(pv[2], pv[3]));
+                pl[0] = pl[1] = 0u;
+            } else {
+                // ---- online softmax of row g over the tile's 16 tokens (this lane: 2t, 2t+1, 8+2t, 9+2t)
+                float sv[4];
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int pos = tok0 + 8 * n + 2 * t + k;
+                        sv[2 * n + k] = (pos < ctx && pos >= first_pos) ? s_acc[n][k] * sc : -INFINITY;
+                    }
+                float tmax = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+                tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
+                tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
+                float alpha = 1.f;
+                if (tmax > m_used + 8.f) {  // lazy rescale: p <= 2^8 un-normalised
+                    alpha = pa::fast_exp2(m_used - tmax);  // 0 on the first tile
+                    l_run *= alpha;
+                    m_used = tmax;
+                }
+                if (__any_sync(kFull, alpha != 1.f)) {  // O^T columns are heads: head h's factor from lane 4h
+                    const float a0 = __shfl_sync(kFull, alpha, 8 * t), a1 = __shfl_sync(kFull, alpha, 8 * t + 4);
+#pragma unroll
+                    for (int n = 0; n < 8; ++n) {
+                        o[n][0] *= a0;
+                        o[n][1] *= a1;
+                        o[n][2] *= a0;
+                        o[n][3] *= a1;
+                    }
+                }
+                const float mref = m_used == -INFINITY ? 0.f : m_used;  // a row with no visible key yet
+                float pv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    pv[k] = pa::fast_exp2(sv[k] - mref);
+                    l_run += pv[k];
+                }
+                // P as the B operand (tokens of head g), as two bf16 terms: P_hi truncated
+                // and P_lo the rounded rest, two MMAs (a single bf16 term, within 2^-9 of p,
+                // can miss an absolute 2e-3 on short rows)
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
                     const uint32_t bx = __float_as_uint(pv[2 * n]), by = __float_as_uint(pv[2 * n + 1]);
                     ph[n] = __byte_perm(bx, by, 0x7632);
                     pl[n] = pa::float2_to_bf16x2(pv[2 * n] - __uint_as_float(bx & 0xffff0000u),
                                                  pv[2 * n + 1] - __uint_as_float(by & 0xffff0000u));
-                } else {
-                    ph[n] = f2_to_h2(pv[2 * n], pv[2 * n + 1]);
-                    pl[n] = 0u;
                 }
             }
             if constexpr (EB == 1) __syncwarp();  // the widened V tile is complete
@@ -864,6 +937,10 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
     }
     l_run += __shfl_xor_sync(kFull, l_run, 1);
     l_run += __shfl_xor_sync(kFull, l_run, 2);
+#pragma unroll
+    for (int k = 0; k < 2; ++k)  // E4M3: a head's sum over its 8 lanes
+#pragma unroll
+        for (int o2 = 4; o2 <= 16; o2 <<= 1) l2[k] += __shfl_xor_sync(kFull, l2[k], o2);
 
     __syncthreads();  // every warp is done with its ring: reuse it for the merge
     float* mo = reinterpret_cast<float*>(stages);  // [NW][G][D]
@@ -881,7 +958,16 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
             }
         }
     }
-    if (g < G && t == 0) {
+    if constexpr (EB == 1) {
+        if (g == 0) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                if (2 * t + k < G) {
+                    mm[warp * G + 2 * t + k] = m2[k];
+                    ml[warp * G + 2 * t + k] = l2[k];
+                }
+        }
+    } else if (g < G && t == 0) {
         mm[warp * G + g] = m_used;
         ml[warp * G + g] = l_run;
     }
