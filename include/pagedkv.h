@@ -363,7 +363,9 @@ int pa_decode_fp8(void* out, const void* q, const void* k_pool, const void* v_po
  *  q_start_loc   int32 [n_seqs+1], non-decreasing, q_start_loc[0] = 0
  *  context_lens  int32 [n_seqs], >= L_s
  *  max_chunk_len upper bound of L_s
- * head_dim must be 128 and the group n_heads/n_kv_heads 1, 2, 4 or 8.
+ * head_dim 64 or 128 and the group n_heads/n_kv_heads 1, 2, 4 or 8, else
+ * PA_ERR_UNSUPPORTED. The workspace size of pa_prefill_paged_ex does not
+ * depend on head_dim (a partial row holds up to 128 dims).
  * QK^T and PV run on the tcgen05 tensor cores with fp32 accumulation in
  * tensor memory; softmax in fp32. QK^T takes bf16 q and K. PV takes P rounded
  * to fp16 (within 2^-12 of p) and V staged in fp16 as v * 2^-8, which holds

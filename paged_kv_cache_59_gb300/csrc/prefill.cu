@@ -9,7 +9,9 @@
 // positions; chunk row i sits at position p = ctx - L + i and
 //     out[i][h] = sum_{t <= p} softmax_t(scale * q[i][h] . K[t]) V[t].
 //
-// Design (GB300). A query tile is 128 matrix rows = QT = 128/G chunk tokens x
+// Design (GB300), for head_dim D = 64 or 128 (one instantiation each; the
+// K/V block rows are D bf16 values, moved as D/64 boxes of 64 dims). A query
+// tile is 128 matrix rows = QT = 128/G chunk tokens x
 // the G query heads of one KV head's group, so every K/V byte staged in
 // shared memory feeds all G heads. One CTA owns two query tiles (A and B) of
 // the same (sequence, KV head): both use every K/V tile it loads, and the
@@ -26,7 +28,7 @@
 //     whatever the pool has there, become zeros);
 //   - one thread of an MMA warp issues, per query tile X, S_X = Q_X K_j^T
 //     (tcgen05.mma kind::f16, bf16 in, fp32 accumulator in tensor memory,
-//     M = N = 128) and, once X's softmax has written P, O_X += P V_j (fp16
+//     M = N = 128, K = D) and, once X's softmax has written P, O_X += P V_j (fp16
 //     in: P read from tensor memory, V as an MN-major shared-memory operand)
 //     with S_X(j+1) right behind it. The MMAs of one thread execute in issue
 //     order, so S_X(j+1) may follow the PV MMA that still reads P(j) out of
@@ -63,7 +65,6 @@
 
 namespace {
 
-constexpr int kD = 128;          // head_dim (the only one built)
 constexpr int kBS = 16;          // tokens per block
 constexpr int kKT = 128;         // keys per key tile
 constexpr int kBPT = kKT / kBS;  // blocks per key tile
@@ -73,16 +74,26 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kKS = 2;  // K tile stages
 constexpr int kVS = 3;  // V tile stages
 constexpr int kThreads = 448;  // 8 softmax warps, MMA warp (8), producer (9), 4 converter warps (10..13)
-// shared memory map; the dynamic shared memory base must be 1024-byte
-// aligned (swizzle atoms of TMA and of the matrix descriptors): checked
-constexpr uint32_t kQ = 0;                      // Q_A, Q_B: 2 x 32 KiB
-constexpr uint32_t kK0 = 2 * 32768;             // K stages
-constexpr uint32_t kV0 = kK0 + kKS * 32768;     // V stages
-constexpr uint32_t kBars = kV0 + kVS * 32768;   // mbarriers
-constexpr uint32_t kMisc = kBars + 256;            // tmem slot, abort flag
-constexpr uint32_t kSmemBytes = kMisc + 64;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-constexpr uint32_t kTmemCols = 512;  // tile X: S at 256X, O at 256X + 128
+// Shared memory map for head_dim D (64 or 128): a Q tile (128 rows) and a
+// K or V tile (128 keys) are 128 x D bf16 values each, stored as D / 64
+// 128B-swizzled halves of 64 dims (16 KiB each). The dynamic shared memory
+// base must be 1024-byte aligned (swizzle atoms of TMA and of the matrix
+// descriptors): checked.
+template <int D>
+struct PfLay {
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static constexpr int kHalves = D / 64;               // 64-dim halves of a row
+    static constexpr uint32_t kTile = kKT * D * 2;       // K or V tile bytes
+    static constexpr uint32_t kQTile = kRows * D * 2;    // Q tile bytes
+    static constexpr uint32_t kQ = 0;                    // Q_A, Q_B
+    static constexpr uint32_t kK0 = 2 * kQTile;          // K stages
+    static constexpr uint32_t kV0 = kK0 + kKS * kTile;   // V stages
+    static constexpr uint32_t kBars = kV0 + kVS * kTile; // mbarriers
+    static constexpr uint32_t kMisc = kBars + 256;       // tmem slot, abort flag, segment entries
+    static constexpr uint32_t kSmem = kMisc + 64;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+constexpr uint32_t kTmemCols = 512;  // tile X: S at 256X, O at 256X + 128 (D columns)
 
 struct PrefillParams {
     uint16_t* out;
@@ -112,9 +123,11 @@ struct PrefillParams {
     unsigned int* err;
 };
 
-// A piece's partial for one row: the un-normalised O (128 floats), the
-// reference maximum m (base-2 units) and the sum l of 2^(s*scale - m).
+// A piece's partial for one row: the un-normalised O (head_dim floats from
+// offset 0), and at offset 128 the reference maximum m (base-2 units) and the
+// sum l of 2^(s*scale - m); the same row size for both head dims.
 constexpr int kPartStride = 132;  // floats, 16-byte aligned rows
+constexpr int kPartML = 128;      // offset of (m, l) in a partial row
 
 // Key tiles [kt0, kt1) of piece sp out of `splits` over a pair's n_kt tiles.
 __host__ __device__ inline void piece_range(int n_kt, int sp, int splits, int& kt0, int& kt1) {
@@ -159,10 +172,14 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigne
     }
 }
 
-template <int G>
+template <int G, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
+    using L_ = PfLay<D>;
+    constexpr uint32_t kQ = L_::kQ, kK0 = L_::kK0, kV0 = L_::kV0, kBars = L_::kBars, kMisc = L_::kMisc;
+    constexpr uint32_t kTile = L_::kTile, kQTile = L_::kQTile;
+    constexpr int kNH = L_::kHalves;
     constexpr int QT = kRows / G;  // chunk tokens per query tile
     extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
@@ -274,11 +291,11 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         if (warp < 8) {
             const int x = warp >> 2, r = threadIdx.x & 127;
             const int i = i0 + x * QT + r / G;
-            const uint4* src = reinterpret_cast<const uint4*>(P.q + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
+            const uint4* src = reinterpret_cast<const uint4*>(P.q + ((size_t)(q0 + i) * H + h0 + r % G) * D);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < D / 8; ++c) {
                 const uint4 v = i < L ? src[c] : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sm + kQ + x * 32768 + (c >> 3) * 16384 + tc::sw128_offset(r, c & 7)) = v;
+                *reinterpret_cast<uint4*>(sm + kQ + x * kQTile + (c >> 3) * 16384 + tc::sw128_offset(r, c & 7)) = v;
             }
         }
         tc::fence_async_smem();
@@ -289,7 +306,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
         have_tmem = true;
 
         constexpr uint32_t ID_QK = tc::idesc_bf16_f32(128, 128, 0, 0);
-        constexpr uint32_t ID_PV = idesc_f16_f32(128, 128, 0, 1);
+        constexpr uint32_t ID_PV = idesc_f16_f32(128, D, 0, 1);
 
         if (warp == 9) {
             // ------------------------------------------------------- TMA producer
@@ -305,26 +322,26 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                     const int blk = w.group * 32 + lane;
                     w.ids = blk < nblk ? trow[blk] : -1;
                 }
-                // lane l < 16 moves box (block b = l / 2, dims 64 g .. 64 g + 63, g = l % 2)
-                const int b = (lane >> 1) & (kBPT - 1), g = lane & 1;
+                // lane l < 8 * kNH moves box (block b = l / kNH, dims 64 g .. 64 g + 63, g = l % kNH)
+                const int b = (lane / kNH) & (kBPT - 1), g = lane % kNH;
                 const int bid = __shfl_sync(kFull, w.ids, (j & 3) * kBPT + b);
                 const int blk = j * kBPT + b;
                 bool ok = blk < nblk;
                 if (ok && (bid < 0 || bid >= P.num_blocks)) {
-                    if (lane < 2 * kBPT && g == 0) pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
+                    if (lane < kNH * kBPT && g == 0) pa::set_error(P.err, PA_DEVERR_BLOCK_ID);
                     ok = false;
                 }
                 const int y = ok ? (bid * Hk + kvh) * kBS : P.oob_row;  // out of range: zero fill
-                if (lane == 0) pa::mbar_arrive_expect_tx(bar, 32768);
+                if (lane == 0) pa::mbar_arrive_expect_tx(bar, kTile);
                 __syncwarp();
-                if (lane < 2 * kBPT) tc::tma_load_2d(dst + g * 16384 + b * 2048, map, g * 64, y, bar);
+                if (lane < kNH * kBPT) tc::tma_load_2d(dst + g * 16384 + b * 2048, map, g * 64, y, bar);
                 __syncwarp();
             };
             auto issue_k = [&](int j) {
-                issue_tile(idk, &tmK, sm + kK0 + (j % kKS) * 32768, &k_full[j % kKS], kt0 + j);
+                issue_tile(idk, &tmK, sm + kK0 + (j % kKS) * kTile, &k_full[j % kKS], kt0 + j);
             };
             auto issue_v = [&](int j) {
-                issue_tile(idv, &tmV, sm + kV0 + (j % kVS) * 32768, &v_full[j % kVS], kt0 + j);
+                issue_tile(idv, &tmV, sm + kV0 + (j % kVS) * kTile, &v_full[j % kVS], kt0 + j);
             };
             int nk = 0, nv = 0;  // loads issued
             bool ok = true;
@@ -367,10 +384,10 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 return ((uint64_t)(uint32_t)(d >> 32) << 32) | (uint32_t)((uint32_t)d + off16);
             };
             auto issue_qk = [&](int x, int kst) {  // S_x = Q_x K^T, K in stage kst (one thread)
-                const uint32_t qo = x * (32768 >> 4), ko = kst * (32768 >> 4);
+                const uint32_t qo = x * (kQTile >> 4), ko = kst * (kTile >> 4);
                 const uint32_t dst = tbase + x * 256;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
+                for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
                     tc::mma_bf16(dst, at(dq, qo + o), at(dk, ko + o), ID_QK, ks > 0 ? 1u : 0u);
                 }
@@ -378,7 +395,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 tc::mma_commit(&s_full[x]);
             };
             auto issue_pv = [&](int x, int vst, bool first) {  // O_x += P V (fp16), V in stage vst (one thread)
-                const uint32_t vo = vst * (32768 >> 4);
+                const uint32_t vo = vst * (kTile >> 4);
                 const uint32_t pcol = tbase + x * 256, dst = pcol + 128;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
@@ -453,10 +470,10 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 ok = __all_sync(kFull, ok);
                 if (!ok) break;
                 const int kb = (kt0 + j) * kKT;
-                uint4* vs = reinterpret_cast<uint4*>(sm + kV0 + (j % kVS) * 32768);
+                uint4* vs = reinterpret_cast<uint4*>(sm + kV0 + (j % kVS) * kTile);
                 const int valid = ctx - kb;  // key rows of this tile inside the context (may exceed 128)
 #pragma unroll 4
-                for (int c = 0; c < 16; ++c) {
+                for (int c = 0; c < (int)(kTile / 2048); ++c) {
                     const int e = t + 128 * c;
                     uint4 w = vs[e];
                     if (((e & 1023) >> 3) >= valid) w = make_uint4(0, 0, 0, 0);
@@ -594,7 +611,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                     ok = __all_sync(kFull, ok);
                     tc::fence_after_sync();
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < D / 32; ++c) {
                         uint32_t raw[32];
                         tc::tmem_ld32(tO + c * 32, raw);
                         tc::tmem_wait_ld();
@@ -617,7 +634,7 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 float* dst = part_base + ((size_t)x * 128 + r) * kPartStride;
                 bool finite = true;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t raw[32];
                     tc::tmem_ld32(tO + c * 32, raw);
                     tc::tmem_wait_ld();
@@ -635,14 +652,14 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                     }
                 }
                 if (!finite) pa::set_error(P.err, PA_DEVERR_RANGE);
-                if (i < L) *reinterpret_cast<float2*>(dst + 128) = make_float2(m_used, l);
+                if (i < L) *reinterpret_cast<float2*>(dst + kPartML) = make_float2(m_used, l);
             } else if (ok) {
                 tc::fence_after_sync();
                 const float inv = 256.f / l;  // with V's 2^-8 undone
-                uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)(q0 + i) * H + h0 + r % G) * kD);
+                uint4* dst = reinterpret_cast<uint4*>(P.out + ((size_t)(q0 + i) * H + h0 + r % G) * D);
                 bool finite = true;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t raw[32];
                     tc::tmem_ld32(tO + c * 32, raw);
                     tc::tmem_wait_ld();
@@ -762,18 +779,19 @@ __global__ void __launch_bounds__(1024) pa_prefill_plan_kernel(const PrefillPara
 }
 
 // Combines the pieces of one output row: O = sum_k O_k 2^(m_k - M),
-// l = sum_k l_k 2^(m_k - M), out = O / l (lane: 4 of the 128 dims). Piece k
-// covers key tiles piece_range(n_kt_all, k, n_pieces); empty ones wrote
-// nothing and are skipped. Lane k reads piece k's (m, l) (n_pieces <= 64),
-// then every piece's O slice is loaded in one batch.
-template <typename PartOf>
+// l = sum_k l_k 2^(m_k - M), out = O / l (lane: D / 32 consecutive dims).
+// Piece k covers key tiles piece_range(n_kt_all, k, n_pieces); empty ones
+// wrote nothing and are skipped. Lane k reads piece k's (m, l)
+// (n_pieces <= 64), then every piece's O slice is loaded in one batch.
+template <int D, typename PartOf>
 __device__ __forceinline__ void merge_row(int n_pieces, int n_kt_all, PartOf part_of, int lane, uint16_t* out_row) {
+    constexpr int NV = D / 32;  // dims per lane: 4 or 2
     float m_mine = -INFINITY, l_mine = 0.f;
     for (int k = lane; k < n_pieces; k += 32) {
         int a, b;
         piece_range(n_kt_all, k, n_pieces, a, b);
         if (b > a) {
-            const float2 ml = *reinterpret_cast<const float2*>(part_of(k) + 128);
+            const float2 ml = *reinterpret_cast<const float2*>(part_of(k) + kPartML);
             if (ml.x > m_mine) {  // keep the larger reference; rescale the other sum
                 l_mine = l_mine * (m_mine == -INFINITY ? 0.f : pa::fast_exp2(m_mine - ml.x)) + ml.y;
                 m_mine = ml.x;
@@ -788,9 +806,9 @@ __device__ __forceinline__ void merge_row(int n_pieces, int n_kt_all, PartOf par
     float l = m_mine == -INFINITY ? 0.f : l_mine * pa::fast_exp2(m_mine - M);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[NV] = {};
     for (int k0 = 0; k0 < n_pieces; k0 += 8) {
-        float4 v[8];
+        float v[8][NV];
         float f[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -798,28 +816,39 @@ __device__ __forceinline__ void merge_row(int n_pieces, int n_kt_all, PartOf par
             int a = 0, b = 0;
             if (k < n_pieces) piece_range(n_kt_all, k, n_pieces, a, b);
             f[u] = 0.f;
-            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < NV; ++e) v[u][e] = 0.f;
             if (b > a) {
                 const float* src = part_of(k);
-                const float m = src[128];
+                const float m = src[kPartML];
                 f[u] = m == -INFINITY ? 0.f : pa::fast_exp2(m - M);
-                v[u] = *reinterpret_cast<const float4*>(src + lane * 4);
+                if constexpr (NV == 4) {
+                    const float4 t = *reinterpret_cast<const float4*>(src + lane * 4);
+                    v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+                } else {
+                    const float2 t = *reinterpret_cast<const float2*>(src + lane * 2);
+                    v[u][0] = t.x; v[u][1] = t.y;
+                }
             }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            acc.x += v[u].x * f[u]; acc.y += v[u].y * f[u]; acc.z += v[u].z * f[u]; acc.w += v[u].w * f[u];
-        }
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int e = 0; e < NV; ++e) acc[e] += v[u][e] * f[u];
     }
     const float inv = 1.f / l;
-    uint2 pk;
-    pk.x = pa::float2_to_bf16x2(acc.x * inv, acc.y * inv);
-    pk.y = pa::float2_to_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(out_row + lane * 4) = pk;
+    if constexpr (NV == 4) {
+        uint2 pk;
+        pk.x = pa::float2_to_bf16x2(acc[0] * inv, acc[1] * inv);
+        pk.y = pa::float2_to_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(out_row + lane * 4) = pk;
+    } else {
+        *reinterpret_cast<uint32_t*>(out_row + lane * 2) = pa::float2_to_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
 }
 
 // Per-pair mode with splits > 1: one warp per (chunk row, query head).
-template <int G>
+template <int G, int D>
 __global__ void __launch_bounds__(128)
 pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int n_qp) {
     constexpr int QT = kRows / G;
@@ -843,15 +872,15 @@ pa_prefill_merge_kernel(const PrefillParams P, int n_seqs, int n_rows_total, int
     const int i0 = qp * 2 * QT;
     const int n_kt_all = (ctx - L + min(i0 + 2 * QT, L) - 1) / kKT + 1;
     const size_t item = ((size_t)s * Hk + kvh) * n_qp + qp;
-    merge_row(P.splits, n_kt_all,
-              [&](int k) { return P.part + (((item * P.splits + k) * 2 + x) * 128 + r) * kPartStride; }, lane,
-              P.out + ((size_t)t * H + h) * kD);
+    merge_row<D>(P.splits, n_kt_all,
+                 [&](int k) { return P.part + (((item * P.splits + k) * 2 + x) * 128 + r) * kPartStride; }, lane,
+                 P.out + ((size_t)t * H + h) * D);
 }
 
 // Balanced mode: one warp per (row, head) of the cut pairs, warp w = 256 *
 // (cut pair) + 128 * (query tile) + (tile row); the cut pairs are the
 // piece-0 entries of the work list's tail.
-template <int G>
+template <int G, int D>
 __global__ void __launch_bounds__(128) pa_prefill_merge_cut_kernel(const PrefillParams P) {
     constexpr int QT = kRows / G;
     pa::grid_dependency_wait();  // every piece's partial is written
@@ -867,14 +896,15 @@ __global__ void __launch_bounds__(128) pa_prefill_merge_cut_kernel(const Prefill
     if (i >= L) return;
     const int n_kt_all = (ctx - L + min(i0 + 2 * QT, L) - 1) / kKT + 1;
     const size_t slot0 = (size_t)t * S;
-    merge_row(S, n_kt_all, [&](int k) { return P.part + (((slot0 + k) * 2 + x) * 128 + r) * kPartStride; }, lane,
-              P.out + ((size_t)(q0 + i) * P.n_heads + kvh * G + r % G) * kD);
+    merge_row<D>(S, n_kt_all, [&](int k) { return P.part + (((slot0 + k) * 2 + x) * 128 + r) * kPartStride; },
+                 lane, P.out + ((size_t)(q0 + i) * P.n_heads + kvh * G + r % G) * D);
 }
 
-template <int G>
+template <int G, int D>
 int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtensorMap& tv, int n_seqs,
                    int max_chunk_len, int n_rows, cudaStream_t stream) {
-    auto kern = pa_prefill_tc_kernel<G>;
+    auto kern = pa_prefill_tc_kernel<G, D>;
+    constexpr uint32_t kSmemBytes = PfLay<D>::kSmem;
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -895,12 +925,12 @@ int launch_prefill(const PrefillParams& Pp, const CUtensorMap& tk, const CUtenso
     }
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (Pp.work)  // the cut pairs (fewer than one per CTA): 256 rows each
-        return pa_launch_pdl(pa_prefill_merge_cut_kernel<G>, dim3((unsigned)Pp.n_cta * 64), dim3(128), 0, stream,
+        return pa_launch_pdl(pa_prefill_merge_cut_kernel<G, D>, dim3((unsigned)Pp.n_cta * 64), dim3(128), 0, stream,
                              Pp);
     if (Pp.splits <= 1) return PA_OK;
     // rows of all chunks: the merge finds each row's sequence in q_start_loc
     const long long warps = (long long)n_rows * Pp.n_heads;
-    return pa_launch_pdl(pa_prefill_merge_kernel<G>, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, stream, Pp,
+    return pa_launch_pdl(pa_prefill_merge_kernel<G, D>, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, stream, Pp,
                          n_seqs, n_rows, n_qp);
 }
 
@@ -949,7 +979,7 @@ int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_poo
     if (n_seqs < 0 || max_chunk_len < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || n_heads <= 0 ||
         n_kv_heads <= 0 || splits < 0 || splits > 64)
         return PA_ERR_INVALID_ARG;
-    if (head_dim != kD || block_size != kBS) return PA_ERR_UNSUPPORTED;
+    if ((head_dim != 64 && head_dim != 128) || block_size != kBS) return PA_ERR_UNSUPPORTED;
     if (n_heads % n_kv_heads != 0) return PA_ERR_INVALID_ARG;
     const int G = n_heads / n_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
@@ -973,8 +1003,8 @@ int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_poo
     unsigned int* err = pa_device_error_ptr();
     if (!err) return PA_ERR_CUDA;
     CUtensorMap tk, tv;
-    if (!pa_make_tmap_2d_bf16(&tk, k_pool, kD, (uint64_t)rows, kD * 2, 64, kBS) ||
-        !pa_make_tmap_2d_bf16(&tv, v_pool, kD, (uint64_t)rows, kD * 2, 64, kBS))
+    if (!pa_make_tmap_2d_bf16(&tk, k_pool, head_dim, (uint64_t)rows, head_dim * 2, 64, kBS) ||
+        !pa_make_tmap_2d_bf16(&tv, v_pool, head_dim, (uint64_t)rows, head_dim * 2, 64, kBS))
         return PA_ERR_CUDA;
     PrefillParams Pp;
     Pp.out = static_cast<uint16_t*>(out);
@@ -1006,11 +1036,20 @@ int prefill_impl(void* out, const void* q, const void* k_pool, const void* v_poo
     const long long n_rows = (long long)n_seqs * max_chunk_len;
     if (n_rows > 0x7fffffffLL || n_rows * n_heads > 0x7fffffffLL * 4LL) return PA_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int nr = (int)n_rows;
+    if (head_dim == 64) {
+        switch (G) {
+            case 1: return launch_prefill<1, 64>(Pp, tk, tv, n_seqs, max_chunk_len, nr, st);
+            case 2: return launch_prefill<2, 64>(Pp, tk, tv, n_seqs, max_chunk_len, nr, st);
+            case 4: return launch_prefill<4, 64>(Pp, tk, tv, n_seqs, max_chunk_len, nr, st);
+            default: return launch_prefill<8, 64>(Pp, tk, tv, n_seqs, max_chunk_len, nr, st);
+        }
+    }
     switch (G) {
-        case 1: return launch_prefill<1>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
-        case 2: return launch_prefill<2>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
-        case 4: return launch_prefill<4>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
-        default: return launch_prefill<8>(Pp, tk, tv, n_seqs, max_chunk_len, (int)n_rows, st);
+        case 1: return launch_prefill<1, 128>(Pp, tk, tv, n_seqs, max_chunk_len, nr, st);
+        case 2: return launch_prefill<2, 128>(Pp, tk, tv, n_seqs, max_chunk_len, nr, st);
+        case 4: return launch_prefill<4, 128>(Pp, tk, tv, n_seqs, max_chunk_len, nr, st);
+        default: return launch_prefill<8, 128>(Pp, tk, tv, n_seqs, max_chunk_len, nr, st);
     }
 }
 

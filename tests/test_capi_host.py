@@ -321,8 +321,8 @@ def test_prefill_workspace_formula_and_errors(capi):
 def test_prefill_argument_errors_need_no_device(capi):
     p = C.c_void_p(4096)
     args = [p, p, p, p, p, p, p, C.c_float(0.1)]
-    # head_dim 64 is not built for prefill; block size 8 unsupported; group 3 unsupported
-    assert capi.pa_prefill_paged(*args, 8, 8, 64, 16, 2, 4, 64, 16, None) == -2
+    # head_dim 96 is not built for prefill (64 and 128 are); block size 8 unsupported; group 3 unsupported
+    assert capi.pa_prefill_paged(*args, 8, 8, 96, 16, 2, 4, 64, 16, None) == -2
     assert capi.pa_prefill_paged(*args, 8, 8, 128, 8, 2, 4, 64, 16, None) == -2
     assert capi.pa_prefill_paged(*args, 12, 4, 128, 16, 2, 4, 64, 16, None) == -2
     assert capi.pa_prefill_paged(*args, 8, 8, 128, 16, -1, 4, 64, 16, None) == -1

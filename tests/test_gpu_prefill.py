@@ -3,8 +3,9 @@
 Tolerance (per element): |gpu - ref| <= 2e-3 + 1e-2 * |ref|. Cases cover a
 whole prompt as one chunk, chunks at an offset with ragged lengths and
 partial last blocks (NaN-poisoned slots past the context), several key
-tiles, every group size, padding rows of a partial query tile, and sampled
-rows of the full mixed workload (4 chunks of 512 at 32K context).
+tiles, every group size, both head dims (64 and 128), padding rows of a
+partial query tile, and sampled rows of the full mixed workload (4 chunks of
+512 at 32K context).
 """
 import numpy as np
 import pytest
@@ -51,25 +52,28 @@ def _run(pk, wl, splits=None):
     dict(ctx=[700], lens=[33], H=64, Hk=8),               # G=8, 6 key tiles
     dict(ctx=[256, 255, 17], lens=[256, 1, 17], H=32, Hk=8),  # exact tiles, single-row chunk
 ])
-def test_prefill_matches_oracle(pk, case):
-    wl = make_prefill_case(700 + sum(case["ctx"]), case["ctx"], case["lens"], [], case["H"], case["Hk"], 128)
+@pytest.mark.parametrize("head_dim", [128, 64])
+def test_prefill_matches_oracle(pk, case, head_dim):
+    wl = make_prefill_case(700 + sum(case["ctx"]) + head_dim, case["ctx"], case["lens"], [], case["H"], case["Hk"],
+                           head_dim)
     got = _run(pk, wl)
     ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
     ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
-    stats = assert_attention_close(got, ref, f"prefill {case}")
+    stats = assert_attention_close(got, ref, f"prefill head_dim {head_dim} {case}")
     check_device_error(0)
     print(case, stats)
 
 
-def test_prefill_hot_logits(pk):
+@pytest.mark.parametrize("head_dim", [128, 64])
+def test_prefill_hot_logits(pk, head_dim):
     """q x 16: row maxima grow tile after tile, exercising the O rescale path."""
-    wl = make_prefill_case(731, [600], [64], [], 32, 8, 128)
+    wl = make_prefill_case(731 + head_dim, [600], [64], [], 32, 8, head_dim)
     qf = (wl.q_pf.astype(np.uint32) << 16).view(np.float32) * 16.0
     wl.q_pf = ((qf.view(np.uint32) + 0x8000) >> 16).astype(np.uint16)
     got = _run(pk, wl)
     ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
     ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
-    assert_attention_close(got, ref, "prefill hot")
+    assert_attention_close(got, ref, f"prefill hot, head_dim {head_dim}")
     check_device_error(0)
 
 
@@ -135,6 +139,19 @@ def test_prefill_split_pieces_match_oracle(pk, case, splits):
     ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
     ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
     assert_attention_close(got, ref, f"prefill split={splits} {case}")
+    check_device_error(0)
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_prefill_split_pieces_head_dim_64(pk, splits):
+    """The merge at head_dim 64 (two dims per lane): pieces of long key
+    ranges, empty pieces, every group size in one batch of sequences."""
+    for G, (ctx, lens) in {1: ([900, 33], [130, 33]), 8: ([1500, 40], [300, 40])}.items():
+        wl = make_prefill_case(860 + G + splits, ctx, lens, [], 8 * G, 8, 64)
+        got = _run(pk, wl, splits)
+        ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
+        ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
+        assert_attention_close(got, ref, f"prefill head_dim 64 group {G} split={splits}")
     check_device_error(0)
 
 
