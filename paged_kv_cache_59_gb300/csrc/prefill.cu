@@ -472,17 +472,22 @@ pa_prefill_tc_kernel(const PrefillParams P, const __grid_constant__ CUtensorMap 
                 const int kb = (kt0 + j) * kKT;
                 uint4* vs = reinterpret_cast<uint4*>(sm + kV0 + (j % kVS) * kTile);
                 const int valid = ctx - kb;  // key rows of this tile inside the context (may exceed 128)
+                auto convert = [&](auto partial) {
 #pragma unroll 4
-                for (int c = 0; c < (int)(kTile / 2048); ++c) {
-                    const int e = t + 128 * c;
-                    uint4 w = vs[e];
-                    if (((e & 1023) >> 3) >= valid) w = make_uint4(0, 0, 0, 0);
-                    w.x = cvt(w.x);
-                    w.y = cvt(w.y);
-                    w.z = cvt(w.z);
-                    w.w = cvt(w.w);
-                    vs[e] = w;
-                }
+                    for (int c = 0; c < (int)(kTile / 2048); ++c) {
+                        const int e = t + 128 * c;
+                        uint4 w = vs[e];
+                        if constexpr (decltype(partial)::value)
+                            if (((e & 1023) >> 3) >= valid) w = make_uint4(0, 0, 0, 0);
+                        w.x = cvt(w.x);
+                        w.y = cvt(w.y);
+                        w.z = cvt(w.z);
+                        w.w = cvt(w.w);
+                        vs[e] = w;
+                    }
+                };
+                if (valid < kKT) convert(std::true_type{});  // the context ends inside this tile
+                else convert(std::false_type{});
                 tc::fence_async_smem();  // generic-proxy writes, read next by the tensor core
                 __syncwarp();
                 if (lane == 0) pa::mbar_arrive(&v_conv[j % kVS]);
