@@ -1183,11 +1183,19 @@ int sm_count() {
 // Default partition size of the CUDA-core kernel. One CTA streams one
 // partition of one (sequence, KV head); when the grid is a few waves of CTA
 // slots deep, a last wave that fills only part of the slots leaves SMs idle.
-// Among the multiples of 64 tokens in [512, 1024] (each needs no more
+// When one CTA per (sequence, KV head) gives every SM at least one and fits
+// a single wave (sms <= n_seqs x n_kv_heads <= slots) and a context fits one
+// partition (<= 2048 tokens), each sequence takes a single partition: one
+// wave of HBM-bound streams, no split-K partials and no merge. Otherwise,
+// among the multiples of 64 tokens in [512, 1024] (each needs no more
 // workspace than 512), take the one whose grid - n_seqs x n_kv_heads x
 // ceil(context / size) CTAs, exact when every context is `context` - fills
 // its last wave best (waves / ceil(waves)), the smallest on ties.
-int wave_partition_tokens(int n_seqs, int n_kv_heads, int context, int slots) {
+int wave_partition_tokens(int n_seqs, int n_kv_heads, int context, int sms, int slots) {
+    const long long groups = (long long)n_seqs * n_kv_heads;
+    if (sms > 0 && groups >= sms && groups <= slots && context > kDefaultPartitionTokens &&
+        context <= 4 * kDefaultPartitionTokens)
+        return (context + 63) / 64 * 64;
     if (slots <= 0 || context <= kDefaultPartitionTokens) return kDefaultPartitionTokens;
     int best = kDefaultPartitionTokens;
     double best_fill = -1.0;
@@ -1207,7 +1215,8 @@ int default_partition_tokens(bool tensor, int eb, int n_seqs, int n_kv_heads, in
                              int max_context_len, int window) {
     if (tensor) return 2 * kDefaultPartitionTokens;
     const int span = window >= 0 && window + 2 * kBS < max_context_len ? window + 2 * kBS : max_context_len;
-    return wave_partition_tokens(n_seqs, n_kv_heads, span, sm_count() * k1_ctas_per_sm(head_dim, G, eb));
+    const int sms = sm_count();
+    return wave_partition_tokens(n_seqs, n_kv_heads, span, sms, sms * k1_ctas_per_sm(head_dim, G, eb));
 }
 
 int resolve_partition_tokens(int pt) {

@@ -127,3 +127,56 @@ def test_hundreds_of_partitions(pk, tc):
     out = _run(pk, d, wl, ws, 64, tc)
     assert_attention_close(host_bits(out), ref, f"313 partitions tc={tc}")
     check_device_error(0)
+
+
+def _default_rule(n_seqs, n_kv_heads, span, sms, slots):
+    """The CUDA-core kernel's default partition size, restated: one partition
+    per sequence when one CTA per (sequence, KV head) covers every SM in a
+    single wave and a context fits 2048 tokens; otherwise the multiple of 64
+    in [512, 1024] whose grid fills its last wave of CTA slots best."""
+    groups = n_seqs * n_kv_heads
+    if sms <= groups <= slots and 512 < span <= 2048:
+        return -(-span // 64) * 64
+    if span <= 512:
+        return 512
+    best, best_fill = 512, -1.0
+    for pt in range(512, 1025, 64):
+        waves = groups * -(-span // pt) / slots
+        fill = waves / np.ceil(waves)
+        if fill > best_fill + 1e-9:
+            best, best_fill = pt, fill
+    return best
+
+
+@pytest.mark.parametrize("shape", [
+    (8, 32, 32, 128, 2048),    # 7B MHA batch: 256 groups in one wave -> one partition of 2048
+    (8, 32, 32, 128, 1500),    # the same at a shorter bound -> 1536
+    (64, 32, 8, 128, 4096),    # 8B GQA batch: 512 groups, more than one wave
+    (4, 32, 32, 128, 2048),    # 128 groups, fewer than the SMs
+    (32, 32, 8, 128, 4096),    # one partition would exceed 2048 tokens
+])
+def test_default_partition_tokens_follow_the_rule(pk, capi, shape):
+    torch = torch_cuda()
+    n_seqs, H, Hk, D, ctx = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    want = _default_rule(n_seqs, Hk, ctx, sms, 3 * sms)   # 3 CTAs per SM for groups up to 4
+    assert pk.pa_decode_partition_tokens(n_seqs, H, Hk, D, ctx) == want
+
+
+def test_single_partition_default_matches_oracle(pk):
+    """Uneven contexts up to 2048 tokens over 160 (sequence, KV head) groups
+    of MHA: the default takes one partition per sequence, no merge."""
+    torch = torch_cuda()
+    rng = np.random.default_rng(77)
+    ctx = [2048, 1, 17, 1500] + [int(c) for c in rng.integers(300, 2049, 16)]
+    wl, ref, d = _case(711, ctx, H=8, Hk=8, D=128)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if not sms <= len(ctx) * 8 <= 3 * sms:
+        pytest.skip("the one-partition rule does not apply on this device")
+    assert pk.pa_decode_partition_tokens(len(ctx), 8, 8, 128, 2048) == 2048
+    assert pk.decode_workspace(d["q"], 2048) is not None       # sized for 512, the bound of every default
+    out = torch.full_like(d["q"], 0x7FC0)
+    pk.pa_decode(out, d["q"], d["kp"], d["vp"], d["tab"], d["ctx"], wl.scale, 2048)
+    torch.cuda.synchronize()
+    assert_attention_close(host_bits(out), ref, "one partition per sequence (default)")
+    check_device_error(0)
