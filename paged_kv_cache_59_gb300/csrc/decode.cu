@@ -506,9 +506,12 @@ pa_decode_partition_kernel(const DecodeParams P) {
 //                                            the 16 tokens as M, the heads as N, one
 //                                            MMA per k-step, and P^T for the P.V
 //                                            product from two movmatrix transposes)
-//   O^T[128 x 8]     += V^T . P^T           (A = V^T via ldmatrix.trans; B = P^T,
-//                                            which is S's accumulator layout as it
-//                                            stands; the 8 head rows fill N = 8)
+//   O^T[128 x 8]     += V^T . P^T           (A = V^T via ldmatrix.trans; with an
+//                                            E4M3 cache V's codes widened in
+//                                            registers and transposed by movmatrix;
+//                                            B = P^T, which is S's accumulator
+//                                            layout as it stands; the 8 head rows
+//                                            fill N = 8)
 // With a bf16 cache P enters as two bf16 terms (P_hi = p truncated, P_lo =
 // the rounded remainder), so the weights keep ~16 significant bits. (A single
 // fp16 P, as the prefill uses, would need V widened to fp16 element by element
@@ -522,17 +525,15 @@ namespace mma {
 constexpr int kNW = 4;  // warps per CTA
 // Per warp, bf16 cache: 2 stages of K 4 KiB + V 4 KiB (each two 2 KiB boxes,
 // 16 rows x 64 dims): 64 KiB per CTA, three CTAs per SM. E4M3 cache: 2
-// stages of K 2 KiB + V 2 KiB (one box of 16 rows x 128 codes each) and one
-// 4 KiB fp16 tile the V codes are widened into (K's codes are widened in
-// registers, straight from the stage): 48 KiB per CTA, four CTAs per SM (its
-// per-block work is latency-bound, so more warps per SM beat a deeper ring:
-// 67.3 -> 62.8 us on the 8B batch against three CTAs with three stages).
+// stages of K 2 KiB + V 2 KiB (one box of 16 rows x 128 codes each; both are
+// widened in registers, straight from the stage): 32 KiB per CTA and four
+// CTAs per SM, the most its registers allow (its per-block work is
+// latency-bound, so more warps per SM beat a deeper ring).
 template <int EB>
 struct Lay {
     static constexpr int kStage = EB == 2 ? 8192 : 4096;
-    static constexpr int kConv = EB == 2 ? 0 : 4096;
     static constexpr int kStages = 2;  // ring stages per warp
-    static constexpr int kWarp = kStages * kStage + kConv;
+    static constexpr int kWarp = kStages * kStage;
     static constexpr int kSmem = kNW * kWarp + kNW * kStages * 8;
 };
 
@@ -656,7 +657,6 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
     const int my_n = nb_local > warp ? (nb_local - warp + NW - 1) / NW : 0;  // <= 32
 
     unsigned char* my_stages = stages + (size_t)warp * kWarp;
-    unsigned char* my_conv = my_stages + S * kStage;  // E4M3 cache: the widened tile pair
     uint64_t* my_bars = bars + warp * S;
     if (lane == 0) {
 #pragma unroll
@@ -741,33 +741,8 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
         consumed = i + 1;
         const int bid = __shfl_sync(kFull, my_bid, i);
         if (bid >= 0 && bid < P.num_blocks) {
-            if constexpr (EB == 1) {
-                // widen the V codes into the fp16 tile (same swizzled layout as a bf16 tile):
-                // lane (row r = lane/2, half) takes 64 codes = 4 chunks of 16
-                const unsigned char* raw = my_stages + (size_t)st * kStage;
-                const int r = lane >> 1, hf = lane & 1;
-#pragma unroll
-                for (int kv = 1; kv < 2; ++kv) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int c = hf * 4 + j;  // 16-code chunk of the 128-code row
-                        const uint4 w = *reinterpret_cast<const uint4*>(raw + kv * 2048 + r * 128 +
-                                                                        ((c ^ (r & 7)) << 4));
-                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                        uint32_t h[8];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            h[2 * k] = e4m3x2_to_h2((uint16_t)(ws[k] & 0xffffu));
-                            h[2 * k + 1] = e4m3x2_to_h2((uint16_t)(ws[k] >> 16));
-                        }
-                        unsigned char* cv = my_conv;
-                        *reinterpret_cast<uint4*>(cv + sw_off(r, 2 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
-                        *reinterpret_cast<uint4*>(cv + sw_off(r, 2 * c + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-                    }
-                }
-            }
             const uint32_t kb = pa::smem_u32(my_stages + (size_t)st * kStage);
-            const uint32_t vb = EB == 2 ? kb + 4096 : pa::smem_u32(my_conv);
+            const uint32_t vb = kb + 4096;  // bf16 cache: the V tile
             const int tok0 = (blk_begin + warp + NW * i) * kBS;
             // ---- S = Q K^T: two n-tiles of 8 tokens
             float s_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -903,12 +878,12 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
                                                  pv[2 * n + 1] - __uint_as_float(by & 0xffff0000u));
                 }
             }
-            if constexpr (EB == 1) __syncwarp();  // the widened V tile is complete
             // V rows of the sequence's last, partial block past the context hold
             // whatever the pool has there (p = 0 must not meet a NaN): zero them
-            if (ctx < tok0 + kBS) {
+            // (E4M3: in registers, below)
+            if (EB == 2 && ctx < tok0 + kBS) {
                 const int r0 = ctx - tok0;
-                unsigned char* vt = EB == 2 ? my_stages + (size_t)st * kStage + 4096 : my_conv;
+                unsigned char* vt = my_stages + (size_t)st * kStage + 4096;
                 for (int e = lane; e < (kBS - r0) * 32; e += 32)  // a row: 2 boxes x 128 B
                     *reinterpret_cast<uint2*>(vt + ((e & 31) >> 4) * 2048 + (r0 + (e >> 5)) * 128 + (e & 15) * 8) =
                         make_uint2(0u, 0u);
@@ -917,14 +892,36 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
             }
             // ---- O^T += V^T P^T: 8 m-tiles of 16 dims, k = the tile's 16 tokens, n = the 8 head
             // rows; P's accumulator layout is already the B operand (tokens 2t.. and 2t+8.. of head g)
-            {
+            if constexpr (EB == 2) {
                 const int m = lane >> 3, row = 8 * (m >> 1) + (lane & 7), dh = m & 1;  // matrix: (token half, dim half)
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_t(vb + sw_off(row, 2 * mt + dh), a0, a1, a2, a3);
                     mma_full<EB>(o[mt], a0, a1, a2, a3, ph[0], ph[1]);
-                    if constexpr (EB == 2) mma_full<EB>(o[mt], a0, a1, a2, a3, pl[0], pl[1]);
+                    mma_full<EB>(o[mt], a0, a1, a2, a3, pl[0], pl[1]);
+                }
+            } else {
+                // E4M3: V^T's fragments straight from the codes. Within m-tile mt the
+                // 16 rows of O^T are the dims in the order that gives lane (g, t) the
+                // four consecutive codes 16mt + 4t .. +3 of its token rows g and g + 8:
+                // codes 4t, 4t+1 are rows 2t, 2t+1 and codes 4t+2, 4t+3 rows 8+2t,
+                // 9+2t. Widened to fp16 pairs they are the m8n8 fragments of V's
+                // four 8 x 8 (token, dim) blocks; a movmatrix transpose makes each
+                // the matching block of V^T, the A operand. Token rows past the
+                // context are zero (p = 0 must not meet a NaN).
+                const unsigned char* rv = my_stages + (size_t)st * kStage + 2048;
+                const bool lo_ok = tok0 + g < ctx, hi_ok = tok0 + g + 8 < ctx;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    const int off = ((mt ^ (g & 7)) << 4) + 4 * t;  // rows g and g + 8 share the swizzle
+                    const uint32_t w0 = lo_ok ? *reinterpret_cast<const uint32_t*>(rv + g * 128 + off) : 0u;
+                    const uint32_t w1 = hi_ok ? *reinterpret_cast<const uint32_t*>(rv + (g + 8) * 128 + off) : 0u;
+                    const uint32_t a0 = movmatrix_t(e4m3x2_to_h2((uint16_t)(w0 & 0xffffu)));
+                    const uint32_t a1 = movmatrix_t(e4m3x2_to_h2((uint16_t)(w0 >> 16)));
+                    const uint32_t a2 = movmatrix_t(e4m3x2_to_h2((uint16_t)(w1 & 0xffffu)));
+                    const uint32_t a3 = movmatrix_t(e4m3x2_to_h2((uint16_t)(w1 >> 16)));
+                    mma_full<EB>(o[mt], a0, a1, a2, a3, ph[0], ph[1]);
                 }
             }
         }
@@ -951,11 +948,16 @@ pa_decode_mma_kernel(const DecodeParams P, const __grid_constant__ CUtensorMap t
     for (int k = 0; k < 2; ++k) {  // heads 2t and 2t + 1
         const int h = 2 * t + k;
         if (h < G) {
-            float* dst = mo + ((size_t)warp * G + h) * D + g;
+            // O^T rows g and g + 8 of an m-tile: dims g and g + 8 (bf16 cache); with an
+            // E4M3 cache the rows' dims as ordered above: 2g, 2g + 2 (g even) or
+            // 2g - 1, 2g + 1 (g odd)
+            const int d_lo = EB == 2 ? g : ((g & 1) ? 2 * g - 1 : 2 * g);
+            const int d_hi = EB == 2 ? g + 8 : ((g & 1) ? 2 * g + 1 : 2 * g + 2);
+            float* dst = mo + ((size_t)warp * G + h) * D;
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
-                dst[16 * mt] = o[mt][k];
-                dst[16 * mt + 8] = o[mt][2 + k];
+                dst[16 * mt + d_lo] = o[mt][k];
+                dst[16 * mt + d_hi] = o[mt][2 + k];
             }
         }
     }
