@@ -45,7 +45,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 TRAFFIC_KERNELS = ("pa_decode_partition_kernel", "pa_decode_mma_kernel")
 TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none "
                    "-k regex:'pa_decode_(partition|mma)' -s 5 -c 2 --csv --log-file dram_{w}.csv "
-                   "python bench.py --workload {w} --steps 20 --warmup 3 --skip-baselines")
+                   "python bench.py --workload {w} --steps 20 --warmup 3 --skip-baselines --no-prefill-leg")
 
 
 def parse_args():
