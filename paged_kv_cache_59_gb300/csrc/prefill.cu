@@ -786,11 +786,65 @@ __global__ void __launch_bounds__(1024) pa_prefill_plan_kernel(const PrefillPara
 // Combines the pieces of one output row: O = sum_k O_k 2^(m_k - M),
 // l = sum_k l_k 2^(m_k - M), out = O / l (lane: D / 32 consecutive dims).
 // Piece k covers key tiles piece_range(n_kt_all, k, n_pieces); empty ones
-// wrote nothing and are skipped. Lane k reads piece k's (m, l)
-// (n_pieces <= 64), then every piece's O slice is loaded in one batch.
+// wrote nothing and are skipped. Up to 8 pieces: every lane loads every
+// piece's (m, l) (one broadcast load each) and its O slices, all at once, so
+// the row costs one round of memory latency. More pieces (n_pieces <= 64):
+// lane k reads piece k's (m, l), then the O slices are loaded 8 pieces at a
+// time.
+template <int NV>
+__device__ __forceinline__ void store_row(const float (&acc)[NV], float inv, int lane, uint16_t* out_row) {
+    if constexpr (NV == 4) {
+        uint2 pk;
+        pk.x = pa::float2_to_bf16x2(acc[0] * inv, acc[1] * inv);
+        pk.y = pa::float2_to_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(out_row + lane * 4) = pk;
+    } else {
+        *reinterpret_cast<uint32_t*>(out_row + lane * 2) = pa::float2_to_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+}
+template <int NV>
+__device__ __forceinline__ void load_slice(const float* src, int lane, float (&v)[NV]) {
+    if constexpr (NV == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(src + lane * 4);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+        const float2 t = *reinterpret_cast<const float2*>(src + lane * 2);
+        v[0] = t.x; v[1] = t.y;
+    }
+}
 template <int D, typename PartOf>
 __device__ __forceinline__ void merge_row(int n_pieces, int n_kt_all, PartOf part_of, int lane, uint16_t* out_row) {
     constexpr int NV = D / 32;  // dims per lane: 4 or 2
+    if (n_pieces <= 8) {
+        float v[8][NV];
+        float2 ml[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            int a = 0, b = 0;
+            if (k < n_pieces) piece_range(n_kt_all, k, n_pieces, a, b);
+            ml[k] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int e = 0; e < NV; ++e) v[k][e] = 0.f;
+            if (b > a) {
+                const float* src = part_of(k);
+                ml[k] = *reinterpret_cast<const float2*>(src + kPartML);
+                load_slice<NV>(src, lane, v[k]);
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) M = fmaxf(M, ml[k].x);
+        float l = 0.f, acc[NV] = {};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float f = ml[k].x == -INFINITY ? 0.f : pa::fast_exp2(ml[k].x - M);
+            l += ml[k].y * f;
+#pragma unroll
+            for (int e = 0; e < NV; ++e) acc[e] += v[k][e] * f;
+        }
+        store_row<NV>(acc, 1.f / l, lane, out_row);
+        return;
+    }
     float m_mine = -INFINITY, l_mine = 0.f;
     for (int k = lane; k < n_pieces; k += 32) {
         int a, b;
@@ -827,13 +881,7 @@ __device__ __forceinline__ void merge_row(int n_pieces, int n_kt_all, PartOf par
                 const float* src = part_of(k);
                 const float m = src[kPartML];
                 f[u] = m == -INFINITY ? 0.f : pa::fast_exp2(m - M);
-                if constexpr (NV == 4) {
-                    const float4 t = *reinterpret_cast<const float4*>(src + lane * 4);
-                    v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
-                } else {
-                    const float2 t = *reinterpret_cast<const float2*>(src + lane * 2);
-                    v[u][0] = t.x; v[u][1] = t.y;
-                }
+                load_slice<NV>(src, lane, v[u]);
             }
         }
 #pragma unroll
@@ -841,15 +889,7 @@ __device__ __forceinline__ void merge_row(int n_pieces, int n_kt_all, PartOf par
 #pragma unroll
             for (int e = 0; e < NV; ++e) acc[e] += v[u][e] * f[u];
     }
-    const float inv = 1.f / l;
-    if constexpr (NV == 4) {
-        uint2 pk;
-        pk.x = pa::float2_to_bf16x2(acc[0] * inv, acc[1] * inv);
-        pk.y = pa::float2_to_bf16x2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2*>(out_row + lane * 4) = pk;
-    } else {
-        *reinterpret_cast<uint32_t*>(out_row + lane * 2) = pa::float2_to_bf16x2(acc[0] * inv, acc[1] * inv);
-    }
+    store_row<NV>(acc, 1.f / l, lane, out_row);
 }
 
 // Per-pair mode with splits > 1: one warp per (chunk row, query head).

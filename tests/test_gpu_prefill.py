@@ -124,7 +124,7 @@ def test_prefill_mixed_workload_sampled_rows(pk):
     check_device_error(0)
 
 
-@pytest.mark.parametrize("splits", [0, 2, 3, 5, 8])
+@pytest.mark.parametrize("splits", [0, 2, 3, 5, 8, 13])   # the merge combines up to 8 pieces in one round, more in batches
 @pytest.mark.parametrize("case", [
     dict(ctx=[300, 129], lens=[37, 129], H=32, Hk=8),     # G=4, offsets, partial blocks (few key tiles)
     dict(ctx=[700], lens=[33], H=64, Hk=8),               # G=8, 6 key tiles
