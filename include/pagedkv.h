@@ -106,12 +106,16 @@ size_t pa_decode_workspace_bytes(int n_seqs, int n_heads, int head_dim,
  * The partition size (tokens per context partition) pa_decode, pa_decode_fp8
  * (elem_bytes 1) and pa_decode_window (window >= 0; -1 for none) use when
  * partition_tokens is 0, for this batch shape on the current device: 1024 on
- * the tensor-core kernel; on the CUDA-core kernel the multiple of 64 in
+ * the tensor-core kernel. On the CUDA-core kernel, with context =
+ * max_context_len (or the window's span): when n_seqs x n_kv_heads is at
+ * least the device's SM count and at most its CTA slots (one wave) and the
+ * context is at most 2048 tokens, the context rounded up to 64 (one
+ * partition per sequence, no split-K merge); otherwise the multiple of 64 in
  * [512, 1024] whose grid of n_seqs x n_kv_heads x ceil(context / size) CTAs
- * (context = max_context_len, or the window's span) fills the last wave of
- * the device's CTA slots best, the smallest on ties. Every such size needs
- * no more workspace than pa_decode_workspace_bytes(..., 0) gives. Negative
- * status for arguments the decode entry points would reject.
+ * fills the last wave of the device's CTA slots best, the smallest on ties.
+ * Every such size needs no more workspace than
+ * pa_decode_workspace_bytes(..., 0) gives. Negative status for arguments the
+ * decode entry points would reject.
  */
 int pa_decode_partition_tokens(int n_seqs, int n_heads, int n_kv_heads, int head_dim,
                                int max_context_len, int window, int elem_bytes);
