@@ -11,8 +11,9 @@ import pytest
 
 from oracle.attention import paged_decode, paged_prefill
 from oracle.cache_ops import reshape_and_cache as o_rac
+from oracle.fp8 import paged_decode_fp8
 from tests._gpu import assert_attention_close, check_device_error, dev, host_bits, torch_cuda
-from workloads import make_decode_case, make_prefill_case
+from workloads import make_decode_case, make_decode_case_fp8, make_prefill_case
 
 pytestmark = pytest.mark.gpu
 
@@ -61,10 +62,36 @@ def test_decode_writes_stay_inside(pk, H, Hk, tc, pt):
     check_device_error(0)
 
 
-@pytest.mark.parametrize("splits", [None, 0, 3])
-def test_prefill_writes_stay_inside(pk, splits):
+@pytest.mark.parametrize("pt", [0, 64])
+def test_fp8_decode_writes_stay_inside(pk, pt):
+    """The E4M3 tensor-core kernel (V widened in registers, outputs in a
+    permuted dims order put back by its epilogue)."""
     torch = torch_cuda()
-    wl = make_prefill_case(62, [300, 129, 40], [37, 129, 40], [], 32, 8, 128)
+    ctx = [1, 17, 300, 1000, 2049]
+    H, Hk, D = 32, 8, 128
+    wl = make_decode_case_fp8(63 + pt, ctx, H, Hk, D, n_new=0)
+    n = len(ctx)
+    out_buf, out_bytes = _guarded(n * H * D * 2)
+    out = out_bytes.view(torch.int16).view(n, H, D)
+    wsb = pk.pa_decode_workspace_bytes(n, H, D, max(ctx), pt)
+    ws_buf, ws = _guarded(wsb)
+    pk.pa_decode_fp8(out, dev(wl.q), dev(wl.k_pool), dev(wl.v_pool), dev(wl.meta["k_scale"]),
+                     dev(wl.meta["v_scale"]), dev(wl.dec_tables), dev(wl.dec_ctx), wl.scale, max(ctx),
+                     workspace=ws, partition_tokens=pt)
+    torch.cuda.synchronize()
+    assert _guards_intact(out_buf), "fp8 decode wrote outside out"
+    assert _guards_intact(ws_buf), "fp8 decode wrote outside the workspace"
+    ref = paged_decode_fp8(wl.q, wl.k_pool, wl.v_pool, wl.dec_tables, wl.dec_ctx, wl.scale, wl.meta["k_scale"],
+                           wl.meta["v_scale"])
+    assert_attention_close(host_bits(out), ref, f"guarded fp8 decode pt={pt}")
+    check_device_error(0)
+
+
+@pytest.mark.parametrize("head_dim", [128, 64])
+@pytest.mark.parametrize("splits", [None, 0, 3])
+def test_prefill_writes_stay_inside(pk, splits, head_dim):
+    torch = torch_cuda()
+    wl = make_prefill_case(62 + head_dim, [300, 129, 40], [37, 129, 40], [], 32, 8, head_dim)
     kp, vp = dev(wl.k_pool), dev(wl.v_pool)
     pk.pa_reshape_and_cache(dev(wl.new_k), dev(wl.new_v), kp, vp, dev(wl.slot_mapping))
     q = dev(wl.q_pf)
@@ -86,5 +113,5 @@ def test_prefill_writes_stay_inside(pk, splits):
         assert _guards_intact(ws_buf), "prefill wrote outside the workspace"
     ek, ev = o_rac(wl.new_k, wl.new_v, wl.k_pool, wl.v_pool, wl.slot_mapping)
     ref = paged_prefill(wl.q_pf, ek, ev, wl.pf_tables, wl.pf_ctx, wl.q_start_loc, wl.scale)
-    assert_attention_close(host_bits(out), ref, f"guarded prefill splits={splits}")
+    assert_attention_close(host_bits(out), ref, f"guarded prefill splits={splits} head_dim={head_dim}")
     check_device_error(0)
