@@ -570,13 +570,6 @@ __device__ __forceinline__ uint32_t f2_to_h2(float a, float b) {  // fp16x2, a i
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
     return r;
 }
-__device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
-    float a, b;
-    asm("{\n\t.reg .f16 x, y;\n\tmov.b32 {x, y}, %2;\n\tcvt.f32.f16 %0, x;\n\tcvt.f32.f16 %1, y;\n\t}"
-        : "=f"(a), "=f"(b)
-        : "r"(h));
-    return make_float2(a, b);
-}
 // transposes an 8 x 8 matrix of 16-bit elements held in the m8n8 fragment
 // layout (lane l: row l / 4, columns 2 (l % 4), +1)
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
