@@ -464,6 +464,7 @@ def run_ours(args):
     achieved = alg_bytes / (dec_avg / 1e3) / 1e9
     traffic = profiled_traffic(args.workload) if pt == 0 else None
 
+    step_tokens = B + (int(wl.q_start_loc[-1]) if has_pf else 0)
     result = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -497,10 +498,12 @@ def run_ours(args):
                 B, H, Hk, D, max_ctx, window if window is not None else -1, eb),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
-        "tokens_per_s": round(world * B / (ms_per_step / 1e3), 1),
+        # tokens the step produces: one per decode sequence, plus every prefill
+        # chunk token on the mixed workload
+        "tokens_per_s": round(world * step_tokens / (ms_per_step / 1e3), 1),
         "kv_tokens_per_s": round(world * sum_ctx / (ms_per_step / 1e3), 1),
         "attention_only_model_tokens_per_s": round(
-            world * B / (ms_per_step / 1e3) / WORKLOAD_LAYERS[args.workload], 1),
+            world * step_tokens / (ms_per_step / 1e3) / WORKLOAD_LAYERS[args.workload], 1),
         "hbm_frac_of_measured": round(value / world / peak, 4),
         "hbm_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {
