@@ -69,6 +69,8 @@ def parse_args():
     ap.add_argument("--record-traffic", metavar="CSV",
                     help="store the decode kernel's ncu DRAM bytes per launch from CSV for --workload "
                          "in profiles/traffic.json, then exit")
+    ap.add_argument("--no-plan", action="store_true",
+                    help="decode without the host-built work plan (pa_decode / _fp8 / _window in grid order)")
     ap.add_argument("--no-prefill-leg", action="store_true",
                     help="skip the tensor-core prefill leg of the default run")
     return ap.parse_args()
@@ -356,8 +358,19 @@ def run_ours(args):
         else:
             pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
 
+    # the decode call's work plan, built on the host from the batch's lengths
+    # (which do not change between the steps) and kept on the device like the tables
+    plan_host = None if args.no_plan else pk.pa_decode_plan(
+        wl.dec_ctx, H, Hk, D, wl.dec_tables.shape[1], max_ctx, wl.num_blocks,
+        window=-1 if window is None else window, elem_bytes=eb, partition_tokens=pt)
+    plan = to_dev(plan_host) if plan_host is not None else None
+
     def decode():
-        if fp8:
+        if plan is not None:
+            pk.pa_decode_planned(out, q, kp, vp, tabs, ctx, wl.scale, max_ctx, plan,
+                                 k_scale=ks if fp8 else None, v_scale=vs if fp8 else None,
+                                 window=-1 if window is None else window, workspace=ws, partition_tokens=pt)
+        elif fp8:
             pk.pa_decode_fp8(out, q, kp, vp, ks, vs, tabs, ctx, wl.scale, max_ctx, workspace=ws,
                              partition_tokens=pt)
         elif window is not None:
@@ -496,6 +509,10 @@ def run_ours(args):
             "l2": f"no flush: the KV stream ({kv_bytes / 1e6:.0f} MB/step) exceeds the 129 MB L2",
             "partition_tokens": pt or pk.pa_decode_partition_tokens(
                 B, H, Hk, D, max_ctx, window if window is not None else -1, eb),
+            "decode_plan": ("none: the decode call's CTAs in grid order" if plan_host is None else
+                            f"pa_decode_planned over a host-built plan (pa_decode_plan) of {len(plan_host)} "
+                            "work items, longest partitions first, built once (the lengths do not change "
+                            "between steps) and resident like the block tables"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         # tokens the step produces: one per decode sequence, plus every prefill
@@ -509,7 +526,8 @@ def run_ours(args):
         "roofline": {
             "bound": "hbm",
             "kernel": (("pa_decode_mma_kernel (warp-level tensor-core MMAs)" if tc_path else
-                        "pa_decode_partition_kernel") + " + pa_decode_merge_kernel (one decode call)"),
+                        "pa_decode_partition_kernel") + " + pa_decode_merge_kernel (one decode call"
+                       + (", CTAs from the host-built plan)" if plan_host is not None else ")")),
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_source": f"{peak_kind} HBM copy GB/s",
@@ -541,7 +559,7 @@ def run_ours(args):
     if not args.skip_baselines:
         result["e2e"] = run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world,
                                 dist if world > 1 else None,
-                                (ks, vs) if fp8 else None)
+                                (ks, vs) if fp8 else None, plan_host)
         if rank == 0:
             # an oracle process holds its own host copy of the pools plus numpy's working arrays
             child_bytes = int(1.2 * 2 * kp.numel() * kp.element_size()) + (256 << 20)
@@ -716,7 +734,8 @@ def prefill_roofline(flops, ms, ws):
                 "masked halves of the diagonal tiles; CUDA events around each call"}
 
 
-def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dist, fp8_scales=None):
+def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dist, fp8_scales=None,
+            plan_host=None):
     """Same metric through the public API with host buffers. Each step copies
     its inputs (q, new K/V, slots, tables, context lengths) from page-locked
     host memory, runs the hot path and copies the output back, then the host
@@ -731,6 +750,9 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
     srcs = [wl.q, new_k, new_v, slots, wl.dec_tables, wl.dec_ctx]
     if has_pf:
         srcs += [wl.q_pf, wl.pf_tables, wl.pf_ctx, wl.q_start_loc]
+    i_plan = len(srcs)
+    if plan_host is not None:  # the decode plan travels with the other inputs
+        srcs.append(plan_host)
     srcs = [np.ascontiguousarray(x) for x in srcs]
     offs, off = [], 0
     for x in srcs:                                  # 256-byte aligned slots in one buffer
@@ -765,10 +787,16 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
             else:
                 pk.pa_reshape_and_cache(nk, nv, kp, vp, sl)
         if has_pf:
-            q_pf, pf_tabs, pf_ctx, qsl = d_in[6:]
+            q_pf, pf_tabs, pf_ctx, qsl = d_in[6:10]
             pk.pa_prefill_paged_ex(d_out[1], q_pf, kp, vp, pf_tabs, pf_ctx, qsl, wl.scale, max_chunk,
                                    splits=0, workspace=ws_pf)
-        if fp8_scales is not None:
+        if plan_host is not None:
+            pk.pa_decode_planned(d_out[0], q, kp, vp, tabs, ctx, wl.scale, max_ctx, d_in[i_plan],
+                                 k_scale=fp8_scales[0] if fp8_scales else None,
+                                 v_scale=fp8_scales[1] if fp8_scales else None,
+                                 window=-1 if wl.meta.get("window") is None else wl.meta["window"],
+                                 workspace=ws, partition_tokens=args.partition_tokens)
+        elif fp8_scales is not None:
             pk.pa_decode_fp8(d_out[0], q, kp, vp, *fp8_scales, tabs, ctx, wl.scale, max_ctx, workspace=ws,
                              partition_tokens=args.partition_tokens)
         elif wl.meta.get("window") is not None:
@@ -820,7 +848,8 @@ def run_e2e(args, pk, wl, new_k, new_v, slots, kp, vp, dev, kv_bytes, world, dis
     res = {"value": round(world * kv_bytes * n / dt / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": round(dt * 1e3 / n, 5),
-           "how": "wall clock over K steps; each step: one pinned host-to-device copy of all inputs, the "
+           "how": "wall clock over K steps; each step: one pinned host-to-device copy of all inputs (with the "
+                  "decode plan, when used), the "
                   "step's kernels, one device-to-host copy of the output, host waits; the step is "
                   + ("replayed as a captured CUDA graph" if graph is not None else "run eagerly")}
     if graph is None:

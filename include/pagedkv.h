@@ -81,10 +81,12 @@ enum pa_device_error {
                                prefill chunk longer than its context */
     PA_DEVERR_LAYOUT = 32,  /* the shared-memory base was not 1024-byte aligned
                                (prefill; nothing computed) */
-    PA_DEVERR_RANGE = 64    /* a prefill output (or split partial) was not finite:
+    PA_DEVERR_RANGE = 64,   /* a prefill output (or split partial) was not finite:
                                a V element beyond +-65504*2^8 in a key tile the
                                chunk reads (the P.V product stages V in fp16), or
                                non-finite inputs */
+    PA_DEVERR_PLAN = 128    /* a pa_decode_planned item outside the call's bounds
+                               (that CTA did nothing) */
 };
 
 /* ------------------------------------------------------------------ decode */
@@ -351,6 +353,44 @@ int pa_decode_fp8(void* out, const void* q, const void* k_pool, const void* v_po
                   int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
                   int max_context_len, int num_blocks, int partition_tokens, void* workspace,
                   size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Host-side work plan for one decode call, for callers that hold the batch's
+ * context lengths on the host (a block manager does): the call's work items,
+ * one per CTA, each a (partition, KV head, sequence) of the partition
+ * kernel, the longest partitions first (the short last partitions of the
+ * sequences run at the end, where a grid in plain order can end on full
+ * partitions that started late). No device work; the plan stays valid for
+ * any call whose lengths give every sequence the same number of partitions.
+ *  context_lens   HOST int32 [n_seqs]: the lengths the call will get
+ *  other arguments as the decode entry points (num_blocks and elem_bytes
+ *                 pick the kernel and so the default partition size;
+ *                 window -1 for none; partition_tokens 0 = default)
+ *  items          HOST int32 [cap][4], written as (partition, kv head,
+ *                 sequence, 0); NULL to query the count
+ * Returns the item count, or a negative status (PA_ERR_CAPACITY when cap is
+ * too small).
+ */
+int pa_decode_plan(const int32_t* context_lens, int n_seqs, int n_heads, int n_kv_heads, int head_dim,
+                   int max_blocks_per_seq, int max_context_len, int num_blocks, int window,
+                   int elem_bytes, int partition_tokens, int32_t* items, int cap);
+
+/*
+ * pa_decode_ex (k_scale, v_scale NULL), pa_decode_fp8 (both given) or, with
+ * window >= 0, pa_decode_window, run from a plan: CTA i computes item i of
+ * items (DEVICE int32 [n_items][4], 16-byte aligned), which must be
+ * pa_decode_plan's output for the same lengths and arguments. The results
+ * are bit-identical to the unplanned call's. An item outside the call's
+ * bounds sets PA_DEVERR_PLAN and is skipped; a plan missing items leaves
+ * their outputs unwritten.
+ */
+int pa_decode_planned(void* out, const void* q, const void* k_pool, const void* v_pool,
+                      const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                      const int32_t* context_lens, float scale, int n_heads, int n_kv_heads,
+                      int head_dim, int block_size, int n_seqs, int max_blocks_per_seq,
+                      int max_context_len, int num_blocks, int window, int partition_tokens,
+                      const int32_t* items, int n_items, void* workspace, size_t workspace_bytes,
+                      pa_stream_t stream);
 
 /* ------------------------------------------------------- chunked prefill */
 

@@ -275,6 +275,63 @@ def pa_decode_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, contex
     check("pa_decode_fp8", st)
 
 
+def pa_decode_plan(context_lens, n_heads: int, n_kv_heads: int, head_dim: int, max_blocks_per_seq: int,
+                   max_context_len: int, num_blocks: int, window: int = -1, elem_bytes: int = 2,
+                   partition_tokens: int = 0):
+    """The decode call's work items, longest partitions first, from HOST
+    context lengths (a sequence of ints or an int32 array): an int32 numpy
+    array [n_items][4] of (partition, kv head, sequence, 0)."""
+    import numpy as np
+    ctx = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32).reshape(-1))
+    args = (ctx.ctypes.data_as(C.c_void_p), len(ctx), n_heads, n_kv_heads, head_dim, max_blocks_per_seq,
+            int(max_context_len), num_blocks, int(window), elem_bytes, int(partition_tokens))
+    n = int(load().pa_decode_plan(*args, None, 0))
+    check("pa_decode_plan", min(n, 0))
+    items = np.zeros((max(n, 1), 4), dtype=np.int32)
+    st = int(load().pa_decode_plan(*args, items.ctypes.data_as(C.c_void_p), n))
+    check("pa_decode_plan", min(st, 0))
+    return items[:st]
+
+
+def pa_decode_planned(out, q, k_pool, v_pool, block_tables, context_lens, scale: float, max_context_len: int,
+                      items, k_scale=None, v_scale=None, window: int = -1, workspace=None,
+                      partition_tokens: int = 0, stream=None) -> None:
+    """pa_decode (bf16 pools), pa_decode_fp8 (uint8 pools with k_scale and
+    v_scale) or, with window >= 0, pa_decode_window, run from a plan: items is
+    pa_decode_plan's output for the same lengths and arguments, on the device
+    (int32 [n_items][4])."""
+    torch = _torch()
+    n_seqs, n_heads, head_dim = q.shape
+    num_blocks, n_kv_heads, block_size, hd2 = k_pool.shape
+    if hd2 != head_dim or tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if block_tables.dim() != 2 or block_tables.shape[0] != n_seqs or context_lens.numel() != n_seqs:
+        raise ValueError("block_tables must be [n_seqs][max_blocks], context_lens [n_seqs]")
+    if items.dim() != 2 or items.shape[1] != 4:
+        raise ValueError("items must be int32 [n_items][4]")
+    fp8 = k_pool.dtype == torch.uint8
+    if fp8 != (k_scale is not None) or (k_scale is None) != (v_scale is None):
+        raise ValueError("an fp8 (uint8) pool needs k_scale and v_scale, a bf16 pool neither")
+    ws_ptr, ws_bytes = C.c_void_p(None), 0
+    if workspace is not None:
+        ws_ptr = _ptr(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    if fp8:
+        kp, vp_ = _fp8_pool(k_pool, "k_pool"), _fp8_pool(v_pool, "v_pool")
+        ks = _ptr(k_scale, "k_scale", dtype=torch.float32)
+        vs = _ptr(v_scale, "v_scale", dtype=torch.float32)
+    else:
+        kp, vp_ = _ptr(k_pool, "k_pool", bf16=True), _ptr(v_pool, "v_pool", bf16=True)
+        ks = vs = C.c_void_p(None)
+    st = load().pa_decode_planned(
+        _ptr(out, "out", bf16=True), _ptr(q, "q", bf16=True), kp, vp_, ks, vs,
+        _ptr(block_tables, "block_tables", dtype=torch.int32), _ptr(context_lens, "context_lens", dtype=torch.int32),
+        float(scale), n_heads, n_kv_heads, head_dim, block_size, n_seqs, block_tables.shape[1],
+        int(max_context_len), num_blocks, int(window), int(partition_tokens),
+        _ptr(items, "items", dtype=torch.int32), items.shape[0], ws_ptr, ws_bytes, _stream(stream))
+    check("pa_decode_planned", st)
+
+
 def pa_copy_blocks(k_pool, v_pool, block_mapping, stream=None) -> None:
     """block_mapping int64 [n][2] (src, dst) on the device: dst block := src block.
     The pools may be bf16 or fp8 (uint8 E4M3 codes); the element size is read

@@ -28,6 +28,7 @@ PA_DEVERR_PAIR = 8
 PA_DEVERR_CONTEXT = 16
 PA_DEVERR_LAYOUT = 32
 PA_DEVERR_RANGE = 64
+PA_DEVERR_PLAN = 128
 
 vp = C.c_void_p
 i32 = C.c_int
@@ -57,6 +58,9 @@ SIGNATURES = {
     "pa_reshape_and_cache_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     "pa_decode_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32,
                             i32, i32, vp, C.c_size_t, vp]),
+    "pa_decode_plan": (i32, [vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, i32]),
+    "pa_decode_planned": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32, i32,
+                                i32, i32, i32, vp, i32, vp, C.c_size_t, vp]),
     "pa_prefill_paged": (i32, [vp, vp, vp, vp, vp, vp, vp, C.c_float, i32, i32, i32, i32, i32, i32,
                                i32, i32, vp]),
     "pa_prefill_workspace_bytes": (C.c_size_t, [i32, i32, i32, i32, i32]),

@@ -6,6 +6,7 @@ import os
 import random
 import re
 
+import numpy as np
 import pytest
 
 from oracle.block_manager import BlockManagerError, BlockManagerModel, OutOfBlocks
@@ -406,3 +407,67 @@ def test_default_partition_tokens_without_a_device(capi):
     assert capi.pa_decode_partition_tokens(4, 6, 4, 128, 100, -1, 2) == -1
     assert capi.pa_decode_partition_tokens(4, 4, 4, 96, 100, -1, 2) == -2
     assert capi.pa_decode_partition_tokens(4, 4, 4, 128, 100, -1, 3) == -1
+
+
+def _plan_items_model(ctx, Hk, part_blocks, max_blocks, max_parts, window):
+    """The decode plan restated: every (partition, kv head, sequence) item
+    the partition kernels run (a sequence without partitions keeps p = 0),
+    longest partition first, (sequence, kv head, partition) order within a
+    length."""
+    items = []
+    for b, c in enumerate(ctx):
+        np_, last = 0, 0
+        if c > 0:
+            nblk = (c + 15) // 16
+            bf = (max(0, c - 1 - window) if window >= 0 else 0) // 16
+            np_ = (nblk - bf + part_blocks - 1) // part_blocks
+            if nblk > max_blocks or np_ > max_parts:
+                nblk = min(nblk, max_blocks)
+                bf = min(bf, nblk)
+                np_ = min((nblk - bf + part_blocks - 1) // part_blocks, max_parts)
+                nblk = min(nblk, bf + np_ * part_blocks)
+            if np_ > 0:
+                last = (nblk - bf) - (np_ - 1) * part_blocks
+        if np_ <= 0:
+            np_, last = 1, 0
+        for kh in range(Hk):
+            for p in range(np_):
+                items.append((p, kh, b, part_blocks if p + 1 < np_ else last))
+    items.sort(key=lambda t: -t[3])   # stable
+    return [t[:3] for t in items]
+
+
+@pytest.mark.parametrize("window", [-1, 300])
+def test_decode_plan_matches_model(capi, window):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is visible: the default partition size depends on its SM count")
+    import paged_kv_cache_59_gb300 as pk
+    rng = np.random.default_rng(5)
+    for n_seqs, Hk, H in [(1, 1, 1), (7, 8, 32), (64, 8, 32), (33, 2, 16)]:
+        ctx = [int(c) for c in rng.integers(0, 4000, n_seqs)]
+        ctx[0] = 0                                       # an empty sequence keeps one item
+        max_ctx = max(ctx) + 5
+        max_blocks = (max_ctx + 15) // 16
+        items = pk.pa_decode_plan(ctx, H, Hk, 128, max_blocks, max_ctx, 1 << 20, window=window)
+        pt = pk.pa_decode_partition_tokens(n_seqs, H, Hk, 128, max_ctx, window)   # 512, or 1024 at group 8
+        max_parts = (max_ctx + pt - 1) // pt
+        if window >= 0:
+            max_parts = min(max_parts, ((window + 31) // 16 + pt // 16 - 1) // (pt // 16))
+        want = _plan_items_model(ctx, Hk, pt // 16, max_blocks, max_parts, window)
+        assert [tuple(int(v) for v in r[:3]) for r in items] == want
+        assert (items[:, 3] == 0).all()
+
+
+def test_decode_plan_errors(capi):
+    ctx = (C.c_int32 * 3)(100, 2000, 5)
+    buf = (C.c_int32 * 4096)()
+    n = capi.pa_decode_plan(ctx, 3, 32, 8, 128, 200, 2000, 4096, -1, 2, 0, None, 0)
+    assert n > 0
+    assert capi.pa_decode_plan(ctx, 3, 32, 8, 128, 200, 2000, 4096, -1, 2, 0, buf, n - 1) == -8   # capacity
+    assert capi.pa_decode_plan(ctx, 3, 32, 8, 128, 200, 2000, 4096, -1, 2, 0, buf, n) == n
+    assert capi.pa_decode_plan(ctx, 3, 32, 8, 96, 200, 2000, 4096, -1, 2, 0, buf, n) == -2      # head_dim
+    assert capi.pa_decode_plan(ctx, 3, 32, 6, 128, 200, 2000, 4096, -1, 2, 0, buf, n) == -1     # 32 % 6
+    assert capi.pa_decode_plan(ctx, 3, 32, 8, 128, 200, 2000, 4096, -1, 3, 0, buf, n) == -1     # elem_bytes
+    assert capi.pa_decode_plan(ctx, 3, 32, 8, 128, 200, 2000, 4096, -1, 2, 100, buf, n) == -1   # not a multiple of 64
+    assert capi.pa_decode_plan(None, 3, 32, 8, 128, 200, 2000, 4096, -1, 2, 0, buf, n) == -1
