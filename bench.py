@@ -501,11 +501,12 @@ def run_ours(args):
             "sum_context_tokens": sum_ctx, "distinct_cached_tokens_read": uniq_tok,
             "max_context": max_ctx, "num_blocks": wl.num_blocks,
             "kv_bytes_per_step": kv_bytes,
-            "step": ("pa_reshape_and_cache_fp8 (1 new token/seq, encoded) + pa_decode_fp8 (partition "
-                     "kernel + split-K merge)" if fp8 else
-                     f"pa_reshape_and_cache (1 new token/seq) + pa_decode_window (window {window})"
-                     if window is not None else
-                     "pa_reshape_and_cache (1 new token/seq) + pa_decode (partition kernel + split-K merge)"),
+            "step": (("pa_reshape_and_cache_fp8 (1 new token/seq, encoded) + pa_decode_fp8 (partition "
+                      "kernel + split-K merge)" if fp8 else
+                      f"pa_reshape_and_cache (1 new token/seq) + pa_decode_window (window {window})"
+                      if window is not None else
+                      "pa_reshape_and_cache (1 new token/seq) + pa_decode (partition kernel + split-K merge)")
+                     + ("; the decode as pa_decode_planned" if plan_host is not None else "")),
             "l2": f"no flush: the KV stream ({kv_bytes / 1e6:.0f} MB/step) exceeds the 129 MB L2",
             "partition_tokens": pt or pk.pa_decode_partition_tokens(
                 B, H, Hk, D, max_ctx, window if window is not None else -1, eb),
